@@ -1,0 +1,331 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each pin takes the oracle module as an argument so that the mutation test can
+run the same pins against copies of the oracle with a planted mistake.  A pin
+raises AssertionError when the oracle disagrees with:
+
+* the published format tables (bf16, OCP FP4 E2M1, OCP FP8 E4M3) kept as text
+  fixtures under tests/golden/,
+* closed forms (zero router weights, silu at ln 3, saturated silu),
+* library routines for special cases (torch fp64 matmul / silu for a dense
+  SwiGLU MLP, scipy softmax for top_k = E, numpy's stable argsort for the
+  grouping),
+* brute force over all k-subsets on tiny routers,
+* exact invariants (token-order equivariance, exact scaling by 2).
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            code, val = line.split()
+            rows.append((int(code, 16), val))
+    return rows
+
+
+def _val(s):
+    if s == "nan":
+        return float("nan")
+    if s == "-0":
+        return -0.0
+    return float(Fraction(s))
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_round(a):
+    """Round fp32 values to bf16 bit patterns (nearest even) -- builds inputs."""
+    b = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def _rand_bf16(rng, shape, std):
+    return _bf16_round(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
+
+
+# ------------------------------------------------------------------ formats
+
+def pin_bf16_table(o):
+    for code, val in _read_table("bf16_bits.txt"):
+        got = o.bf16_to_f64(np.array([code], dtype=np.uint16))[0]
+        assert got == _val(val), (hex(code), got, val)
+
+
+def pin_e2m1_table(o):
+    for code, val in _read_table("e2m1_codes.txt"):
+        got = o.e2m1_to_f64(np.array([code]))[0]
+        exp = _val(val)
+        assert got == exp and math.copysign(1, got) == math.copysign(1, exp), (hex(code), got, val)
+
+
+def pin_e4m3_table(o):
+    for code, val in _read_table("e4m3_codes.txt"):
+        got = o.e4m3_to_f64(np.array([code]))[0]
+        exp = _val(val)
+        if math.isnan(exp):
+            assert math.isnan(got), hex(code)
+        else:
+            assert got == exp and math.copysign(1, got) == math.copysign(1, exp), (hex(code), got, val)
+
+
+def pin_nvfp4_layout(o):
+    """Element k of a row sits in byte k//2 (low nibble for even k) and uses
+    scale k//16; values from the two format tables times the global scale."""
+    e2m1 = {c: _val(v) for c, v in _read_table("e2m1_codes.txt")}
+    e4m3 = {c: _val(v) for c, v in _read_table("e4m3_codes.txt")}
+    rng = _rng(7)
+    E, R, K = 2, 3, 64
+    codes = rng.integers(0, 256, size=(E, R, K // 2), dtype=np.uint8)
+    scale_codes = np.array([c for c in e4m3 if not math.isnan(e4m3[c])], dtype=np.uint8)
+    scales = rng.choice(scale_codes, size=(E, R, K // 16)).astype(np.uint8)
+    glob = np.array([0.75, 1.0 / 3.0], dtype=np.float32)
+    W = o.nvfp4_dequant(codes, scales, glob)
+    assert W.shape == (E, R, K)
+    for e in range(E):
+        for r in range(R):
+            for k in range(K):
+                byte = int(codes[e, r, k // 2])
+                nib = (byte & 0xF) if k % 2 == 0 else (byte >> 4)
+                exp = e2m1[nib] * e4m3[int(scales[e, r, k // 16])] * float(glob[e])
+                assert W[e, r, k] == exp, (e, r, k, W[e, r, k], exp)
+
+
+# ------------------------------------------------------------------ router
+
+def pin_router_zero_gate(o):
+    """All-zero gate weights give equal logits: experts 0..k-1 in index order,
+    each with weight exactly 1/k (closed form)."""
+    T, H, E, k = 3, 16, 6, 4
+    x = o.bf16_to_f64(_rand_bf16(_rng(1), (T, H), 1.0))
+    gw = np.zeros((E, H))
+    _, idx, w = o.route(x, gw, None, k)
+    assert (idx == np.arange(k)[None, :]).all(), idx
+    assert np.all(w == 1.0 / k), w
+
+
+def pin_router_bias_only(o):
+    """Zero gate weights plus a bias: the logits are the bias, so the ranking is
+    numpy's stable argsort of -bias and the weights are scipy's softmax of the
+    selected biases."""
+    from scipy.special import softmax as sp_softmax
+    T, H, E, k = 2, 8, 7, 3
+    bias = np.array([0.3, -1.0, 2.5, 0.3, 1.25, -0.5, 2.0], dtype=np.float32)
+    x = o.bf16_to_f64(_rand_bf16(_rng(2), (T, H), 1.0))
+    _, idx, w = o.route(x, np.zeros((E, H)), bias, k)
+    exp_idx = np.argsort(-bias.astype(np.float64), kind="stable")[:k]
+    for t in range(T):
+        assert (idx[t] == exp_idx).all(), (idx[t], exp_idx)
+        assert np.allclose(w[t], sp_softmax(bias[exp_idx].astype(np.float64)), rtol=0, atol=1e-15)
+
+
+def pin_router_brute_force(o):
+    """Tiny routers: the selected set is the k-subset with the largest logit
+    sum (checked over all subsets), slots are ordered by descending logit, the
+    weights equal exp(l_s)/sum exp(l_sel) evaluated without max subtraction,
+    and the logits equal torch's fp64 matmul."""
+    import torch
+    rng = _rng(3)
+    for trial in range(12):
+        T = int(rng.integers(1, 5))
+        H = int(rng.integers(2, 24))
+        E = int(rng.integers(2, 9))
+        k = int(rng.integers(1, E + 1))
+        x = o.bf16_to_f64(_rand_bf16(rng, (T, H), 1.0))
+        gw = o.bf16_to_f64(_rand_bf16(rng, (E, H), 0.5))
+        bias = (rng.standard_normal(E).astype(np.float32) * 0.1) if trial % 2 else None
+        l, idx, w = o.route(x, gw, bias, k)
+        ref_l = (torch.from_numpy(x) @ torch.from_numpy(gw).T).numpy()
+        if bias is not None:
+            ref_l = ref_l + bias.astype(np.float64)[None, :]
+        assert np.allclose(l, ref_l, rtol=1e-12, atol=1e-12)
+        for t in range(T):
+            best = max(itertools.combinations(range(E), k), key=lambda c: sum(ref_l[t, e] for e in c))
+            exp_order = sorted(best, key=lambda e: -ref_l[t, e])
+            assert list(idx[t]) == exp_order, (trial, t, idx[t], exp_order)
+            den = sum(math.exp(ref_l[t, e]) for e in exp_order)
+            for s, e in enumerate(exp_order):
+                assert abs(w[t, s] - math.exp(ref_l[t, e]) / den) <= 1e-14, (trial, t, s)
+
+
+def pin_router_exact_ties(o):
+    """Two identical gate rows tie exactly; the lower expert index wins."""
+    rng = _rng(4)
+    T, H, E, k = 4, 32, 8, 3
+    x = o.bf16_to_f64(_rand_bf16(rng, (T, H), 1.0))
+    gw = o.bf16_to_f64(_rand_bf16(rng, (E, H), 0.05))
+    gw[6] = gw[2]
+    # make experts 2 and 6 the two largest logits for every token
+    gw[2] = gw[6] = np.sign(x[0]) * 0.5
+    x[:] = np.abs(x) * np.sign(x[0])[None, :]
+    _, idx, w = o.route(x, gw, None, k)
+    for t in range(T):
+        assert idx[t, 0] == 2 and idx[t, 1] == 6, idx[t]
+        assert w[t, 0] == w[t, 1]
+
+
+def pin_topk_all_is_softmax(o):
+    """With top_k = E the weights are the full softmax (scipy) in rank order."""
+    from scipy.special import softmax as sp_softmax
+    rng = _rng(5)
+    T, H, E = 5, 40, 6
+    x = o.bf16_to_f64(_rand_bf16(rng, (T, H), 1.0))
+    gw = o.bf16_to_f64(_rand_bf16(rng, (E, H), 0.1))
+    l, idx, w = o.route(x, gw, None, E)
+    p = sp_softmax(l, axis=1)
+    for t in range(T):
+        assert np.allclose(w[t], p[t, idx[t]], rtol=0, atol=1e-15)
+        assert abs(w[t].sum() - 1.0) <= 1e-15
+
+
+# ------------------------------------------------------------------ grouping
+
+def pin_permute_stable_argsort(o):
+    """Counts = bincount, offsets = exclusive cumsum, perm = numpy's stable
+    argsort of the flat expert ids, inv_perm its inverse."""
+    rng = _rng(6)
+    for T, k, E in ((1, 1, 1), (7, 2, 5), (33, 4, 16), (64, 8, 128)):
+        idx = rng.integers(0, E, size=(T, k)).astype(np.int32)
+        counts, offsets, perm, inv_perm = o.permute(idx, E)
+        flat = idx.reshape(-1)
+        assert (counts == np.bincount(flat, minlength=E)).all()
+        assert (offsets == np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))])).all()
+        assert (perm == np.argsort(flat, kind="stable")).all()
+        assert (inv_perm[perm] == np.arange(T * k)).all()
+
+
+# ------------------------------------------------------------------ experts
+
+def pin_silu_closed_forms(o):
+    """sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4, silu(0) = 0, and silu(z)
+    equals z to within z*e^-z for large z and vanishes for large -z."""
+    ln3 = math.log(3.0)
+    z = np.array([0.0, ln3, -ln3, 40.0, -40.0])
+    s = o.silu(z)
+    assert s[0] == 0.0
+    assert abs(s[1] - 0.75 * ln3) <= 1e-15
+    assert abs(s[2] + 0.25 * ln3) <= 1e-15
+    assert abs(s[3] - 40.0) <= 40.0 * math.exp(-40.0) * 2
+    assert abs(s[4]) <= 40.0 * math.exp(-40.0) * 2
+
+
+def _dense_swiglu_torch(x, gu, dn):
+    import torch
+    X = torch.from_numpy(x)
+    I = gu.shape[0] // 2
+    g = X @ torch.from_numpy(gu[:I]).T
+    u = X @ torch.from_numpy(gu[I:]).T
+    return (torch.nn.functional.silu(g) * u @ torch.from_numpy(dn).T).numpy()
+
+
+def pin_single_expert_dense(o):
+    """E = 1, top_k = 1: the layer is a dense SwiGLU MLP (torch fp64)."""
+    rng = _rng(8)
+    T, H, I = 6, 48, 20
+    xb = _rand_bf16(rng, (T, H), 1.0)
+    gb = _rand_bf16(rng, (1, H), 0.1)
+    gub = _rand_bf16(rng, (1, 2 * I, H), 0.2)
+    dnb = _rand_bf16(rng, (1, H, I), 0.2)
+    res = o.forward(xb, gb, None, 1, o.ExpertWeights(gub, dnb))
+    ref = _dense_swiglu_torch(o.bf16_to_f64(xb), o.bf16_to_f64(gub[0]), o.bf16_to_f64(dnb[0]))
+    assert np.allclose(res["out"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert (res["w"] == 1.0).all()
+
+
+def pin_topk_all_mixture(o):
+    """top_k = E: the output is the softmax-weighted sum of every expert's MLP
+    (torch fp64 softmax and einsum)."""
+    import torch
+    rng = _rng(9)
+    T, H, I, E = 5, 32, 12, 4
+    xb = _rand_bf16(rng, (T, H), 1.0)
+    gb = _rand_bf16(rng, (E, H), 0.2)
+    gub = _rand_bf16(rng, (E, 2 * I, H), 0.2)
+    dnb = _rand_bf16(rng, (E, H, I), 0.2)
+    res = o.forward(xb, gb, None, E, o.ExpertWeights(gub, dnb))
+    x = o.bf16_to_f64(xb)
+    p = torch.softmax(torch.from_numpy(x) @ torch.from_numpy(o.bf16_to_f64(gb)).T, dim=1)
+    ys = torch.stack([torch.from_numpy(_dense_swiglu_torch(x, o.bf16_to_f64(gub[e]), o.bf16_to_f64(dnb[e])))
+                      for e in range(E)], dim=1)  # [T, E, H]
+    ref = torch.einsum("te,teh->th", p, ys).numpy()
+    assert np.allclose(res["out"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def pin_hand_case(o):
+    """H = 2, I = 1, E = 2, top_k = 2, worked by hand.
+
+    x = (1, 0); gate rows (1, 0) and (2, 0) give logits 1 and 2, so expert 1 is
+    slot 0 with weight e^2/(e+e^2) = e/(1+e) and expert 0 is slot 1.
+    Expert 1: gate row (40, 0), up row (3, 0), down column (2, -1):
+      g = 40, u = 3, silu(40) = 40 to within 40e^-40, so y = (240, -120).
+    Expert 0: gate row (0, 0) makes silu(g) = 0, so y = 0.
+    out = e/(1+e) * (240, -120)."""
+    f = o.bf16_to_f64  # noqa: F841  (inputs below are bf16-exact integers)
+    xb = _bf16_round(np.array([[1.0, 0.0]], dtype=np.float32))
+    gb = _bf16_round(np.array([[1.0, 0.0], [2.0, 0.0]], dtype=np.float32))
+    gu = np.array([[[0.0, 0.0], [5.0, 0.0]], [[40.0, 0.0], [3.0, 0.0]]], dtype=np.float32)
+    dn = np.array([[[7.0], [7.0]], [[2.0], [-1.0]]], dtype=np.float32)
+    res = o.forward(xb, gb, None, 2, o.ExpertWeights(_bf16_round(gu), _bf16_round(dn)))
+    assert list(res["idx"][0]) == [1, 0]
+    c = math.e / (1.0 + math.e)
+    exp = np.array([240.0 * c, -120.0 * c])
+    assert np.allclose(res["out"][0], exp, rtol=1e-14, atol=0), (res["out"], exp)
+    assert abs(res["w"][0, 0] - c) <= 1e-15 and abs(res["w"][0, 1] - (1 - c)) <= 1e-15
+
+
+def _small_layer(rng, T=9, H=24, I=8, E=6, k=3):
+    return dict(xb=_rand_bf16(rng, (T, H), 1.0), gb=_rand_bf16(rng, (E, H), 0.3),
+                gub=_rand_bf16(rng, (E, 2 * I, H), 0.2), dnb=_rand_bf16(rng, (E, H, I), 0.2), k=k)
+
+
+def pin_token_order_equivariance(o):
+    """Permuting the tokens permutes the output rows exactly."""
+    rng = _rng(10)
+    L = _small_layer(rng)
+    a = o.forward(L["xb"], L["gb"], None, L["k"], o.ExpertWeights(L["gub"], L["dnb"]))["out"]
+    p = rng.permutation(L["xb"].shape[0])
+    b = o.forward(L["xb"][p], L["gb"], None, L["k"], o.ExpertWeights(L["gub"], L["dnb"]))["out"]
+    assert np.array_equal(a[p], b)
+
+
+def pin_down_scaling(o):
+    """Doubling w_down (exact in bf16) doubles the output exactly; the routing
+    does not depend on the expert weights."""
+    rng = _rng(11)
+    L = _small_layer(rng)
+    a = o.forward(L["xb"], L["gb"], None, L["k"], o.ExpertWeights(L["gub"], L["dnb"]))
+    dn2 = _bf16_round(o.bf16_to_f64(L["dnb"]).astype(np.float32) * 2)
+    b = o.forward(L["xb"], L["gb"], None, L["k"], o.ExpertWeights(L["gub"], dn2))
+    assert np.array_equal(2 * a["out"], b["out"])
+    assert np.array_equal(a["idx"], b["idx"])
+
+
+def pin_sampled_tokens(o):
+    """Asking for a subset of tokens returns exactly those rows of the full
+    output, and the routing of the whole batch is unchanged."""
+    rng = _rng(12)
+    L = _small_layer(rng)
+    W = o.ExpertWeights(L["gub"], L["dnb"])
+    full = o.forward(L["xb"], L["gb"], None, L["k"], W)
+    sub = o.forward(L["xb"], L["gb"], None, L["k"], W, tokens=[7, 2])
+    assert np.array_equal(sub["out"], full["out"][[7, 2]])
+    assert np.array_equal(sub["perm"], full["perm"])
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

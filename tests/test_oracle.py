@@ -1,0 +1,174 @@
+"""CPU tests of the oracle against its pins, plus planted-mistake checks.
+
+The second half loads fresh copies of the oracle module, plants one plausible
+mistake in each (a wrong sign, a dropped term, a swapped operand, a wrong
+index or layout) and checks that at least one pin catches it, so that the
+pins are known to constrain every step of the oracle.
+"""
+import importlib.util
+import os
+import sys
+
+import numpy as np
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+import oracle_pins  # noqa: E402
+
+from oracle import moe_oracle  # noqa: E402
+
+ORACLE_FILE = moe_oracle.__file__
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_pin(pin):
+    pin(moe_oracle)
+
+
+def _fresh_copy(tag):
+    spec = importlib.util.spec_from_file_location(f"oracle_mutant_{tag}", ORACLE_FILE)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _mut_silu_sign(m):
+    m.silu = lambda z: z / (1.0 + np.exp(z))
+
+
+def _mut_no_renorm(m):
+    orig_softmax = m.softmax
+
+    def route(x, gate_w, bias, top_k):
+        l = m.router_logits(x, gate_w, bias)
+        p = orig_softmax(l)
+        idx = np.stack([m.topk_order(l[t], top_k) for t in range(l.shape[0])]).astype(np.int32)
+        w = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+        return l, idx, w
+    m.route = route
+
+
+def _mut_tie_high_index(m):
+    m.topk_order = lambda l_row, k: np.lexsort((-np.arange(l_row.shape[0]), -l_row))[:k]
+
+
+def _mut_topk_smallest(m):
+    m.topk_order = lambda l_row, k: np.lexsort((np.arange(l_row.shape[0]), l_row))[:k]
+
+
+def _mut_gate_up_swapped(m):
+    def expert_swiglu(X, w_gu, w_dn):
+        I = w_gu.shape[0] // 2
+        return np.stack([w_dn @ (m.silu(w_gu[I:] @ x) * (w_gu[:I] @ x)) for x in X])
+    m.expert_swiglu = expert_swiglu
+
+
+def _mut_down_layout(m):
+    def expert_swiglu(X, w_gu, w_dn):
+        I = w_gu.shape[0] // 2
+        return np.stack([(m.silu(w_gu[:I] @ x) * (w_gu[I:] @ x)) @ w_dn.reshape(I, -1) for x in X])
+    m.expert_swiglu = expert_swiglu
+
+
+def _mut_bias_sign(m):
+    orig = m.router_logits
+
+    def router_logits(x, gate_w, bias):
+        return orig(x, gate_w, None if bias is None else -np.asarray(bias))
+    m.router_logits = router_logits
+
+
+def _mut_logit_drop_last_h(m):
+    orig = m.router_logits
+
+    def router_logits(x, gate_w, bias):
+        return orig(x[:, :-1], gate_w[:, :-1], bias)
+    m.router_logits = router_logits
+
+
+def _mut_perm_unstable(m):
+    orig = m.permute
+
+    def permute(idx, E):
+        counts, offsets, perm, inv = orig(idx, E)
+        perm = perm.copy()
+        for e in range(E):
+            perm[offsets[e]:offsets[e + 1]] = perm[offsets[e]:offsets[e + 1]][::-1]
+        inv = np.empty_like(perm)
+        inv[perm] = np.arange(perm.shape[0])
+        return counts, offsets, perm, inv
+    m.permute = permute
+
+
+def _mut_combine_drops_slot(m):
+    # the combine loses the last slot's contribution
+    orig_route = m.route
+
+    def route(x, gate_w, bias, top_k):
+        l, idx, w = orig_route(x, gate_w, bias, top_k)
+        if top_k > 1:
+            w = w.copy()
+            w[:, -1] = 0.0
+        return l, idx, w
+    m.route = route
+
+
+def _mut_bf16_shift(m):
+    m.bf16_to_f64 = lambda bits: (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32)
+                                  << np.uint32(15)).view(np.float32).astype(np.float64)
+
+
+def _mut_e2m1_mantissa(m):
+    def e2m1_to_f64(code):
+        c = np.asarray(code, dtype=np.int64) & 0xF
+        sign = np.where(c >> 3, -1.0, 1.0)
+        e = (c >> 1) & 3
+        mm = c & 1
+        mag = np.where(e == 0, 0.5 * mm, np.ldexp(1.0 + mm, e - 1))
+        return sign * mag
+    m.e2m1_to_f64 = e2m1_to_f64
+
+
+def _mut_e4m3_bias(m):
+    orig = m.e4m3_to_f64
+    m.e4m3_to_f64 = lambda b: orig(b) * 0.5
+
+
+def _mut_nibble_order(m):
+    orig = m.nvfp4_dequant
+
+    def nvfp4_dequant(codes, scales, glob):
+        c = np.asarray(codes, dtype=np.uint8)
+        swapped = ((c & 0xF) << 4) | (c >> 4)
+        return orig(swapped.astype(np.uint8), scales, glob)
+    m.nvfp4_dequant = nvfp4_dequant
+
+
+def _mut_scale_block(m):
+    orig = m.nvfp4_dequant
+
+    def nvfp4_dequant(codes, scales, glob):
+        s = np.asarray(scales)
+        return orig(codes, s[:, :, ::-1].copy(), glob)
+    m.nvfp4_dequant = nvfp4_dequant
+
+
+def _mut_softmax_no_exp(m):
+    m.softmax = lambda l: (l - l.min(axis=-1, keepdims=True)) / (l - l.min(axis=-1, keepdims=True)).sum(
+        axis=-1, keepdims=True)
+
+
+MUTANTS = [v for k, v in sorted(globals().items()) if k.startswith("_mut_")]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__[5:])
+def test_pins_catch_planted_mistake(mutant):
+    m = _fresh_copy(mutant.__name__)
+    mutant(m)
+    failures = 0
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(m)
+        except Exception:
+            failures += 1
+    assert failures > 0, f"no pin caught mutant {mutant.__name__}"
