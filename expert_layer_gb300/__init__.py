@@ -1,0 +1,201 @@
+"""GB300-native Mixture-of-Experts FFN layer forward.
+
+Thin Python binding (ctypes) over the C ABI of ``libmoe_gb300.so``
+(``include/moe.h``).  The functions here only check and marshal arguments:
+every step of the layer runs in the library's CUDA kernels.  PyTorch supplies
+device memory and the current CUDA stream.  If the library has not been
+built, every call raises ``MoEError``; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["MoEError", "lib", "workspace_size", "alloc_workspace", "route", "permute", "forward",
+           "read_status", "read_diagnostics", "LIB_PATH"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_gb300.so")
+
+MOE_OK = 0
+
+
+class MoEError(RuntimeError):
+    pass
+
+
+class _NVFP4(ctypes.Structure):
+    _fields_ = [("gu_codes", ctypes.c_void_p), ("gu_scales", ctypes.c_void_p),
+                ("gu_global", ctypes.c_void_p), ("dn_codes", ctypes.c_void_p),
+                ("dn_scales", ctypes.c_void_p), ("dn_global", ctypes.c_void_p)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward": (_I, [_P, _P, _P, _P, _P, ctypes.POINTER(_NVFP4), _I, _I, _I, _I, _I, _P, _P, _P,
+                         _P, _SZ, _P]),
+    "moe_forward_profiled": (_I, [_P, _P, _P, _P, _P, ctypes.POINTER(_NVFP4), _I, _I, _I, _I, _I, _P,
+                                  _P, _P, _P, _SZ, _P, ctypes.POINTER(_P),
+                                  ctypes.POINTER(ctypes.c_int32)]),
+    "moe_read_status": (_I, [_P, _P]),
+    "moe_read_diagnostics": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "moe_error_string": (ctypes.c_char_p, [_I]),
+    "moe_version": (_I, []),
+}
+
+
+def lib():
+    """Load libmoe_gb300.so (raises MoEError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MoEError(f"{LIB_PATH} is missing: build it with `python -m expert_layer_gb300._build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        msg = lib().moe_error_string(rc).decode()
+        raise MoEError(f"{what} failed: {msg} ({rc})")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _want(t: torch.Tensor, dtype, shape, name):
+    if not isinstance(t, torch.Tensor):
+        raise MoEError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise MoEError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MoEError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise MoEError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise MoEError(f"{name} must be contiguous")
+
+
+def workspace_size(T: int, H: int, E: int, I: int, top_k: int) -> int:
+    return int(lib().moe_workspace_size(T, H, E, I, top_k))
+
+
+def alloc_workspace(T: int, H: int, E: int, I: int, top_k: int, device="cuda") -> torch.Tensor:
+    n = workspace_size(T, H, E, I, top_k)
+    if n == 0:
+        raise MoEError("unsupported shape")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def route(x, gate_w, bias, top_k, workspace=None, stream=None):
+    """Router: returns (topk_idx int32 [T,k], topk_w fp32 [T,k])."""
+    T, H = x.shape
+    E = gate_w.shape[0]
+    _want(x, torch.bfloat16, (T, H), "x")
+    _want(gate_w, torch.bfloat16, (E, H), "gate_w")
+    if bias is not None:
+        _want(bias, torch.float32, (E,), "bias")
+    if workspace is None:
+        workspace = alloc_workspace(max(T, 1), H, E, 128, top_k, x.device)
+    idx = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    rc = lib().moe_route(_ptr(x), _ptr(gate_w), _ptr(bias), T, H, E, top_k, _ptr(idx), _ptr(w),
+                         _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "moe_route")
+    return idx, w
+
+
+def permute(topk_idx, E, workspace=None, stream=None):
+    """Grouping: returns (counts [E], offsets [E+1], perm [S], inv_perm [S]), int32."""
+    T, k = topk_idx.shape
+    _want(topk_idx, torch.int32, (T, k), "topk_idx")
+    dev = topk_idx.device
+    if workspace is None:
+        workspace = alloc_workspace(max(T, 1), 128, E, 128, k, dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    rc = lib().moe_permute(_ptr(topk_idx), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+                           _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "moe_permute")
+    return counts, offsets, perm, inv
+
+
+def forward(x, gate_w, bias, w_gate_up, w_down, top_k, nvfp4_gate_up=None, nvfp4_down=None,
+            out=None, workspace=None, topk_idx=None, topk_w=None, stream=None):
+    """The MoE layer forward; returns out bf16 [T, H].
+
+    bf16 weights: w_gate_up [E, 2I, H], w_down [E, H, I].  NVFP4 weights: pass
+    ``nvfp4_gate_up`` / ``nvfp4_down`` objects with ``codes`` (uint8),
+    ``scales`` (uint8 e4m3) and ``glob`` (fp32 [E]) tensors and leave the bf16
+    weights None.  ``topk_idx`` / ``topk_w`` optionally receive the routing."""
+    T, H = x.shape
+    E = gate_w.shape[0]
+    _want(x, torch.bfloat16, (T, H), "x")
+    _want(gate_w, torch.bfloat16, (E, H), "gate_w")
+    if bias is not None:
+        _want(bias, torch.float32, (E,), "bias")
+    nv = None
+    if nvfp4_gate_up is not None:
+        if w_gate_up is not None or w_down is not None:
+            raise MoEError("pass either bf16 or NVFP4 expert weights, not both")
+        q, d = nvfp4_gate_up, nvfp4_down
+        I = q.codes.shape[1] // 2
+        _want(q.codes, torch.uint8, (E, 2 * I, H // 2), "gate_up codes")
+        _want(q.scales, torch.uint8, (E, 2 * I, H // 16), "gate_up scales")
+        _want(q.glob, torch.float32, (E,), "gate_up global")
+        _want(d.codes, torch.uint8, (E, H, I // 2), "down codes")
+        _want(d.scales, torch.uint8, (E, H, I // 16), "down scales")
+        _want(d.glob, torch.float32, (E,), "down global")
+        nv = _NVFP4(q.codes.data_ptr(), q.scales.data_ptr(), q.glob.data_ptr(), d.codes.data_ptr(),
+                    d.scales.data_ptr(), d.glob.data_ptr())
+    else:
+        I = w_gate_up.shape[1] // 2
+        _want(w_gate_up, torch.bfloat16, (E, 2 * I, H), "w_gate_up")
+        _want(w_down, torch.bfloat16, (E, H, I), "w_down")
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _want(out, torch.bfloat16, (T, H), "out")
+    if topk_idx is not None:
+        _want(topk_idx, torch.int32, (T, top_k), "topk_idx")
+    if topk_w is not None:
+        _want(topk_w, torch.float32, (T, top_k), "topk_w")
+    if workspace is None:
+        workspace = alloc_workspace(max(T, 1), H, E, I, top_k, x.device)
+    rc = lib().moe_forward(_ptr(x), _ptr(gate_w), _ptr(bias), _ptr(w_gate_up), _ptr(w_down),
+                           ctypes.byref(nv) if nv is not None else None, T, H, E, I, top_k,
+                           _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace),
+                           workspace.numel(), _stream(stream))
+    _check(rc, "moe_forward")
+    return out
+
+
+def read_status(workspace, stream=None) -> int:
+    """Synchronise and return the device status code of the last call."""
+    return int(lib().moe_read_status(_ptr(workspace), _stream(stream)))
+
+
+def read_diagnostics(workspace, stream=None) -> dict:
+    buf = (ctypes.c_int32 * 4)()
+    _check(lib().moe_read_diagnostics(_ptr(workspace), _stream(stream), buf), "moe_read_diagnostics")
+    return dict(num_active=buf[0], num_large=buf[1], router_flagged=buf[2], router_fallback=buf[3])

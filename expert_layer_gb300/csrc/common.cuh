@@ -1,0 +1,112 @@
+// Shared device helpers and the workspace layout of the MoE layer library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ----------------------------------------------------------------- status
+// Bits of the device status word kept in the workspace header.
+enum : int {
+  kStatusBadExpert = 1,   // moe_permute saw an expert id outside [0, E)
+  kStatusTimeout = 2,     // a bounded device-side wait gave up
+};
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+  int status;             // OR of kStatus* bits
+  int num_active;         // experts with at least one routed slot
+  int num_large;          // active experts served by the tensor-core path
+  int router_flagged;     // tokens whose ranking needed fp64 logits
+  int router_fallback;    // tokens that needed fp64 logits for every expert
+  int pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte slot");
+
+// Offsets (bytes) of every workspace region for one shape.
+struct WsLayout {
+  size_t hdr, xnorm, wnorm, logits, logits64, idx, w, counts, offsets, active, tiles, blk_cnt,
+      blk_base, lrank, perm, inv_perm, h, partial, total;
+  int nblk;               // 512-slot blocks of the grouping kernels
+  bool partial_f32;       // fp32 partials (else bf16)
+};
+
+constexpr int kPermBlock = 512;            // slots per grouping block
+constexpr size_t kPartialF32Limit = 32ull << 20;
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+inline WsLayout make_layout(long long T, long long H, long long E, long long I, long long k) {
+  WsLayout L{};
+  const long long S = T * k;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
+  L.nblk = (int)((S + kPermBlock - 1) / kPermBlock);
+  L.partial_f32 = (size_t)S * (size_t)H * 4 <= kPartialF32Limit;
+  L.hdr = take(sizeof(WsHeader));
+  L.xnorm = take(sizeof(float) * T);
+  L.wnorm = take(sizeof(float) * E);
+  L.logits = take(sizeof(float) * T * E);
+  L.logits64 = take(sizeof(double) * T * E);
+  L.idx = take(sizeof(int) * S);
+  L.w = take(sizeof(float) * S);
+  L.counts = take(sizeof(int) * E);
+  L.offsets = take(sizeof(int) * (E + 1));
+  L.active = take(sizeof(int) * E);
+  L.tiles = take(sizeof(int) * (2 * E + 2));
+  L.blk_cnt = take(sizeof(int) * (size_t)L.nblk * E);
+  L.blk_base = take(sizeof(int) * (size_t)L.nblk * E);
+  L.lrank = take(sizeof(int) * S);
+  L.perm = take(sizeof(int) * S);
+  L.inv_perm = take(sizeof(int) * S);
+  L.h = take(sizeof(uint16_t) * S * I);
+  L.partial = take((L.partial_f32 ? 4 : 2) * (size_t)S * H);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+__host__ __device__ inline T* ws_ptr(void* ws, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
+}
+
+// ----------------------------------------------------------------- numerics
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// mma.sync m16n8k16, bf16 inputs, fp32 accumulate (in place).
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void set_status(void* ws, int bit) {
+  atomicOr(&reinterpret_cast<WsHeader*>(ws)->status, bit);
+}
+
+}  // namespace moe

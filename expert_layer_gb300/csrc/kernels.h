@@ -1,0 +1,59 @@
+// Host-side launchers of the MoE layer kernels (one translation unit each).
+// Every launcher only enqueues on `stream`, adds the number of kernels it
+// launched to *launches (if non-null) and returns the launch error.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// router.cu -- logits, certified top-k, renormalised weights
+cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
+                         int E, int k, int32_t* idx, float* w, void* ws, const WsLayout& L,
+                         cudaStream_t stream, int* launches);
+
+// permute.cu -- histogram, exclusive scan, stable permutation, active list
+cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws,
+                           const WsLayout& L, int large_threshold, int tile_rows,
+                           cudaStream_t stream, int* launches);
+
+// stream_gemm.cu -- weight-streaming grouped GEMV/GEMM (mma.sync), bf16 or NVFP4 weights
+struct StreamGemmArgs {
+  // common
+  int T, H, E, I, k;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int32_t* active;     // active experts (ascending)
+  const int* num_active;     // device scalar
+  const int* num_large;      // device scalar: leading active experts served elsewhere (may be null)
+  // gate/up
+  const uint16_t* x;         // [T, H]
+  const uint16_t* w_gate_up; // [E, 2I, H] bf16 (or null)
+  const uint8_t* gu_codes;   // NVFP4 (or null)
+  const uint8_t* gu_scales;
+  const float* gu_global;
+  uint16_t* h;               // [S, I] bf16, grouped order
+  // down
+  const uint16_t* w_down;    // [E, H, I]
+  const uint8_t* dn_codes;
+  const uint8_t* dn_scales;
+  const float* dn_global;
+  const float* topk_w;       // [S]
+  void* partial;             // [S, H] fp32 or bf16, slot order
+  bool partial_f32;
+  int num_sms;
+};
+cudaError_t launch_stream_gate_up(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
+cudaError_t launch_stream_down(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
+
+// combine.cu -- out[t] = sum_s partial[t*k+s] in slot order
+cudaError_t launch_combine(const void* partial, bool partial_f32, int T, int H, int k,
+                           uint16_t* out, cudaStream_t stream, int* launches);
+
+}  // namespace moe

@@ -1,0 +1,253 @@
+// C ABI of the MoE layer library: argument checks, workspace layout, launch
+// sequence.  Nothing here allocates, synchronises or keeps state between
+// calls (moe_read_status is the one call that synchronises, by design).
+#include <limits.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(long long T, long long H, long long E, long long I, long long k) {
+  if (T < 0 || H <= 0 || E <= 0 || I <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+  if (k > E) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+  if (H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T * k >= (1ll << 31) || T * H >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int check_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
+  if (num_sms &&
+      cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                 \
+  do {                                \
+    const int _rc = (expr);           \
+    if (_rc != MOE_OK) return _rc;    \
+  } while (0)
+
+#define MOE_TRY_CUDA(expr)                                 \
+  do {                                                     \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA;        \
+  } while (0)
+
+int check_ptr(const void* p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(p)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+const char* moe_error_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: unsupported shape, alignment or device";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime or launch failure";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: a kernel found invalid data";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+    default: return "unknown moe_status";
+  }
+}
+
+size_t moe_workspace_size(int T, int H, int E, int I, int top_k) {
+  if (check_shape(T, H, E, I, top_k) != MOE_OK) return 0;
+  return make_layout(T, H, E, I, top_k).total;
+}
+
+int moe_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H, int E,
+              int top_k, int32_t* topk_idx, float* topk_w, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_shape(T, H, E, 128, top_k));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x));
+  MOE_TRY(check_ptr(gate_w));
+  MOE_TRY(check_ptr(topk_idx));
+  MOE_TRY(check_ptr(topk_w));
+  MOE_TRY(check_ptr(workspace));
+  if (bias && !aligned16(bias)) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = make_layout(T, H, E, 128, top_k);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device(nullptr));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s));
+  return cuda_status(
+      launch_route(x, gate_w, bias, T, H, E, top_k, topk_idx, topk_w, workspace, L, s, nullptr));
+}
+
+int moe_permute(const int32_t* topk_idx, int T, int E, int top_k, int32_t* counts,
+                int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_shape(T, 128, E, 128, top_k));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(topk_idx));
+  MOE_TRY(check_ptr(counts));
+  MOE_TRY(check_ptr(offsets));
+  MOE_TRY(check_ptr(perm));
+  MOE_TRY(check_ptr(inv_perm));
+  MOE_TRY(check_ptr(workspace));
+  const WsLayout L = make_layout(T, 128, E, 128, top_k);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device(nullptr));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s));
+  return cuda_status(launch_permute(topk_idx, T, E, top_k, counts, offsets, perm, inv_perm,
+                                    workspace, L, INT_MAX, 128, s, nullptr));
+}
+
+static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* bias,
+                        const uint16_t* w_gate_up, const uint16_t* w_down,
+                        const moe_nvfp4_weights* nvfp4, int T, int H, int E, int I, int top_k,
+                        uint16_t* out, int32_t* topk_idx, float* topk_w, void* workspace,
+                        size_t workspace_bytes, void* stream, void* const* events,
+                        int* launches) {
+  MOE_TRY(check_shape(T, H, E, I, top_k));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x));
+  MOE_TRY(check_ptr(gate_w));
+  MOE_TRY(check_ptr(out));
+  MOE_TRY(check_ptr(workspace));
+  if (bias && !aligned16(bias)) return MOE_ERR_UNSUPPORTED;
+  if (topk_idx && !aligned16(topk_idx)) return MOE_ERR_UNSUPPORTED;
+  if (topk_w && !aligned16(topk_w)) return MOE_ERR_UNSUPPORTED;
+  if (nvfp4) {
+    if (w_gate_up || w_down) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ptr(nvfp4->gu_codes));
+    MOE_TRY(check_ptr(nvfp4->gu_scales));
+    MOE_TRY(check_ptr(nvfp4->gu_global));
+    MOE_TRY(check_ptr(nvfp4->dn_codes));
+    MOE_TRY(check_ptr(nvfp4->dn_scales));
+    MOE_TRY(check_ptr(nvfp4->dn_global));
+  } else {
+    MOE_TRY(check_ptr(w_gate_up));
+    MOE_TRY(check_ptr(w_down));
+  }
+  const WsLayout L = make_layout(T, H, E, I, top_k);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  int num_sms = 0;
+  MOE_TRY(check_device(&num_sms));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  int32_t* idx = topk_idx ? topk_idx : ws_ptr<int32_t>(workspace, L.idx);
+  float* w = topk_w ? topk_w : ws_ptr<float>(workspace, L.w);
+  int32_t* counts = ws_ptr<int32_t>(workspace, L.counts);
+  int32_t* offsets = ws_ptr<int32_t>(workspace, L.offsets);
+  int32_t* perm = ws_ptr<int32_t>(workspace, L.perm);
+  int32_t* inv_perm = ws_ptr<int32_t>(workspace, L.inv_perm);
+  WsHeader* hdr = ws_ptr<WsHeader>(workspace, L.hdr);
+
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+  };
+  MOE_TRY_CUDA(mark(0));
+  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s));
+  MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches));
+  MOE_TRY_CUDA(mark(1));
+  MOE_TRY_CUDA(launch_permute(idx, T, E, top_k, counts, offsets, perm, inv_perm, workspace, L,
+                              INT_MAX, 128, s, launches));
+  MOE_TRY_CUDA(mark(2));
+
+  StreamGemmArgs a{};
+  a.T = T; a.H = H; a.E = E; a.I = I; a.k = top_k;
+  a.counts = counts; a.offsets = offsets; a.perm = perm;
+  a.active = ws_ptr<int32_t>(workspace, L.active);
+  a.num_active = &hdr->num_active;
+  a.num_large = &hdr->num_large;
+  a.x = x;
+  a.w_gate_up = w_gate_up;
+  a.w_down = w_down;
+  if (nvfp4) {
+    a.gu_codes = nvfp4->gu_codes; a.gu_scales = nvfp4->gu_scales; a.gu_global = nvfp4->gu_global;
+    a.dn_codes = nvfp4->dn_codes; a.dn_scales = nvfp4->dn_scales; a.dn_global = nvfp4->dn_global;
+  }
+  a.h = ws_ptr<uint16_t>(workspace, L.h);
+  a.topk_w = w;
+  a.partial = ws_ptr<void>(workspace, L.partial);
+  a.partial_f32 = L.partial_f32;
+  a.num_sms = num_sms;
+  MOE_TRY_CUDA(launch_stream_gate_up(a, s, launches));
+  MOE_TRY_CUDA(mark(3));
+  MOE_TRY_CUDA(launch_stream_down(a, s, launches));
+  MOE_TRY_CUDA(mark(4));
+  MOE_TRY_CUDA(launch_combine(a.partial, L.partial_f32, T, H, top_k, out, s, launches));
+  MOE_TRY_CUDA(mark(5));
+  return MOE_OK;
+}
+
+int moe_forward(const uint16_t* x, const uint16_t* gate_w, const float* bias,
+                const uint16_t* w_gate_up, const uint16_t* w_down, const moe_nvfp4_weights* nvfp4,
+                int T, int H, int E, int I, int top_k, uint16_t* out, int32_t* topk_idx,
+                float* topk_w, void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_impl(x, gate_w, bias, w_gate_up, w_down, nvfp4, T, H, E, I, top_k, out, topk_idx,
+                      topk_w, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+int moe_forward_profiled(const uint16_t* x, const uint16_t* gate_w, const float* bias,
+                         const uint16_t* w_gate_up, const uint16_t* w_down,
+                         const moe_nvfp4_weights* nvfp4, int T, int H, int E, int I, int top_k,
+                         uint16_t* out, int32_t* topk_idx, float* topk_w, void* workspace,
+                         size_t workspace_bytes, void* stream, void* const* events,
+                         int32_t* kernels_launched) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  int n = 0;
+  const int rc = forward_impl(x, gate_w, bias, w_gate_up, w_down, nvfp4, T, H, E, I, top_k, out,
+                              topk_idx, topk_w, workspace, workspace_bytes, stream, events, &n);
+  if (kernels_launched) *kernels_launched = n;
+  return rc;
+}
+
+int moe_read_status(const void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (st & kStatusTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (st & kStatusBadExpert) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+int moe_read_diagnostics(const void* workspace, void* stream, int32_t* out4) {
+  if (!workspace || !out4) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  out4[0] = h.num_active;
+  out4[1] = h.num_large;
+  out4[2] = h.router_flagged;
+  out4[3] = h.router_fallback;
+  return MOE_OK;
+}
+
+}  // extern "C"

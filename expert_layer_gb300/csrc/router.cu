@@ -1,0 +1,531 @@
+// Router: "MoE gate" GEMV + "topk" with renormalised weights (page "Decode
+// 吞吐专项实验分析报告", section "下一步 profiling 方向", items 2-3).
+//
+// logit[t,e] = sum_h x[t,h] * gate_w[e,h] (+ bias[e]).  The ranking key is the
+// logit (larger first, lower expert index first on equal logits); the weights
+// are the softmax over all E experts renormalised over the k selected, which
+// equals exp(l_s - l_max) / sum_{s'} exp(l_s' - l_max) over the selected set.
+//
+// Certified ranking.  Logits accumulate in fp32.  bf16 x bf16 products are
+// exact in fp32 (barring underflow, bounded separately), so the only error is
+// the summation: with every product passing through at most n roundings the
+// error is at most gamma_n * sum_h |x_h w_h| <= gamma_n * ||x|| * ||w_e||
+// (Cauchy-Schwarz), gamma_n = n*u/(1-n*u), u = 2^-24.  Per token we take the
+// uniform bound delta = gamma_n ||x|| max_e ||w_e|| (1 + 2^-10) + 2^-22 max|l|
+// + H 2^-149.  Adjacent ranks closer than 2*delta inside the top region are
+// recomputed in fp64 (exact products, ~1e-16 relative sums) and re-ranked, so
+// the selected experts and their order equal those of the exact logits.
+#include <float.h>
+#include <limits.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kCandCap = 64;  // candidates a warp can hold while certifying
+
+__host__ __device__ inline float gamma_bound(int n) {
+  const double u = 5.9604644775390625e-08;  // 2^-24
+  return (float)(n * u / (1.0 - n * u));
+}
+
+// Exact-product fp64 dot of two bf16 rows of length H (H % 8 == 0), whole warp.
+// Every lane returns the same value (xor butterfly).
+__device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
+                               int H) {
+  const int lane = threadIdx.x & 31;
+  double s = 0.0;
+  for (int h = lane * 8; h < H; h += 256) {
+    uint4 va = *reinterpret_cast<const uint4*>(a + h);
+    uint4 vb = *reinterpret_cast<const uint4*>(b + h);
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+    const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s = fma((double)bf16lo(wa[i]), (double)bf16lo(wb[i]), s);
+      s = fma((double)bf16hi(wa[i]), (double)bf16hi(wb[i]), s);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
+struct WarpScratch {
+  int cand_e[kCandCap];
+  float cand_v[kCandCap];
+  double key[kCandCap];
+  float ex[32];
+  double kmax;
+};
+
+// (v, e) ordering: larger value first, lower index first on equal values.
+__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
+  return v > bv || (v == bv && e < be);
+}
+
+// Select the certified top-k of one token.  Whole warp; `L` holds the E fp32
+// logits in shared memory.  Writes idx_out[0..k) and w_out[0..k).
+__device__ void select_token(const float* L, int E, int k, float delta, const uint16_t* xrow,
+                             const uint16_t* gate_w, const float* bias, int H, double* l64_row,
+                             WarpScratch& sc, int32_t* idx_out, float* w_out, WsHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  uint32_t mytaken = 0;  // bit i: expert lane + 32 i already extracted
+  const int per_lane = (E + 31) >> 5;
+  int m = 0, end = -1;
+  bool fallback = false;
+  const float thr = 2.0f * delta * 1.001f;
+  while (true) {
+    float bv = -FLT_MAX;
+    int be = INT_MAX;
+    bool any = false;
+    for (int i = 0; i < per_lane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((mytaken >> i) & 1u)) {
+        const float v = L[e];
+        if (v != v) continue;  // NaN logits rank last
+        if (!any || better(v, e, bv, be)) { bv = v; be = e; any = true; }
+      }
+    }
+    if (!any) { bv = -FLT_MAX; be = INT_MAX; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (oe != INT_MAX && (be == INT_MAX || better(ov, oe, bv, be))) { bv = ov; be = oe; }
+    }
+    if (be == INT_MAX) {  // only NaN logits left: take the lowest remaining index
+      unsigned lowest = INT_MAX;
+      for (int i = 0; i < per_lane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((mytaken >> i) & 1u)) { lowest = min(lowest, (unsigned)e); break; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lowest = min(lowest, __shfl_xor_sync(0xffffffffu, lowest, o));
+      be = (int)lowest;
+      bv = L[be];
+    }
+    if ((be & 31) == lane) mytaken |= 1u << (be >> 5);
+    if (lane == 0) { sc.cand_e[m] = be; sc.cand_v[m] = bv; }
+    __syncwarp();
+    ++m;
+    if (m >= k + 1 && sc.cand_v[m - 2] - sc.cand_v[m - 1] > thr) { end = m - 2; break; }
+    if (m == E) { end = m - 1; break; }
+    if (m == kCandCap) { fallback = true; break; }
+  }
+
+  if (!fallback) {
+    // Ambiguous candidates: members of an adjacent pair closer than 2*delta.
+    bool amb0 = false, amb1 = false;
+    for (int r = 0; r < 2; ++r) {
+      const int i = lane + 32 * r;
+      bool a = false;
+      if (i <= end) {
+        if (i > 0 && !(sc.cand_v[i - 1] - sc.cand_v[i] > thr)) a = true;
+        if (i < end && !(sc.cand_v[i] - sc.cand_v[i + 1] > thr)) a = true;
+      }
+      if (r == 0) amb0 = a; else amb1 = a;
+    }
+    const unsigned bal0 = __ballot_sync(0xffffffffu, amb0);
+    const unsigned bal1 = __ballot_sync(0xffffffffu, amb1);
+    if (lane == 0 && (bal0 | bal1)) atomicAdd(&hdr->router_flagged, 1);
+    for (int r = 0; r < 2; ++r) {
+      const int i = lane + 32 * r;
+      if (i <= end) sc.key[i] = (double)sc.cand_v[i];
+    }
+    __syncwarp();
+    for (int r = 0; r < 2; ++r) {
+      unsigned bal = r == 0 ? bal0 : bal1;
+      while (bal) {
+        const int i = __ffs(bal) - 1 + 32 * r;
+        bal &= bal - 1;
+        const int e = sc.cand_e[i];
+        double d = warp_dot_f64(xrow, gate_w + (size_t)e * H, H);
+        if (bias) d += (double)bias[e];
+        if (lane == 0) sc.key[i] = d;
+      }
+    }
+    __syncwarp();
+    // rank of each candidate by (key desc, index asc)
+    int rank[2] = {INT_MAX, INT_MAX};
+    for (int r = 0; r < 2; ++r) {
+      const int i = lane + 32 * r;
+      if (i <= end) {
+        const double ki = sc.key[i];
+        const int ei = sc.cand_e[i];
+        int rk = 0;
+        for (int j = 0; j <= end; ++j) {
+          const double kj = sc.key[j];
+          rk += (kj > ki || (kj == ki && sc.cand_e[j] < ei)) ? 1 : 0;
+        }
+        rank[r] = rk;
+        if (rk < k) idx_out[rk] = ei;
+        if (rk == 0) sc.kmax = ki;
+      }
+    }
+    __syncwarp();
+    const double kmax = sc.kmax;
+    for (int r = 0; r < 2; ++r) {
+      const int i = lane + 32 * r;
+      if (rank[r] < k) sc.ex[rank[r]] = expf((float)(sc.key[i] - kmax));
+    }
+  } else {
+    // Every expert in fp64 (needs >= 64 experts within rounding of each other).
+    if (lane == 0) { atomicAdd(&hdr->router_flagged, 1); atomicAdd(&hdr->router_fallback, 1); }
+    for (int e = 0; e < E; ++e) {
+      double d = warp_dot_f64(xrow, gate_w + (size_t)e * H, H);
+      if (bias) d += (double)bias[e];
+      if (lane == 0) l64_row[e] = d;
+    }
+    __syncwarp();
+    __threadfence_block();
+    uint32_t taken = 0;
+    double kmax = 0.0;
+    for (int s = 0; s < k; ++s) {
+      double bv = 0.0;
+      int be = INT_MAX;
+      for (int i = 0; i < per_lane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u)) {
+          const double v = l64_row[e];
+          if (be == INT_MAX || v > bv || (v == bv && e < be)) { bv = v; be = e; }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) { bv = ov; be = oe; }
+      }
+      if (be == INT_MAX) be = 0;  // unreachable for k <= E
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (s == 0) kmax = bv;
+      if (lane == 0) { idx_out[s] = be; sc.ex[s] = expf((float)(bv - kmax)); }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    float sum = 0.0f;
+    for (int s = 0; s < k; ++s) sum += sc.ex[s];
+    for (int s = 0; s < k; ++s) w_out[s] = sc.ex[s] / sum;
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------ small batches
+// Grid (T, ceil(E/32)), 8 warps, 4 experts per warp.  Lane l sums the products
+// at h = 8l + 256j + (0..7) sequentially (H/32 terms), then a 5-level xor tree:
+// at most H/32 + 4 roundings per product.
+__global__ void __launch_bounds__(256) router_logits_small_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
+    int T, int H, int E, float* __restrict__ logits, float* __restrict__ xnorm,
+    float* __restrict__ wnorm) {
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.y * 32 + warp * 4;
+  const bool want_w = blockIdx.x == 0;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, sqw[4] = {0.f, 0.f, 0.f, 0.f}, sqx = 0.f;
+  const uint16_t* xr = x + (size_t)t * H;
+  for (int h = lane * 8; h < H; h += 256) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      sqx = fmaf(bf16lo(xw[i]), bf16lo(xw[i]), sqx);
+      sqx = fmaf(bf16hi(xw[i]), bf16hi(xw[i]), sqx);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + j;
+      if (e < E) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(gw + (size_t)e * H + h);
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[j] = fmaf(bf16lo(xw[i]), bf16lo(ww[i]), acc[j]);
+          acc[j] = fmaf(bf16hi(xw[i]), bf16hi(ww[i]), acc[j]);
+          if (want_w) {
+            sqw[j] = fmaf(bf16lo(ww[i]), bf16lo(ww[i]), sqw[j]);
+            sqw[j] = fmaf(bf16hi(ww[i]), bf16hi(ww[i]), sqw[j]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+      sqw[j] += __shfl_xor_sync(0xffffffffu, sqw[j], o);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + j;
+      if (e < E) {
+        logits[(size_t)t * E + e] = bias ? acc[j] + bias[e] : acc[j];
+        if (want_w) wnorm[e] = sqrtf(sqw[j]);
+      }
+    }
+    if (blockIdx.y == 0 && warp == 0) xnorm[t] = sqrtf(sqx);
+  }
+}
+
+// One warp per token.
+__global__ void __launch_bounds__(256) router_select_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
+    int T, int H, int E, int k, int gamma_terms, const float* __restrict__ logits,
+    const float* __restrict__ xnorm, const float* __restrict__ wnorm, double* __restrict__ l64,
+    int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem_raw);
+  float* sl = reinterpret_cast<float*>(smem_raw + sizeof(WarpScratch) * 8) + (size_t)warp * E;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float wmax = 0.f, lmax = 0.f;
+  for (int e = lane; e < E; e += 32) {
+    const float v = logits[(size_t)t * E + e];
+    sl[e] = v;
+    wmax = fmaxf(wmax, wnorm[e]);
+    lmax = fmaxf(lmax, fabsf(v));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+  }
+  __syncwarp();
+  const float delta = gamma_bound(gamma_terms) * xnorm[t] * wmax * (1.0f + 0x1p-10f) +
+                      0x1p-22f * lmax + (float)H * 0x1p-149f;
+  select_token(sl, E, k, delta, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, scr[warp],
+               idx + (size_t)t * k, w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
+}
+
+// ------------------------------------------------------------ large batches
+// One CTA = 64 tokens x all E (<= 128) experts, 128 threads; thread (ty, tx)
+// owns tokens 8ty..8ty+7 and experts 8tx..8tx+7.  K runs in chunks of 64: a
+// chunk's 64 products are summed sequentially from zero (63 roundings) and
+// the chunk sum is added to the running total (H/64 additions): at most
+// 64 + H/64 roundings per product.
+constexpr int kTileT = 64, kTileE = 128, kTileK = 64;
+
+__global__ void __launch_bounds__(128) router_tile_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
+    int T, int H, int E, int k, int gamma_terms, const float* __restrict__ wnorm,
+    double* __restrict__ l64, int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* xs = reinterpret_cast<float*>(smem_raw);           // [2][kTileK][kTileT]
+  float* wsm = xs + 2 * kTileK * kTileT;                    // [2][kTileK][kTileE]
+  __shared__ float s_xnorm[kTileT];
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.x * kTileT;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  // ||x_t|| for the tile's tokens: warp-level sums (H/32 + 4 roundings).
+  for (int i = 0; i < kTileT / 4; ++i) {
+    const int tl = warp * (kTileT / 4) + i;
+    const int t = t0 + tl;
+    float sq = 0.f;
+    if (t < T) {
+      for (int h = lane * 8; h < H; h += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          sq = fmaf(bf16lo(u[q]), bf16lo(u[q]), sq);
+          sq = fmaf(bf16hi(u[q]), bf16hi(u[q]), sq);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) s_xnorm[tl] = sqrtf(sq);
+  }
+
+  // Global -> register staging of one K chunk: x tile 64x64 (4 uint4 per
+  // thread), w tile 128x64 (8 uint4 per thread), transposed into [k][row].
+  uint4 rx[4], rw[8];
+  auto load_chunk = [&](int kc) {
+    const int k0 = kc * kTileK;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int v = tid + 128 * i;          // 512 vectors: row v/8, col (v%8)*8
+      const int row = v >> 3, col = (v & 7) * 8;
+      const int t = t0 + row;
+      rx[i] = (t < T) ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + col)
+                      : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = tid + 128 * i;          // 1024 vectors
+      const int row = v >> 3, col = (v & 7) * 8;
+      rw[i] = (row < E) ? *reinterpret_cast<const uint4*>(gw + (size_t)row * H + k0 + col)
+                        : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto store_chunk = [&](int buf) {
+    float* xb = xs + buf * kTileK * kTileT;
+    float* wb = wsm + buf * kTileK * kTileE;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int v = tid + 128 * i;
+      const int row = v >> 3, col = (v & 7) * 8;
+      const uint32_t u[4] = {rx[i].x, rx[i].y, rx[i].z, rx[i].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xb[(col + 2 * q) * kTileT + row] = bf16lo(u[q]);
+        xb[(col + 2 * q + 1) * kTileT + row] = bf16hi(u[q]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = tid + 128 * i;
+      const int row = v >> 3, col = (v & 7) * 8;
+      const uint32_t u[4] = {rw[i].x, rw[i].y, rw[i].z, rw[i].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        wb[(col + 2 * q) * kTileE + row] = bf16lo(u[q]);
+        wb[(col + 2 * q + 1) * kTileE + row] = bf16hi(u[q]);
+      }
+    }
+  };
+
+  float tot[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tot[i][j] = 0.f;
+
+  const int nchunks = H / kTileK;
+  load_chunk(0);
+  store_chunk(0);
+  __syncthreads();
+  for (int kc = 0; kc < nchunks; ++kc) {
+    const int buf = kc & 1;
+    if (kc + 1 < nchunks) load_chunk(kc + 1);
+    const float* xb = xs + buf * kTileK * kTileT + ty * 8;
+    const float* wb = wsm + buf * kTileK * kTileE + tx * 8;
+    float part[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part[i][j] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < kTileK; ++kk) {
+      const float4 xa = *reinterpret_cast<const float4*>(xb + kk * kTileT);
+      const float4 xb4 = *reinterpret_cast<const float4*>(xb + kk * kTileT + 4);
+      const float4 wa = *reinterpret_cast<const float4*>(wb + kk * kTileE);
+      const float4 wb4 = *reinterpret_cast<const float4*>(wb + kk * kTileE + 4);
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb4.x, xb4.y, xb4.z, xb4.w};
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb4.x, wb4.y, wb4.z, wb4.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tot[i][j] += part[i][j];
+    if (kc + 1 < nchunks) store_chunk(buf ^ 1);
+    __syncthreads();
+  }
+
+  // Logits to shared memory [64][E+1] (reusing the staging buffers).
+  const int ld = kTileE + 1;
+  float* sl = xs;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = tx * 8 + j;
+      if (e < E) sl[(ty * 8 + i) * ld + e] = bias ? tot[i][j] + bias[e] : tot[i][j];
+    }
+  __syncthreads();
+  WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem_raw + sizeof(float) * kTileT * ld + 256);
+  float wmax = 0.f;
+  for (int e = lane; e < E; e += 32) wmax = fmaxf(wmax, wnorm[e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+  for (int i = 0; i < kTileT / 4; ++i) {
+    const int tl = warp * (kTileT / 4) + i;
+    const int t = t0 + tl;
+    if (t >= T) break;
+    const float* row = sl + tl * ld;
+    float lmax = 0.f;
+    for (int e = lane; e < E; e += 32) lmax = fmaxf(lmax, fabsf(row[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    const float delta = gamma_bound(gamma_terms) * s_xnorm[tl] * wmax * (1.0f + 0x1p-10f) +
+                        0x1p-22f * lmax + (float)H * 0x1p-149f;
+    select_token(row, E, k, delta, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, scr[warp],
+                 idx + (size_t)t * k, w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
+  }
+}
+
+// ||w_e|| for every expert, one warp per expert.
+__global__ void __launch_bounds__(256) wnorm_kernel(const uint16_t* __restrict__ gw, int H, int E,
+                                                    float* __restrict__ wnorm) {
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;
+  float sq = 0.f;
+  for (int h = lane * 8; h < H; h += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(gw + (size_t)e * H + h);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      sq = fmaf(bf16lo(u[q]), bf16lo(u[q]), sq);
+      sq = fmaf(bf16hi(u[q]), bf16hi(u[q]), sq);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  if (lane == 0) wnorm[e] = sqrtf(sq);
+}
+
+}  // namespace
+
+cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
+                         int E, int k, int32_t* idx, float* w, void* ws, const WsLayout& L,
+                         cudaStream_t stream, int* launches) {
+  if (launches) *launches += 2;
+  float* xnorm = ws_ptr<float>(ws, L.xnorm);
+  float* wnorm = ws_ptr<float>(ws, L.wnorm);
+  double* l64 = ws_ptr<double>(ws, L.logits64);
+  const bool tiled = T >= 2048 && E <= kTileE;
+  if (tiled) {
+    wnorm_kernel<<<(E + 7) / 8, 256, 0, stream>>>(gate_w, H, E, wnorm);
+    const size_t smem = sizeof(float) * 2 * kTileK * (kTileT + kTileE);
+    static_assert(sizeof(float) * kTileT * (kTileE + 1) + 256 + 4 * sizeof(WarpScratch) <=
+                      sizeof(float) * 2 * kTileK * (kTileT + kTileE),
+                  "selection scratch fits in the staging buffers");
+    cudaError_t err = cudaFuncSetAttribute(router_tile_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const int gterms = kTileK + H / kTileK + 1;
+    router_tile_kernel<<<(T + kTileT - 1) / kTileT, 128, smem, stream>>>(
+        x, gate_w, bias, T, H, E, k, gterms, wnorm, l64, idx, w, ws);
+    return cudaGetLastError();
+  }
+  float* logits = ws_ptr<float>(ws, L.logits);
+  dim3 g1(T, (E + 31) / 32);
+  router_logits_small_kernel<<<g1, 256, 0, stream>>>(x, gate_w, bias, T, H, E, logits, xnorm, wnorm);
+  const size_t smem = sizeof(WarpScratch) * 8 + sizeof(float) * 8 * E;
+  cudaError_t err = cudaFuncSetAttribute(router_select_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int gterms = H / 32 + 5;
+  router_select_kernel<<<(T + 7) / 8, 256, smem, stream>>>(x, gate_w, bias, T, H, E, k, gterms,
+                                                           logits, xnorm, wnorm, l64, idx, w, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,187 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300.so: the forward pass of a Mixture-of-Experts
+ * FFN layer (router, expert grouping, grouped SwiGLU experts, combine) on one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * The layer follows the phases that the serving worklogs time inside the
+ * fused-MoE path -- "MoE gate", then "topk, expert kernel, activation, sum"
+ * (page "Decode 吞吐专项实验分析报告", section "下一步 profiling 方向",
+ * items 2-3) -- with the expert grouping done on the device, never returning
+ * to the host per layer (page "第 9 章 prefill：最大的瓶颈", sec. 9.9, fused
+ * path vs. the per-layer cudaStreamSynchronize of the MMQ path), and with no
+ * per-expert row ceiling (sec. 9.5 records entries beyond GMAX = 8 per group
+ * being dropped; here no routed row is ever dropped).
+ *
+ * Notation: T tokens, H hidden size, E experts, k = top_k, I expert
+ * intermediate size, S = T*k routed slots, flat slot index f = t*k + s.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless stated otherwise; bf16 tensors are
+ *     passed as uint16_t bit patterns; all tensors are dense row-major.
+ *   - Every device pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work on `stream`: no host synchronisation, no allocation,
+ *     no global state.  Concurrent calls need distinct workspaces.
+ *   - The caller owns every buffer.  `workspace` is scratch device memory of
+ *     at least moe_workspace_size(...) bytes; its contents on entry do not
+ *     matter.
+ *   - Return value: MOE_OK (0) or a negative moe_status.  Argument errors are
+ *     detected on the host before anything is enqueued.  Errors found by the
+ *     kernels (e.g. an out-of-range expert id handed to moe_permute) are
+ *     recorded in the workspace and reported by moe_read_status.  No kernel
+ *     traps.
+ *   - T == 0 is a valid empty batch: nothing is enqueued and MOE_OK returned.
+ *
+ * Supported shapes: 1 <= E <= 1024, 1 <= top_k <= min(E, 32), H and I
+ * multiples of 128 (NVFP4: H and I multiples of 128 as well), T*top_k < 2^31.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,    /* null pointer, negative size, top_k out of range   */
+  MOE_ERR_UNSUPPORTED = -2,    /* shape outside the supported set, misaligned
+                                  pointer, device is not sm_103                      */
+  MOE_ERR_WORKSPACE = -3,      /* workspace_bytes < moe_workspace_size(...)          */
+  MOE_ERR_CUDA = -4,           /* a CUDA runtime call or kernel launch failed        */
+  MOE_ERR_DEVICE = -5,         /* a kernel found invalid data (moe_read_status)     */
+  MOE_ERR_DEVICE_TIMEOUT = -6  /* a bounded device-side wait gave up (moe_read_status) */
+} moe_status;
+
+/*
+ * NVFP4 expert weights (W4A16: weights in 4 bits, activations stay bf16).
+ * Element W[e,r,k] = e2m1(code) * e4m3(scale[e,r,k/16]) * global[e], with
+ * e2m1 per OCP Microscaling Formats v1.0 (FP4 E2M1) and e4m3 per the OCP
+ * 8-bit floating point specification.  The NVFP4 deployment on the pages is
+ * the 176B MoE served through the "nvfp4-sm80" graft (page "vLLM 0.32
+ * 升级试验：TEP2 prefill 诅咒解除 + decode 本机纪录", header and "背景与动机").
+ *
+ *   gu_codes  [E, 2I, H/2] uint8, two codes per byte, even k in the low nibble
+ *   gu_scales [E, 2I, H/16] uint8 e4m3 bit patterns, 16-element blocks along H
+ *   gu_global [E] fp32
+ *   dn_codes  [E, H, I/2], dn_scales [E, H, I/16], dn_global [E]: same for w_down
+ * Rows [0, I) of the gate/up tensor are the gate projection, rows [I, 2I) the
+ * up projection.  All pointers are device pointers.
+ */
+typedef struct {
+  const uint8_t *gu_codes;
+  const uint8_t *gu_scales;
+  const float *gu_global;
+  const uint8_t *dn_codes;
+  const uint8_t *dn_scales;
+  const float *dn_global;
+} moe_nvfp4_weights;
+
+/* Bytes of device workspace that moe_route, moe_permute and moe_forward need
+ * for this shape (the largest of the three).  Returns 0 for an invalid shape. */
+size_t moe_workspace_size(int T, int H, int E, int I, int top_k);
+
+/*
+ * Router: "MoE gate" + "topk" (page "Decode 吞吐专项实验分析报告", section
+ * "下一步 profiling 方向").
+ *   logit[t,e] = sum_h x[t,h]*gate_w[e,h] (+ bias[e])
+ *   experts ranked by logit, larger first, lower index first on equal logits;
+ *   topk_idx[t,s] = expert in rank s (s = 0..k-1)
+ *   topk_w[t,s]   = exp(logit_s) / sum_{s'<k} exp(logit_s')  (the softmax over
+ *                   all E experts renormalised over the k selected ones)
+ * Logits accumulate in fp32 with a rigorous per-token error bound; a token
+ * whose ranking the bound cannot certify has its contested logits recomputed
+ * in fp64, so topk_idx equals the ranking of the exact logits.
+ *
+ *   x       [T, H] bf16          gate_w [E, H] bf16
+ *   bias    [E] fp32 or NULL     (added to the logits before softmax/top-k)
+ *   topk_idx [T, k] int32 (out)  topk_w [T, k] fp32 (out)
+ */
+int moe_route(const uint16_t *x, const uint16_t *gate_w, const float *bias, int T, int H, int E,
+              int top_k, int32_t *topk_idx, float *topk_w, void *workspace,
+              size_t workspace_bytes, void *stream);
+
+/*
+ * Expert grouping of the routed slots (done on the device, page "第 9 章
+ * prefill：最大的瓶颈", sec. 9.9, fused path):
+ *   counts[e]   = number of slots f with topk_idx[f] == e
+ *   offsets[e]  = sum_{e' < e} counts[e'],   offsets[E] = S      ([E+1])
+ *   perm[r]     = the slot f at grouped position r: slots sorted by expert,
+ *                 ascending f within an expert (a stable sort)       ([S])
+ *   inv_perm[f] = r such that perm[r] == f                           ([S])
+ * topk_idx is [T, k] int32 (device).  Entries outside [0, E) are skipped and
+ * recorded as MOE_ERR_DEVICE for moe_read_status; the outputs are then
+ * unspecified.
+ */
+int moe_permute(const int32_t *topk_idx, int T, int E, int top_k, int32_t *counts,
+                int32_t *offsets, int32_t *perm, int32_t *inv_perm, void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * The whole layer: route, group, per-expert SwiGLU, combine.
+ *   g   = W_gate[e] x_t,  u = W_up[e] x_t       (rows [0,I) / [I,2I) of w_gate_up[e])
+ *   h   = silu(g) * u,    silu(z) = z / (1 + exp(-z))      (rounded to bf16)
+ *   y   = W_down[e] h
+ *   out[t] = sum_{s=0..k-1} topk_w[t,s] * y[t,s]   summed in s order in fp32,
+ *            rounded to bf16 -- no float atomics, so the result is
+ *            bitwise deterministic and independent of token order.
+ *
+ *   x [T, H] bf16; gate_w [E, H] bf16; bias [E] fp32 or NULL
+ *   w_gate_up [E, 2I, H] bf16, w_down [E, H, I] bf16 -- both NULL iff nvfp4
+ *   nvfp4     NULL for bf16 weights, else the NVFP4 weights (host struct
+ *             holding device pointers)
+ *   out [T, H] bf16 (out)
+ *   topk_idx / topk_w: optional [T, k] outputs (NULL to skip) receiving the
+ *             routing that this call used.
+ */
+int moe_forward(const uint16_t *x, const uint16_t *gate_w, const float *bias,
+                const uint16_t *w_gate_up, const uint16_t *w_down,
+                const moe_nvfp4_weights *nvfp4, int T, int H, int E, int I, int top_k,
+                uint16_t *out, int32_t *topk_idx, float *topk_w, void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * moe_forward with timing hooks, for benchmarks and profilers: identical
+ * arguments and results, and additionally records events[i] (cudaEvent_t,
+ * created by the caller) on `stream` at the stage boundaries
+ *   [0] start  [1] after routing  [2] after grouping  [3] after gate/up+SwiGLU
+ *   [4] after down projection  [5] after combine
+ * and stores in *kernels_launched (HOST pointer, may be NULL) the number of
+ * kernels this call launched.  `events` is a HOST array of 6 non-null events.
+ */
+int moe_forward_profiled(const uint16_t *x, const uint16_t *gate_w, const float *bias,
+                         const uint16_t *w_gate_up, const uint16_t *w_down,
+                         const moe_nvfp4_weights *nvfp4, int T, int H, int E, int I, int top_k,
+                         uint16_t *out, int32_t *topk_idx, float *topk_w, void *workspace,
+                         size_t workspace_bytes, void *stream, void *const *events,
+                         int32_t *kernels_launched);
+
+/*
+ * Synchronises `stream`, then reports what the kernels of the last call that
+ * used `workspace` recorded: MOE_OK, MOE_ERR_DEVICE or MOE_ERR_DEVICE_TIMEOUT.
+ * `workspace` must have been passed to a moe_* call before.
+ */
+int moe_read_status(const void *workspace, void *stream);
+
+/*
+ * Synchronises `stream` and copies four counters of the last call that used
+ * `workspace` into the HOST array out4: [0] active experts, [1] active experts
+ * served by the tensor-core path, [2] tokens whose top-k needed fp64 logits,
+ * [3] tokens that needed fp64 logits for every expert.  Diagnostics only.
+ */
+int moe_read_diagnostics(const void *workspace, void *stream, int32_t *out4);
+
+/* Static, human-readable name of a moe_status value. */
+const char *moe_error_string(int status);
+
+/* Version of this library as an integer (major*10000 + minor*100 + patch). */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,209 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Routing (expert ids), counts, offsets and the permutation must match bit for
+bit; routing weights within the derived fp32 bound; outputs within
+max|out - ref| <= 1e-2 * max|ref| (bf16 weights) or 3e-2 (NVFP4 weights).
+"""
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+import gpu_helpers as gh  # noqa: E402
+
+import expert_layer_gb300 as moe  # noqa: E402
+import moe_inputs  # noqa: E402
+import oracle  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from expert_layer_gb300 import _build
+    _build.build()
+    moe.lib()
+
+
+def _small(T, H, E, k, I, bias=None, seed=0, nvfp4=False):
+    return moe_inputs.make_inputs(dict(T=T, H=H, E=E, top_k=k, I=I, bias=bias, nvfp4=nvfp4), seed=seed,
+                                  device="cuda")
+
+
+# ------------------------------------------------------------ small, full oracle
+SMALL_CASES = {
+    "tiny": dict(T=4, H=256, E=8, k=2, I=128),
+    "T1": dict(T=1, H=256, E=8, k=2, I=128),
+    "ragged": dict(T=37, H=384, E=16, k=4, I=256),
+    "k_eq_E": dict(T=6, H=256, E=8, k=8, I=128),
+    "E1024_k32": dict(T=16, H=256, E=1024, k=32, I=128),
+    "zipf": dict(T=50, H=512, E=32, k=4, I=256, bias="zipf"),
+    "nvfp4_small": dict(T=24, H=256, E=8, k=2, I=128, nvfp4=True),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_forward_small(name):
+    c = SMALL_CASES[name]
+    inp = _small(c["T"], c["H"], c["E"], c["k"], c["I"], bias=c.get("bias"), nvfp4=c.get("nvfp4", False))
+    out, idx, w, ws = gh.run_forward(inp)
+    assert moe.read_status(ws) == 0
+    orc = oracle.forward_from_inputs(inp)
+    gh.check_routing(inp, idx, w, orc)
+    gh.check_output(inp, out, orc)
+
+
+def test_tiny_workload():
+    inp = moe_inputs.make_inputs("tiny", device="cuda")
+    out, idx, w, ws = gh.run_forward(inp)
+    orc = oracle.forward_from_inputs(inp)
+    gh.check_routing(inp, idx, w, orc)
+    gh.check_output(inp, out, orc)
+
+
+def test_route_and_permute_entry_points():
+    inp = _small(33, 256, 16, 4, 128, bias="zipf")
+    idx, w = moe.route(inp.x, inp.gate_w, inp.bias, inp.top_k)
+    counts, offsets, perm, inv = moe.permute(idx, inp.E)
+    torch.cuda.synchronize()
+    r = oracle.route_from_inputs(inp)
+    gh.check_routing(inp, idx, w, r)
+    assert np.array_equal(counts.cpu().numpy(), r["counts"])
+    assert np.array_equal(offsets.cpu().numpy(), r["offsets"])
+    assert np.array_equal(perm.cpu().numpy(), r["perm"])
+    assert np.array_equal(inv.cpu().numpy(), r["inv_perm"])
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 1), (100, 64, 8), (512, 128, 8), (2048, 128, 8),
+                                   (3000, 200, 6), (9000, 128, 8)])
+def test_permute_matches_oracle(T, E, k):
+    """Grouping alone on random expert ids, single-block and multi-block paths."""
+    g = torch.Generator().manual_seed(T + E)
+    idx = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
+    ws = moe.alloc_workspace(T, 128, E, 128, k)
+    counts, offsets, perm, inv = moe.permute(idx.cuda(), E, workspace=ws)
+    assert moe.read_status(ws) == 0
+    rc, ro, rp, ri = oracle.permute(idx.numpy(), E)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(perm.cpu().numpy(), rp)
+    assert np.array_equal(inv.cpu().numpy(), ri)
+
+
+def test_permute_flags_bad_expert_id():
+    idx = torch.tensor([[0, 1], [5, 99]], dtype=torch.int32, device="cuda")
+    ws = moe.alloc_workspace(2, 128, 8, 128, 2)
+    moe.permute(idx, 8, workspace=ws)
+    assert moe.read_status(ws) == -5   # MOE_ERR_DEVICE
+
+
+def test_empty_batch():
+    inp = _small(1, 256, 8, 2, 128)
+    x0 = inp.x[:0]
+    out = moe.forward(x0, inp.gate_w, None, inp.w_gate_up, inp.w_down, 2,
+                      workspace=moe.alloc_workspace(1, 256, 8, 128, 2))
+    assert out.shape == (0, 256)
+
+
+# ------------------------------------------------------------ routing edge cases
+def test_exact_ties_lower_index_wins():
+    inp = _small(12, 256, 16, 4, 128)
+    gw = inp.gate_w.clone()
+    gw[9] = gw[2]                         # identical rows: exact logit ties
+    gw[13] = gw[2]
+    inp.gate_w = gw
+    out, idx, w, ws = gh.run_forward(inp)
+    orc = oracle.forward_from_inputs(inp)
+    gh.check_routing(inp, idx, w, orc)
+    gh.check_output(inp, out, orc)
+    i = idx.cpu().numpy()
+    for t in range(inp.T):
+        row = list(i[t])
+        if 2 in row and 9 in row:
+            assert row.index(2) < row.index(9)
+
+
+def test_zero_gate_all_tied():
+    """All-zero router weights: every logit ties; experts 0..k-1, weights 1/k."""
+    inp = _small(5, 256, 8, 3, 128)
+    inp.gate_w = torch.zeros_like(inp.gate_w)
+    out, idx, w, ws = gh.run_forward(inp)
+    assert (idx.cpu().numpy() == np.arange(3)[None, :]).all()
+    assert torch.allclose(w.cpu(), torch.full((5, 3), 1 / 3), atol=1e-7)
+    orc = oracle.forward_from_inputs(inp)
+    gh.check_output(inp, out, orc)
+    d = moe.read_diagnostics(ws)
+    assert d["router_fallback"] == 5 or d["router_flagged"] == 5
+
+
+def test_all_tokens_one_expert():
+    """A dominant bias sends every token's slot 0 to expert 3 (a group larger
+    than one 32-row pass)."""
+    inp = _small(100, 256, 8, 1, 128)
+    b = torch.zeros(8, dtype=torch.float32, device="cuda")
+    b[3] = 100.0
+    inp.bias = b
+    out, idx, w, ws = gh.run_forward(inp)
+    assert (idx.cpu().numpy() == 3).all()
+    orc = oracle.forward_from_inputs(inp)
+    gh.check_output(inp, out, orc)
+
+
+def test_large_router_path():
+    """T >= 2048 uses the token-tiled router and the multi-block grouping."""
+    inp = _small(2304, 256, 64, 4, 128, bias="zipf")
+    idx, w = moe.route(inp.x, inp.gate_w, inp.bias, inp.top_k)
+    counts, offsets, perm, inv = moe.permute(idx, inp.E)
+    torch.cuda.synchronize()
+    r = oracle.route_from_inputs(inp)
+    gh.check_routing(inp, idx, w, r)
+    assert np.array_equal(perm.cpu().numpy(), r["perm"])
+
+
+# ------------------------------------------------------------ determinism / invariance
+def test_deterministic_and_token_order_invariant():
+    inp = moe_inputs.make_inputs("decode64", device="cuda")
+    out1, _, _, ws = gh.run_forward(inp)
+    out2, _, _, _ = gh.run_forward(inp, workspace=ws)
+    assert torch.equal(out1, out2)
+    p = torch.randperm(inp.T, generator=torch.Generator().manual_seed(1)).cuda()
+    inp2 = moe_inputs.MoEInputs(inp.T, inp.H, inp.E, inp.top_k, inp.I, inp.x[p].contiguous(), inp.gate_w,
+                                inp.bias, inp.w_gate_up, inp.w_down)
+    out3, _, _, _ = gh.run_forward(inp2)
+    assert torch.equal(out1[p], out3)
+
+
+# ------------------------------------------------------------ full-size workloads
+@pytest.mark.parametrize("name", ["decode8", "decode64"])
+def test_decode_workloads_full(name):
+    inp = moe_inputs.make_inputs(name, device="cuda")
+    out, idx, w, ws = gh.run_forward(inp)
+    assert moe.read_status(ws) == 0
+    orc = oracle.forward_from_inputs(inp)
+    gh.check_routing(inp, idx, w, orc)
+    gh.check_output(inp, out, orc)
+    r = oracle.route_from_inputs(inp)
+    assert moe.read_diagnostics(ws)["num_active"] == int((r["counts"] > 0).sum())
+
+
+def test_nvfp4_workload_sampled():
+    inp = moe_inputs.make_inputs("nvfp4_256", device="cuda")
+    out, idx, w, ws = gh.run_forward(inp)
+    assert moe.read_status(ws) == 0
+    rows = list(range(0, inp.T, 8)) + [inp.T - 1]
+    orc = oracle.forward_from_inputs(inp, tokens=rows)
+    gh.check_routing(inp, idx, w, orc)
+    gh.check_output(inp, out, orc, rows=rows)
+
+
+def test_prefill_workload_sampled():
+    inp = moe_inputs.make_inputs("prefill8192", device="cuda")
+    out, idx, w, ws = gh.run_forward(inp)
+    assert moe.read_status(ws) == 0
+    rows = list(range(0, inp.T, 331)) + [inp.T - 1]
+    orc = oracle.forward_from_inputs(inp, tokens=rows)
+    gh.check_routing(inp, idx, w, orc)
+    gh.check_output(inp, out, orc, rows=rows)
