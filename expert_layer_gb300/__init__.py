@@ -45,6 +45,7 @@ _SIGNATURES = {
     "moe_forward_profiled": (_I, [_P, _P, _P, _P, _P, ctypes.POINTER(_NVFP4), _I, _I, _I, _I, _I, _P,
                                   _P, _P, _P, _SZ, _P, ctypes.POINTER(_P),
                                   ctypes.POINTER(ctypes.c_int32)]),
+    "moe_route_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_read_status": (_I, [_P, _P]),
     "moe_read_diagnostics": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_error_string": (ctypes.c_char_p, [_I]),

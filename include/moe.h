@@ -174,6 +174,26 @@ int moe_read_status(const void *workspace, void *stream);
  */
 int moe_read_diagnostics(const void *workspace, void *stream, int32_t *out4);
 
+/*
+ * moe_route without a workspace, for callers that cannot allocate device
+ * memory (code running under CUDA graph capture, runtimes that hand out only
+ * pre-reserved pool memory, host integrations that forbid allocation after
+ * start-up).  The pages describe no such entry point; it is an addition of
+ * this library.  Same arguments and results as moe_route minus the
+ * workspace; allocates nothing.
+ *
+ * Its scratch is a fixed device array inside the library (about 0.8 MB, held
+ * on every GPU that loads the library until the process exits), so it serves
+ * only T*E <= 65536 and T <= 8192; larger batches return MOE_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (make that
+ * call before any stream capture).  All calls on a device share the array:
+ * calls whose GPU work overlaps (unordered streams) race and give undefined
+ * results.  Device-side status is not reported (there is no workspace to
+ * pass to moe_read_status).
+ */
+int moe_route_noalloc(const uint16_t *x, const uint16_t *gate_w, const float *bias, int T, int H,
+                      int E, int top_k, int32_t *topk_idx, float *topk_w, void *stream);
+
 /* Static, human-readable name of a moe_status value. */
 const char *moe_error_string(int status);
 
