@@ -49,6 +49,8 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--weight-sets", type=int, default=WEIGHT_SETS,
+                   help="copies of the expert weights cycled across steps")
     p.add_argument("--target-seconds", type=float, default=2.0,
                    help="timed-region length used to pick K when --steps is not given")
     return p.parse_args()
@@ -250,7 +252,8 @@ def run_ours(args):
 
     # weight sets cycled across steps
     sets = []
-    for r in range(WEIGHT_SETS):
+    nsets = max(1, args.weight_sets)
+    for r in range(nsets):
         if nv:
             q = inp.nvfp4_gate_up if r == 0 else moe_inputs.NVFP4Tensor(
                 inp.nvfp4_gate_up.codes.clone(), inp.nvfp4_gate_up.scales.clone(), inp.nvfp4_gate_up.glob.clone())
@@ -277,7 +280,7 @@ def run_ours(args):
     wsn = ws.numel()
 
     def step(i, xp=x_p, op=o_p):
-        gu, dn, nvp, _ = sets[i % WEIGHT_SETS]
+        gu, dn, nvp, _ = sets[i % nsets]
         rc = lib.moe_forward(xp, g_p, b_p, gu, dn, nvp, T, H, E, I, k, op, None, None, ws_p, wsn, sptr)
         if rc != 0:
             raise moe.MoEError(lib.moe_error_string(rc).decode())
@@ -330,7 +333,7 @@ def run_ours(args):
     ev_ptrs = [(P * 6)(*[P(e.cuda_event) for e in row]) for row in evs]
     nk = ctypes.c_int32(0)
     for i in range(K2):
-        gu, dn, nvp, _ = sets[i % WEIGHT_SETS]
+        gu, dn, nvp, _ = sets[i % nsets]
         rc = lib.moe_forward_profiled(x_p, g_p, b_p, gu, dn, nvp, T, H, E, I, k, o_p, None, None, ws_p,
                                       wsn, sptr, ev_ptrs[i], ctypes.byref(nk))
         assert rc == 0
@@ -416,7 +419,7 @@ def run_ours(args):
                    "weights": "nvfp4" if nv else "bf16",
                    "router_bias": "0.5*log-Zipf(1.1)" if inp.bias is not None else None,
                    "seed": args.seed, "parallelism": f"replicas x{world}",
-                   "l2": f"{WEIGHT_SETS} rotating expert-weight sets of {weight_bytes_per_set / 1e9:.2f} GB "
+                   "l2": f"{nsets} rotating expert-weight sets of {weight_bytes_per_set / 1e9:.2f} GB "
                          f"(> 129 MB L2) cycled across steps"},
         "roofline": roof,
         "layer": layer,

@@ -96,7 +96,7 @@ int moe_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int 
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   MOE_TRY(check_device(nullptr));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s));
+  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
   return cuda_status(
       launch_route(x, gate_w, bias, T, H, E, top_k, topk_idx, topk_w, workspace, L, s, nullptr));
 }
@@ -116,7 +116,7 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int top_k, int32_t* count
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   MOE_TRY(check_device(nullptr));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s));
+  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
   return cuda_status(launch_permute(topk_idx, T, E, top_k, counts, offsets, perm, inv_perm,
                                     workspace, L, INT_MAX, 128, s, nullptr));
 }
@@ -166,7 +166,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
     return events ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
   };
   MOE_TRY_CUDA(mark(0));
-  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s));
+  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
   MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches));
   MOE_TRY_CUDA(mark(1));
   MOE_TRY_CUDA(launch_permute(idx, T, E, top_k, counts, offsets, perm, inv_perm, workspace, L,

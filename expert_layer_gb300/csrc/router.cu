@@ -62,60 +62,59 @@ struct WarpScratch {
   double kmax;
 };
 
-// (v, e) ordering: larger value first, lower index first on equal values.
-__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
-  return v > bv || (v == bv && e < be);
+// Sort key of a logit: NaN ranks below every number.
+__device__ __forceinline__ float rank_key(float v) { return v != v ? -INFINITY : v; }
+
+// Sorted candidates: cand_e/cand_v[r] = the expert of rank r (larger logit
+// first, lower index first on equal logits) for r < min(E, kCandCap).  Each
+// of the nthr cooperating threads (thread index tid) ranks its experts by
+// counting the experts that come before it -- no serial dependency chain.
+// The caller synchronises the cooperating threads before using the result.
+__device__ void rank_candidates(const float* L, int E, WarpScratch& sc, int tid, int nthr) {
+  for (int e = tid; e < E; e += nthr) {
+    const float v = rank_key(L[e]);
+    int r = 0;
+    int j = 0;
+    for (; j + 4 <= E; j += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(L + j);
+      const float q0 = rank_key(q.x), q1 = rank_key(q.y), q2 = rank_key(q.z), q3 = rank_key(q.w);
+      r += (q0 > v || (q0 == v && j < e)) + (q1 > v || (q1 == v && j + 1 < e)) +
+           (q2 > v || (q2 == v && j + 2 < e)) + (q3 > v || (q3 == v && j + 3 < e));
+    }
+    for (; j < E; ++j) {
+      const float q = rank_key(L[j]);
+      r += (q > v || (q == v && j < e));
+    }
+    if (r < kCandCap) { sc.cand_e[r] = e; sc.cand_v[r] = v; }
+  }
 }
 
-// Select the certified top-k of one token.  Whole warp; `L` holds the E fp32
-// logits in shared memory.  Writes idx_out[0..k) and w_out[0..k).
-__device__ void select_token(const float* L, int E, int k, float delta, const uint16_t* xrow,
+// Certified top-k of one token from its sorted candidates.  Whole warp.
+// Writes idx_out[0..k) and w_out[0..k).
+__device__ void select_token(int E, int k, float delta, const uint16_t* xrow,
                              const uint16_t* gate_w, const float* bias, int H, double* l64_row,
                              WarpScratch& sc, int32_t* idx_out, float* w_out, WsHeader* hdr) {
   const int lane = threadIdx.x & 31;
-  uint32_t mytaken = 0;  // bit i: expert lane + 32 i already extracted
   const int per_lane = (E + 31) >> 5;
-  int m = 0, end = -1;
-  bool fallback = false;
+  const int nc = E < kCandCap ? E : kCandCap;
   const float thr = 2.0f * delta * 1.001f;
-  while (true) {
-    float bv = -FLT_MAX;
-    int be = INT_MAX;
-    bool any = false;
-    for (int i = 0; i < per_lane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((mytaken >> i) & 1u)) {
-        const float v = L[e];
-        if (v != v) continue;  // NaN logits rank last
-        if (!any || better(v, e, bv, be)) { bv = v; be = e; any = true; }
-      }
-    }
-    if (!any) { bv = -FLT_MAX; be = INT_MAX; }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (oe != INT_MAX && (be == INT_MAX || better(ov, oe, bv, be))) { bv = ov; be = oe; }
-    }
-    if (be == INT_MAX) {  // only NaN logits left: take the lowest remaining index
-      unsigned lowest = INT_MAX;
-      for (int i = 0; i < per_lane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((mytaken >> i) & 1u)) { lowest = min(lowest, (unsigned)e); break; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lowest = min(lowest, __shfl_xor_sync(0xffffffffu, lowest, o));
-      be = (int)lowest;
-      bv = L[be];
-    }
-    if ((be & 31) == lane) mytaken |= 1u << (be >> 5);
-    if (lane == 0) { sc.cand_e[m] = be; sc.cand_v[m] = bv; }
-    __syncwarp();
-    ++m;
-    if (m >= k + 1 && sc.cand_v[m - 2] - sc.cand_v[m - 1] > thr) { end = m - 2; break; }
-    if (m == E) { end = m - 1; break; }
-    if (m == kCandCap) { fallback = true; break; }
+  // The certain set ends at the first rank j >= k-1 whose gap to rank j+1
+  // exceeds 2*delta: everything below is certainly below it.
+  unsigned gap0, gap1;
+  {
+    int j = lane;
+    bool ok = j >= k - 1 && j + 1 < nc && sc.cand_v[j] - sc.cand_v[j + 1] > thr;
+    gap0 = __ballot_sync(0xffffffffu, ok);
+    j = lane + 32;
+    ok = j >= k - 1 && j + 1 < nc && sc.cand_v[j] - sc.cand_v[j + 1] > thr;
+    gap1 = __ballot_sync(0xffffffffu, ok);
   }
+  int end;
+  bool fallback = false;
+  if (gap0) end = __ffs(gap0) - 1;
+  else if (gap1) end = __ffs(gap1) - 1 + 32;
+  else if (E <= kCandCap) end = E - 1;
+  else { end = -1; fallback = true; }
 
   if (!fallback) {
     // Ambiguous candidates: members of an adjacent pair closer than 2*delta.
@@ -216,19 +215,63 @@ __device__ void select_token(const float* L, int E, int k, float delta, const ui
 }
 
 // ------------------------------------------------------------ small batches
-// Grid (T, ceil(E/32)), 8 warps, 4 experts per warp.  Lane l sums the products
-// at h = 8l + 256j + (0..7) sequentially (H/32 terms), then a 5-level xor tree:
-// at most H/32 + 4 roundings per product.
-__global__ void __launch_bounds__(256) router_logits_small_kernel(
+// Grid (T, ceil(E/8)), 8 warps, one (token, expert) logit per warp.  Lane l
+// sums the products at h = 8l + 256j + (0..7) sequentially (H/32 terms), then
+// a 5-level xor tree: at most H/32 + 4 roundings per product.  The last CTA to
+// finish a token (integer counter, no waiting) selects that token's top-k.
+__global__ void __launch_bounds__(256) router_small_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
-    int T, int H, int E, float* __restrict__ logits, float* __restrict__ xnorm,
-    float* __restrict__ wnorm) {
+    int T, int H, int E, int k, int gamma_terms, float* __restrict__ logits,
+    float* __restrict__ wnorm, double* __restrict__ l64, int* __restrict__ cnt,
+    int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
+  __shared__ WarpScratch scr;
+  __shared__ __align__(16) float sl[1024];
+  __shared__ int s_last;
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e0 = blockIdx.y * 32 + warp * 4;
-  const bool want_w = blockIdx.x == 0;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, sqw[4] = {0.f, 0.f, 0.f, 0.f}, sqx = 0.f;
+  const int e = blockIdx.y * 8 + warp;
   const uint16_t* xr = x + (size_t)t * H;
+  if (e < E) {
+    float acc = 0.f, sq = 0.f;
+    const uint16_t* wr = gw + (size_t)e * H;
+#pragma unroll 8
+    for (int h = lane * 8; h < H; h += 256) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
+      const uint4 wv = *reinterpret_cast<const uint4*>(wr + h);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc = fmaf(bf16lo(xw[i]), bf16lo(ww[i]), acc);
+        acc = fmaf(bf16hi(xw[i]), bf16hi(ww[i]), acc);
+        sq = fmaf(bf16lo(ww[i]), bf16lo(ww[i]), sq);
+        sq = fmaf(bf16hi(ww[i]), bf16hi(ww[i]), sq);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    }
+    if (lane == 0) {
+      logits[(size_t)t * E + e] = bias ? acc + bias[e] : acc;
+      wnorm[e] = sqrtf(sq);   // same value from every token's CTA
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&cnt[t], 1) == (int)gridDim.y - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // last CTA of token t: logits to shared memory, ranked by all its threads
+  for (int ee = threadIdx.x; ee < E; ee += blockDim.x) sl[ee] = __ldcg(&logits[(size_t)t * E + ee]);
+  __syncthreads();
+  rank_candidates(sl, E, scr, threadIdx.x, blockDim.x);
+  __syncthreads();
+  if (warp != 0) return;
+  // ||x_t||, max ||w_e||, max |logit| for the error bound
+  float sqx = 0.f;
   for (int h = lane * 8; h < H; h += 256) {
     const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -237,75 +280,22 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(
       sqx = fmaf(bf16lo(xw[i]), bf16lo(xw[i]), sqx);
       sqx = fmaf(bf16hi(xw[i]), bf16hi(xw[i]), sqx);
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + j;
-      if (e < E) {
-        const uint4 wv = *reinterpret_cast<const uint4*>(gw + (size_t)e * H + h);
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[j] = fmaf(bf16lo(xw[i]), bf16lo(ww[i]), acc[j]);
-          acc[j] = fmaf(bf16hi(xw[i]), bf16hi(ww[i]), acc[j]);
-          if (want_w) {
-            sqw[j] = fmaf(bf16lo(ww[i]), bf16lo(ww[i]), sqw[j]);
-            sqw[j] = fmaf(bf16hi(ww[i]), bf16hi(ww[i]), sqw[j]);
-          }
-        }
-      }
-    }
+  }
+  float wmax = 0.f, lmax = 0.f;
+  for (int ee = lane; ee < E; ee += 32) {
+    wmax = fmaxf(wmax, __ldcg(&wnorm[ee]));
+    lmax = fmaxf(lmax, fabsf(sl[ee]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
-      sqw[j] += __shfl_xor_sync(0xffffffffu, sqw[j], o);
-    }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + j;
-      if (e < E) {
-        logits[(size_t)t * E + e] = bias ? acc[j] + bias[e] : acc[j];
-        if (want_w) wnorm[e] = sqrtf(sqw[j]);
-      }
-    }
-    if (blockIdx.y == 0 && warp == 0) xnorm[t] = sqrtf(sqx);
-  }
-}
-
-// One warp per token.
-__global__ void __launch_bounds__(256) router_select_kernel(
-    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
-    int T, int H, int E, int k, int gamma_terms, const float* __restrict__ logits,
-    const float* __restrict__ xnorm, const float* __restrict__ wnorm, double* __restrict__ l64,
-    int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem_raw);
-  float* sl = reinterpret_cast<float*>(smem_raw + sizeof(WarpScratch) * 8) + (size_t)warp * E;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  float wmax = 0.f, lmax = 0.f;
-  for (int e = lane; e < E; e += 32) {
-    const float v = logits[(size_t)t * E + e];
-    sl[e] = v;
-    wmax = fmaxf(wmax, wnorm[e]);
-    lmax = fmaxf(lmax, fabsf(v));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
     wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
     lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
   }
-  __syncwarp();
-  const float delta = gamma_bound(gamma_terms) * xnorm[t] * wmax * (1.0f + 0x1p-10f) +
+  const float delta = gamma_bound(gamma_terms) * sqrtf(sqx) * wmax * (1.0f + 0x1p-10f) +
                       0x1p-22f * lmax + (float)H * 0x1p-149f;
-  select_token(sl, E, k, delta, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, scr[warp],
-               idx + (size_t)t * k, w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
+  select_token(E, k, delta, xr, gw, bias, H, l64 + (size_t)t * E, scr, idx + (size_t)t * k,
+               w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
 }
 
 // ------------------------------------------------------------ large batches
@@ -440,7 +430,7 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
   }
 
   // Logits to shared memory [64][E+1] (reusing the staging buffers).
-  const int ld = kTileE + 1;
+  const int ld = kTileE + 4;   // rows stay 16-byte aligned for the ranking
   float* sl = xs;
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -466,7 +456,9 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
     for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
     const float delta = gamma_bound(gamma_terms) * s_xnorm[tl] * wmax * (1.0f + 0x1p-10f) +
                         0x1p-22f * lmax + (float)H * 0x1p-149f;
-    select_token(row, E, k, delta, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, scr[warp],
+    rank_candidates(row, E, scr[warp], lane, 32);
+    __syncwarp();
+    select_token(E, k, delta, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, scr[warp],
                  idx + (size_t)t * k, w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
   }
 }
@@ -496,15 +488,14 @@ __global__ void __launch_bounds__(256) wnorm_kernel(const uint16_t* __restrict__
 cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
                          int E, int k, int32_t* idx, float* w, void* ws, const WsLayout& L,
                          cudaStream_t stream, int* launches) {
-  if (launches) *launches += 2;
-  float* xnorm = ws_ptr<float>(ws, L.xnorm);
   float* wnorm = ws_ptr<float>(ws, L.wnorm);
   double* l64 = ws_ptr<double>(ws, L.logits64);
   const bool tiled = T >= 2048 && E <= kTileE;
+  if (launches) *launches += tiled ? 2 : 1;
   if (tiled) {
     wnorm_kernel<<<(E + 7) / 8, 256, 0, stream>>>(gate_w, H, E, wnorm);
     const size_t smem = sizeof(float) * 2 * kTileK * (kTileT + kTileE);
-    static_assert(sizeof(float) * kTileT * (kTileE + 1) + 256 + 4 * sizeof(WarpScratch) <=
+    static_assert(sizeof(float) * kTileT * (kTileE + 4) + 256 + 4 * sizeof(WarpScratch) <=
                       sizeof(float) * 2 * kTileK * (kTileT + kTileE),
                   "selection scratch fits in the staging buffers");
     cudaError_t err = cudaFuncSetAttribute(router_tile_kernel,
@@ -516,15 +507,11 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
     return cudaGetLastError();
   }
   float* logits = ws_ptr<float>(ws, L.logits);
-  dim3 g1(T, (E + 31) / 32);
-  router_logits_small_kernel<<<g1, 256, 0, stream>>>(x, gate_w, bias, T, H, E, logits, xnorm, wnorm);
-  const size_t smem = sizeof(WarpScratch) * 8 + sizeof(float) * 8 * E;
-  cudaError_t err = cudaFuncSetAttribute(router_select_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
+  int* cnt = ws_ptr<int>(ws, L.cnt);
+  dim3 g1(T, (E + 7) / 8);
   const int gterms = H / 32 + 5;
-  router_select_kernel<<<(T + 7) / 8, 256, smem, stream>>>(x, gate_w, bias, T, H, E, k, gterms,
-                                                           logits, xnorm, wnorm, l64, idx, w, ws);
+  router_small_kernel<<<g1, 256, 0, stream>>>(x, gate_w, bias, T, H, E, k, gterms, logits, wnorm,
+                                              l64, cnt, idx, w, ws);
   return cudaGetLastError();
 }
 

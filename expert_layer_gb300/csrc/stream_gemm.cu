@@ -7,19 +7,20 @@
 // a handful of token rows.  The kernels therefore stream the weights with
 // coalesced 128-bit loads that bypass L1, keep the (small, reused) activation
 // rows in L1/L2, and do the arithmetic on mma.sync m16n8k16 (bf16 in, fp32
-// accumulate) with the weights as the 16-row A operand and up to 32 gathered
+// accumulate) with the weights as the 16-row A operand and up to 64 gathered
 // token rows as the B operand ("swap AB").  This replaces the ncols <= 8 MMVQ
 // templates of page "第 9 章 prefill：最大的瓶颈" (sec. 9.5): any number of rows
-// per expert is served, in passes of 32.
+// per expert is served, in passes of up to 64.
 //
-// Work unit = (active expert, 16 weight rows over the whole K).
+// Work unit = (active expert, 16 weight rows over the whole K), owned by one
+// warp.
 //   gate/up: A rows 0-7 are gate rows j0..j0+7, rows 8-15 the matching up rows
 //            I+j0..I+j0+7, so one fragment holds g and u of the same j and the
 //            SwiGLU h = silu(g)*u is formed in the epilogue (h rounded to bf16).
 //   down:    A rows are 16 consecutive output features d0..d0+15; the epilogue
 //            scales by the routing weight and writes the slot's partial row.
-// K is split across the CTA's 8 warps; warp partials are summed through
-// shared memory in fixed warp order (deterministic).
+// A warp sums its unit's whole K itself, so results do not depend on the
+// launch shape (deterministic).
 //
 // K-index assignment inside one mma: thread (g, c) of a warp loads 8
 // consecutive bf16 (one 16-byte vector) of rows g and g+8 at k = 8c..8c+7 of
@@ -42,10 +43,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kWarpsPerCta = 8;
-constexpr int kThreadsPerCta = kWarpsPerCta * 32;
-constexpr int kNT = 4;                 // n-tiles (8 tokens each) per pass
-constexpr int kPassRows = 8 * kNT;     // 32 token rows per pass
 
 // e2m1 code -> value, from the format: sign, 2-bit exponent (bias 1), 1-bit
 // mantissa; exponent 0 is subnormal (m * 0.5).
@@ -72,192 +69,280 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Pipeline shape per variant.
+template <bool kFp4>
+struct StreamCfg {
+  static constexpr int KB = kFp4 ? 128 : 32;      // K elements per block
+  static constexpr int KG = kFp4 ? 2 : 4;         // blocks per pipelined group
+  static constexpr int NS = kFp4 ? 5 : 4;         // groups in the ring (NS-1 in flight)
+  static constexpr int kWarps = 12;
+  // per-warp ring: [NS][KG][2 rows][32 lanes] x 16 B of weights (codes), plus
+  // [NS][KG][2][32] x 8 B of scales for NVFP4
+  static constexpr int kWBytes = NS * KG * 2 * 32 * 16;
+  static constexpr int kSBytes = kFp4 ? NS * KG * 2 * 32 * 8 : 0;
+  static constexpr int kWarpBytes = kWBytes + kSBytes;
+  static constexpr int kBRegs = kFp4 ? 16 : 4;    // 32-bit B registers per block
+};
+
+// One (unit, pass) task of a warp: 16 weight rows of one expert over all of K,
+// against 8 of the expert's token rows (pass p covers rows 8p..8p+7).
+struct Task {
+  long long u;   // unit index, < 0 when the warp has no more work
+  int pass, npass, e, blk, m, off;
+};
+
+__device__ __forceinline__ void task_load(Task& t, const StreamGemmArgs& a, int UPE, long long U) {
+  if (t.u >= U) { t.u = -1; return; }
+  t.e = a.active[t.u / UPE];
+  t.blk = (int)(t.u % UPE);
+  t.m = a.counts[t.e];
+  t.off = a.offsets[t.e];
+  t.pass = 0;
+  t.npass = (t.m + 7) / 8;
+}
+
+__device__ __forceinline__ void task_next(Task& t, const StreamGemmArgs& a, int UPE, long long U,
+                                          long long stride) {
+  if (++t.pass < t.npass) return;
+  t.u += stride;
+  task_load(t, a, UPE, U);
+}
+
+// B (token rows) of one K group for this thread: row g of the pass.
+template <bool kFp4, int KG>
+__device__ __forceinline__ void load_b(uint32_t (&b)[KG][StreamCfg<kFp4>::kBRegs],
+                                       const uint16_t* bsrc, int gi, int nkb, int c) {
+#pragma unroll
+  for (int i = 0; i < KG; ++i) {
+    const int kb = gi * KG + i;
+    if constexpr (kFp4) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint4 t = make_uint4(0, 0, 0, 0);
+        if (bsrc && kb < nkb) t = *reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 128 + 32 * c + 8 * v);
+        b[i][4 * v + 0] = t.x; b[i][4 * v + 1] = t.y; b[i][4 * v + 2] = t.z; b[i][4 * v + 3] = t.w;
+      }
+    } else {
+      uint4 t = make_uint4(0, 0, 0, 0);
+      if (bsrc) t = *reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 32 + 8 * c);
+      b[i][0] = t.x; b[i][1] = t.y; b[i][2] = t.z; b[i][3] = t.w;
+    }
+  }
+}
+
+// Each warp owns whole work units (16 weight rows x all of K): no cross-warp
+// reduction.  Weights stream through a private per-thread ring in shared
+// memory filled by cp.async (each thread copies exactly the 16-byte pieces it
+// will later read, so no barrier is needed), NS-1 groups ahead of the mma,
+// across unit boundaries; the token rows (B) of the next group are loaded into
+// registers one group ahead.  Units are dealt in chunks of kWarps consecutive
+// units (one per warp, so the warps of a CTA mostly share an expert and its
+// token rows stay in L1), chunks round-robin over CTAs (so hot experts spread
+// out).  Experts with more than 8 routed rows take several passes; later
+// passes re-read the unit's weights from L2.
 template <bool kDown, bool kFp4>
-__global__ void __launch_bounds__(kThreadsPerCta, 2) stream_gemm_kernel(StreamGemmArgs a) {
-  constexpr int KB = kFp4 ? 128 : 32;       // K elements per block
-  constexpr int STEPS = KB / 16;            // mma k-steps per block
-  constexpr int KG = kFp4 ? 2 : 4;          // K blocks per load group
-  __shared__ float red[kWarpsPerCta][16][kPassRows + 1];
-  __shared__ uint32_t lut_e2m1x2[kFp4 ? 256 : 1];
-  __shared__ uint16_t lut_e4m3[kFp4 ? 256 : 1];
+__global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_kernel(StreamGemmArgs a) {
+  using C = StreamCfg<kFp4>;
+  constexpr int KB = C::KB, KG = C::KG, NS = C::NS, NW = C::kWarps;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ uint32_t lut2[kFp4 ? 256 : 1];
+  __shared__ uint16_t lut8[kFp4 ? 256 : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int K = kDown ? a.I : a.H;
   const int NR = kDown ? a.H : 2 * a.I;     // weight rows per expert
   const int UPE = kDown ? a.H / 16 : a.I / 8;
+  uint4* ring = reinterpret_cast<uint4*>(smem + warp * C::kWarpBytes);
+  uint2* sring = reinterpret_cast<uint2*>(smem + warp * C::kWarpBytes + C::kWBytes);
 
   if constexpr (kFp4) {
-    for (int i = threadIdx.x; i < 256; i += kThreadsPerCta) {
-      lut_e2m1x2[i] = pack_bf16x2(e2m1_value(i & 15), e2m1_value(i >> 4));
-      lut_e4m3[i] = f2bf(e4m3_value(i));
+    for (int i = threadIdx.x; i < 256; i += NW * 32) {
+      lut2[i] = pack_bf16x2(e2m1_value(i & 15), e2m1_value(i >> 4));
+      lut8[i] = f2bf(e4m3_value(i));
     }
     __syncthreads();
   }
 
   const int nsmall = *a.num_active - (a.num_large ? *a.num_large : 0);
   const long long U = (long long)nsmall * UPE;
-  const long long u_begin = U * blockIdx.x / gridDim.x;
-  const long long u_end = U * (blockIdx.x + 1) / gridDim.x;
-
+  const long long stride = (long long)gridDim.x * NW;
   const int nkb = K / KB;
-  const int kb_begin = nkb * warp / kWarpsPerCta;
-  const int kb_end = nkb * (warp + 1) / kWarpsPerCta;
+  const int ngroups = (nkb + KG - 1) / KG;
 
-  for (long long u = u_begin; u < u_end; ++u) {
-    const int e = a.active[u / UPE];
-    const int blk = (int)(u % UPE);
-    const int m = a.counts[e];
-    const int off = a.offsets[e];
-    int row_lo, row_hi;
-    if (kDown) { row_lo = blk * 16 + g; row_hi = blk * 16 + 8 + g; }
-    else { row_lo = blk * 8 + g; row_hi = a.I + blk * 8 + g; }
-    const size_t rlo = (size_t)e * NR + row_lo, rhi = (size_t)e * NR + row_hi;
-    float gscale = 1.0f;
-    if constexpr (kFp4) gscale = kDown ? a.dn_global[e] : a.gu_global[e];
-
-    for (int p0 = 0; p0 < m; p0 += kPassRows) {
-      // token rows of this pass held by this thread: row p0 + nt*8 + g
-      const uint16_t* bsrc[kNT];
+  // ---- producer side: the next group to copy
+  Task it;
+  it.u = (long long)blockIdx.x * NW + warp;
+  task_load(it, a, UPE, U);
+  int ig = 0;        // group index within the producer's task
+  int slot_w = 0;    // ring slot the producer fills next
+  auto issue_next = [&]() {
+    if (it.u >= 0) {
+      int rlo, rhi;
+      if (kDown) { rlo = it.blk * 16 + g; rhi = rlo + 8; }
+      else { rlo = it.blk * 8 + g; rhi = a.I + it.blk * 8 + g; }
+      const size_t Rlo = (size_t)it.e * NR + rlo, Rhi = (size_t)it.e * NR + rhi;
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        const int n = p0 + nt * 8 + g;
-        bsrc[nt] = nullptr;
-        if (n < m) {
-          if (kDown) bsrc[nt] = a.h + (size_t)(off + n) * a.I;
-          else bsrc[nt] = a.x + (size_t)(a.perm[off + n] / a.k) * a.H;
-        }
-      }
-      const int ntiles = min(kNT, (m - p0 + 7) / 8);
-      float acc[kNT][4];
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-
-      for (int kb0 = kb_begin; kb0 < kb_end; kb0 += KG) {
-        // ---- A: weights for up to KG blocks, streamed past L1
-        uint4 alo[KG], ahi[KG];
-        uint32_t slo[KG], shi[KG];
-#pragma unroll
-        for (int i = 0; i < KG; ++i) {
-          const int kb = kb0 + i;
-          if (kb < kb_end) {
-            if constexpr (kFp4) {
-              const uint8_t* cb = kDown ? a.dn_codes : a.gu_codes;
-              const uint8_t* sb = kDown ? a.dn_scales : a.gu_scales;
-              const size_t kc = (size_t)kb * 64 + 16 * c;
-              alo[i] = ldg_nc_v4(cb + rlo * (K / 2) + kc);
-              ahi[i] = ldg_nc_v4(cb + rhi * (K / 2) + kc);
-              const size_t ks = (size_t)kb * 8 + 2 * c;
-              slo[i] = *reinterpret_cast<const uint16_t*>(sb + rlo * (K / 16) + ks);
-              shi[i] = *reinterpret_cast<const uint16_t*>(sb + rhi * (K / 16) + ks);
-            } else {
-              const uint16_t* wb = kDown ? a.w_down : a.w_gate_up;
-              const size_t kc = (size_t)kb * 32 + 8 * c;
-              alo[i] = ldg_nc_v4(wb + rlo * K + kc);
-              ahi[i] = ldg_nc_v4(wb + rhi * K + kc);
-            }
+      for (int i = 0; i < KG; ++i) {
+        const int kb = ig * KG + i;
+        uint4* d = ring + ((slot_w * KG + i) * 2) * 32 + lane;
+        if constexpr (kFp4) {
+          if (kb < nkb) {
+            const uint8_t* cb = kDown ? a.dn_codes : a.gu_codes;
+            const uint8_t* sb = kDown ? a.dn_scales : a.gu_scales;
+            const size_t kc = (size_t)kb * 64 + 16 * c;
+            cp_async16(d, cb + Rlo * (K / 2) + kc);
+            cp_async16(d + 32, cb + Rhi * (K / 2) + kc);
+            uint2* ds = sring + ((slot_w * KG + i) * 2) * 32 + lane;
+            cp_async8(ds, sb + Rlo * (K / 16) + (size_t)kb * 8);
+            cp_async8(ds + 32, sb + Rhi * (K / 16) + (size_t)kb * 8);
           }
-        }
-        // ---- per n-tile: B (activations) and the mma steps
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          if (nt < ntiles) {
-#pragma unroll
-            for (int i = 0; i < KG; ++i) {
-              const int kb = kb0 + i;
-              if (kb < kb_end) {
-                if constexpr (kFp4) {
-                  uint32_t b[16];
-#pragma unroll
-                  for (int v = 0; v < 4; ++v) {
-                    uint4 t = make_uint4(0, 0, 0, 0);
-                    if (bsrc[nt]) t = *reinterpret_cast<const uint4*>(bsrc[nt] + (size_t)kb * 128 + 32 * c + 8 * v);
-                    b[4 * v + 0] = t.x; b[4 * v + 1] = t.y; b[4 * v + 2] = t.z; b[4 * v + 3] = t.w;
-                  }
-                  const uint32_t clo[4] = {alo[i].x, alo[i].y, alo[i].z, alo[i].w};
-                  const uint32_t chi[4] = {ahi[i].x, ahi[i].y, ahi[i].z, ahi[i].w};
-#pragma unroll
-                  for (int q = 0; q < STEPS; ++q) {
-                    const uint32_t sl = lut_e4m3[(slo[i] >> (q < 4 ? 0 : 8)) & 0xff];
-                    const uint32_t sh = lut_e4m3[(shi[i] >> (q < 4 ? 0 : 8)) & 0xff];
-                    const uint32_t sl2 = sl | (sl << 16), sh2 = sh | (sh << 16);
-                    const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
-                    const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
-                    const uint32_t a0 = bf16x2_mul(lut_e2m1x2[wl & 0xff], sl2);
-                    const uint32_t a2 = bf16x2_mul(lut_e2m1x2[(wl >> 8) & 0xff], sl2);
-                    const uint32_t a1 = bf16x2_mul(lut_e2m1x2[wh & 0xff], sh2);
-                    const uint32_t a3 = bf16x2_mul(lut_e2m1x2[(wh >> 8) & 0xff], sh2);
-                    mma_bf16_16816(acc[nt], a0, a1, a2, a3, b[2 * q], b[2 * q + 1]);
-                  }
-                } else {
-                  uint4 t = make_uint4(0, 0, 0, 0);
-                  if (bsrc[nt]) t = *reinterpret_cast<const uint4*>(bsrc[nt] + (size_t)kb * 32 + 8 * c);
-                  mma_bf16_16816(acc[nt], alo[i].x, ahi[i].x, alo[i].y, ahi[i].y, t.x, t.y);
-                  mma_bf16_16816(acc[nt], alo[i].z, ahi[i].z, alo[i].w, ahi[i].w, t.z, t.w);
-                }
-              }
-            }
-          }
+        } else {
+          const uint16_t* wb = kDown ? a.w_down : a.w_gate_up;
+          const size_t kc = (size_t)kb * 32 + 8 * c;
+          cp_async16(d, wb + Rlo * K + kc);
+          cp_async16(d + 32, wb + Rhi * K + kc);
         }
       }
-
-      // ---- cross-warp reduction (fixed warp order) and epilogue
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        red[warp][g][nt * 8 + 2 * c] = acc[nt][0];
-        red[warp][g][nt * 8 + 2 * c + 1] = acc[nt][1];
-        red[warp][g + 8][nt * 8 + 2 * c] = acc[nt][2];
-        red[warp][g + 8][nt * 8 + 2 * c + 1] = acc[nt][3];
-      }
-      __syncthreads();
-      if (!kDown) {
-        // thread -> (token n, feature j): 32 x 8
-        const int j = threadIdx.x & 7, n = threadIdx.x >> 3;
-        if (p0 + n < m) {
-          float gs = 0.f, us = 0.f;
-#pragma unroll
-          for (int w = 0; w < kWarpsPerCta; ++w) { gs += red[w][j][n]; us += red[w][j + 8][n]; }
-          gs *= gscale;
-          us *= gscale;
-          a.h[(size_t)(off + p0 + n) * a.I + blk * 8 + j] = f2bf(silu(gs) * us);
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int id = threadIdx.x + r * kThreadsPerCta;   // 512 = 32 tokens x 16 features
-          const int d = id & 15, n = id >> 4;
-          if (p0 + n < m) {
-            float ys = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarpsPerCta; ++w) ys += red[w][d][n];
-            ys *= gscale;
-            const int f = a.perm[off + p0 + n];
-            const float v = a.topk_w[f] * ys;
-            const size_t o = (size_t)f * a.H + blk * 16 + d;
-            if (a.partial_f32) reinterpret_cast<float*>(a.partial)[o] = v;
-            else reinterpret_cast<uint16_t*>(a.partial)[o] = f2bf(v);
-          }
-        }
-      }
-      __syncthreads();
+      if (++ig == ngroups) { ig = 0; task_next(it, a, UPE, U, stride); }
     }
+    cp_async_commit();
+    slot_w = slot_w + 1 == NS ? 0 : slot_w + 1;
+  };
+
+#pragma unroll 1
+  for (int s = 0; s < NS - 1; ++s) issue_next();
+
+  // ---- consumer side
+  Task ct;
+  ct.u = (long long)blockIdx.x * NW + warp;
+  task_load(ct, a, UPE, U);
+  int slot_r = 0;
+  while (ct.u >= 0) {
+    const int p0 = ct.pass * 8;
+    const uint16_t* bsrc = nullptr;
+    {
+      const int n = p0 + g;
+      if (n < ct.m) {
+        if (kDown) bsrc = a.h + (size_t)(ct.off + n) * a.I;
+        else bsrc = a.x + (size_t)(a.perm[ct.off + n] / a.k) * a.H;
+      }
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t bc[KG][C::kBRegs], bn[KG][C::kBRegs];
+    load_b<kFp4, KG>(bc, bsrc, 0, nkb, c);
+
+#pragma unroll 1
+    for (int gi = 0; gi < ngroups; ++gi) {
+      if (gi + 1 < ngroups) load_b<kFp4, KG>(bn, bsrc, gi + 1, nkb, c);
+      cp_async_wait<NS - 2>();
+#pragma unroll
+      for (int i = 0; i < KG; ++i) {
+        const int kb = gi * KG + i;
+        if (kFp4 && kb >= nkb) continue;
+        const uint4 alo = ring[((slot_r * KG + i) * 2) * 32 + lane];
+        const uint4 ahi = ring[((slot_r * KG + i) * 2 + 1) * 32 + lane];
+        if constexpr (kFp4) {
+          const uint2 slo8 = sring[((slot_r * KG + i) * 2) * 32 + lane];
+          const uint2 shi8 = sring[((slot_r * KG + i) * 2 + 1) * 32 + lane];
+          // this thread's two scales: bytes 2c and 2c+1 of the row's 8
+          const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1));
+          const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1));
+          const uint32_t clo[4] = {alo.x, alo.y, alo.z, alo.w};
+          const uint32_t chi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t sl = lut8[(slo >> (q < 4 ? 0 : 8)) & 0xff];
+            const uint32_t sh = lut8[(shi >> (q < 4 ? 0 : 8)) & 0xff];
+            const uint32_t sl2 = sl | (sl << 16), sh2 = sh | (sh << 16);
+            const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
+            const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
+            const uint32_t a0 = bf16x2_mul(lut2[wl & 0xff], sl2);
+            const uint32_t a2 = bf16x2_mul(lut2[(wl >> 8) & 0xff], sl2);
+            const uint32_t a1 = bf16x2_mul(lut2[wh & 0xff], sh2);
+            const uint32_t a3 = bf16x2_mul(lut2[(wh >> 8) & 0xff], sh2);
+            mma_bf16_16816(acc, a0, a1, a2, a3, bc[i][2 * q], bc[i][2 * q + 1]);
+          }
+        } else {
+          mma_bf16_16816(acc, alo.x, ahi.x, alo.y, ahi.y, bc[i][0], bc[i][1]);
+          mma_bf16_16816(acc, alo.z, ahi.z, alo.w, ahi.w, bc[i][2], bc[i][3]);
+        }
+      }
+      slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
+      issue_next();
+#pragma unroll
+      for (int i = 0; i < KG; ++i)
+#pragma unroll
+        for (int j = 0; j < C::kBRegs; ++j) bc[i][j] = bn[i][j];
+    }
+
+    // epilogue straight from the fragments: c0,c1 = row g, tokens 2c,2c+1;
+    // c2,c3 = row g+8, same tokens
+    float gscale = 1.0f;
+    if constexpr (kFp4) gscale = kDown ? a.dn_global[ct.e] : a.gu_global[ct.e];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int n = p0 + 2 * c + h2;
+      if (n < ct.m) {
+        if (!kDown) {
+          const float gv = acc[h2] * gscale, uv = acc[2 + h2] * gscale;
+          a.h[(size_t)(ct.off + n) * a.I + ct.blk * 8 + g] = f2bf(silu(gv) * uv);
+        } else {
+          const int f = a.perm[ct.off + n];
+          const float wt = a.topk_w[f];
+          const float y0 = wt * (acc[h2] * gscale), y1 = wt * (acc[2 + h2] * gscale);
+          const size_t o = (size_t)f * a.H + ct.blk * 16 + g;
+          if (a.partial_f32) {
+            reinterpret_cast<float*>(a.partial)[o] = y0;
+            reinterpret_cast<float*>(a.partial)[o + 8] = y1;
+          } else {
+            reinterpret_cast<uint16_t*>(a.partial)[o] = f2bf(y0);
+            reinterpret_cast<uint16_t*>(a.partial)[o + 8] = f2bf(y1);
+          }
+        }
+      }
+    }
+    task_next(ct, a, UPE, U, stride);
   }
+  cp_async_wait<0>();
+}
+
+template <bool kDown, bool kFp4>
+cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
+  using C = StreamCfg<kFp4>;
+  const long long S = (long long)a.T * a.k;
+  const long long max_active = S < a.E ? S : a.E;
+  const long long UPE = kDown ? a.H / 16 : a.I / 8;
+  const long long units = max_active * UPE;
+  long long grid = a.num_sms;
+  const long long need = (units + C::kWarps - 1) / C::kWarps;
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;
+  const int smem = C::kWarpBytes * C::kWarps;
+  cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<kDown, kFp4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  stream_gemm_kernel<kDown, kFp4><<<(unsigned)grid, C::kWarps * 32, smem, stream>>>(a);
+  return cudaGetLastError();
 }
 
 template <bool kDown>
 cudaError_t launch_stream(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
-  const bool fp4 = a.gu_codes != nullptr;
-  const long long S = (long long)a.T * a.k;
-  const long long max_active = S < a.E ? S : a.E;
-  const long long UPE = kDown ? a.H / 16 : a.I / 8;
-  long long units = max_active * UPE;
-  long long grid = (long long)a.num_sms * 2;
-  if (grid > units) grid = units;
-  if (grid < 1) grid = 1;
-  if (fp4) stream_gemm_kernel<kDown, true><<<(unsigned)grid, kThreadsPerCta, 0, stream>>>(a);
-  else stream_gemm_kernel<kDown, false><<<(unsigned)grid, kThreadsPerCta, 0, stream>>>(a);
-  return cudaGetLastError();
+  if (a.gu_codes != nullptr) return launch_variant<kDown, true>(a, stream);
+  return launch_variant<kDown, false>(a, stream);
 }
 
 }  // namespace
