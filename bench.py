@@ -298,6 +298,8 @@ def run_ours(args):
 
     diag = moe.read_diagnostics(ws)
     A = diag["num_active"]
+    router_diag = {"tokens_fp64_checked": diag["router_flagged"], "tokens_fp64_all": diag["router_fallback"],
+                   "experts_on_tensor_cores": diag["num_large"]}
     assert moe.read_status(ws) == 0
 
     # ---- device-timed region
@@ -394,7 +396,8 @@ def run_ours(args):
     step_ms = ms / K
     layer = {"weights_bytes": byt["weights"], "weights_gbs": byt["weights"] / (step_ms / 1e3) / 1e9,
              "weights_frac_of_hbm": byt["weights"] / (step_ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6800.0),
-             "active_experts": A, "stage_us": {s: round(stage_ms[s] * 1e3, 2) for s in STAGES}}
+             "active_experts": A, "stage_us": {s: round(stage_ms[s] * 1e3, 2) for s in STAGES},
+             "router": router_diag}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:

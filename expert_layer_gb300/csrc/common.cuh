@@ -29,7 +29,7 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte slot");
 // Offsets (bytes) of every workspace region for one shape.
 struct WsLayout {
   size_t hdr, cnt, xnorm, wnorm, logits, logits64, idx, w, counts, offsets, active, tiles, blk_cnt,
-      blk_base, lrank, perm, inv_perm, h, partial, total;
+      blk_base, lrank, perm, inv_perm, h, partial, xp, total;
   int nblk;               // 512-slot blocks of the grouping kernels
   bool partial_f32;       // fp32 partials (else bf16)
 };
@@ -65,6 +65,7 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
   L.inv_perm = take(sizeof(int) * S);
   L.h = take(sizeof(uint16_t) * S * I);
   L.partial = take((L.partial_f32 ? 4 : 2) * (size_t)S * H);
+  L.xp = take(sizeof(uint16_t) * (size_t)S * H);   // token rows in grouped order (tensor-core path)
   L.total = o;
   return L;
 }

@@ -52,6 +52,30 @@ struct StreamGemmArgs {
 cudaError_t launch_stream_gate_up(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
 cudaError_t launch_stream_down(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
 
+// tc_gemm.cu -- tcgen05/TMEM grouped GEMMs for experts with many rows (bf16 weights)
+struct TcLaunch {
+  int T, H, E, I, k;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int32_t* active;     // small-group experts first, then the large ones
+  const int32_t* tiles;      // m-tile prefix over the large experts
+  const int* num_active;
+  const int* num_large;
+  const uint16_t* x;
+  uint16_t* xp;              // [S, H] scratch: token rows in grouped order
+  const uint16_t* w_gate_up;
+  const uint16_t* w_down;
+  const float* topk_w;
+  uint16_t* h;
+  void* partial;
+  bool partial_f32;
+  int* status;
+  int num_sms;
+};
+constexpr int kTcRows = 128;             // token rows per tensor-core tile
+cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, int* launches);
+
 // combine.cu -- out[t] = sum_s partial[t*k+s] in slot order
 cudaError_t launch_combine(const void* partial, bool partial_f32, int T, int H, int k,
                            uint16_t* out, cudaStream_t stream, int* launches);

@@ -13,6 +13,9 @@ using namespace moe;
 
 namespace {
 
+// Group size from which an expert runs on the tensor-core kernels.
+constexpr int kLargeGroup = 32;
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(long long T, long long H, long long E, long long I, long long k) {
@@ -169,8 +172,12 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
   MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches));
   MOE_TRY_CUDA(mark(1));
+  // Experts with at least kLargeGroup rows go to the tensor-core kernels
+  // (bf16 weights, H a multiple of their 256-wide output tiles); a group can
+  // never exceed T rows, so small batches skip them.
+  const bool use_tc = !nvfp4 && T >= kLargeGroup && H % 256 == 0;
   MOE_TRY_CUDA(launch_permute(idx, T, E, top_k, counts, offsets, perm, inv_perm, workspace, L,
-                              INT_MAX, 128, s, launches));
+                              use_tc ? kLargeGroup : INT_MAX, kTcRows, s, launches));
   MOE_TRY_CUDA(mark(2));
 
   StreamGemmArgs a{};
@@ -191,9 +198,20 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   a.partial = ws_ptr<void>(workspace, L.partial);
   a.partial_f32 = L.partial_f32;
   a.num_sms = num_sms;
+  TcLaunch tc{};
+  tc.T = T; tc.H = H; tc.E = E; tc.I = I; tc.k = top_k;
+  tc.counts = counts; tc.offsets = offsets; tc.perm = perm; tc.active = a.active;
+  tc.tiles = ws_ptr<int32_t>(workspace, L.tiles);
+  tc.num_active = &hdr->num_active; tc.num_large = &hdr->num_large;
+  tc.x = x; tc.xp = ws_ptr<uint16_t>(workspace, L.xp); tc.w_gate_up = w_gate_up; tc.w_down = w_down; tc.topk_w = w;
+  tc.h = a.h; tc.partial = a.partial; tc.partial_f32 = L.partial_f32;
+  tc.status = &hdr->status; tc.num_sms = num_sms;
+
   MOE_TRY_CUDA(launch_stream_gate_up(a, s, launches));
+  if (use_tc) MOE_TRY_CUDA(launch_tc_gemm(tc, false, s, launches));
   MOE_TRY_CUDA(mark(3));
   MOE_TRY_CUDA(launch_stream_down(a, s, launches));
+  if (use_tc) MOE_TRY_CUDA(launch_tc_gemm(tc, true, s, launches));
   MOE_TRY_CUDA(mark(4));
   MOE_TRY_CUDA(launch_combine(a.partial, L.partial_f32, T, H, top_k, out, s, launches));
   MOE_TRY_CUDA(mark(5));

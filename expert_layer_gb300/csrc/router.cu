@@ -62,14 +62,23 @@ struct WarpScratch {
   double kmax;
 };
 
+// Two logits whose fp32 values differ by more than this are ordered like the
+// exact logits (each is within delta of its exact value).
+__device__ __forceinline__ float cert_threshold(float delta) { return 2.0f * delta * 1.001f; }
+
 // Sort key of a logit: NaN ranks below every number.
 __device__ __forceinline__ float rank_key(float v) { return v != v ? -INFINITY : v; }
 
-// Sorted candidates: cand_e/cand_v[r] = the expert of rank r (larger logit
-// first, lower index first on equal logits) for r < min(E, kCandCap).  Each
-// of the nthr cooperating threads (thread index tid) ranks its experts by
-// counting the experts that come before it -- no serial dependency chain.
-// The caller synchronises the cooperating threads before using the result.
+// (v, e) ordering: larger value first, lower index first on equal values.
+__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
+  return v > bv || (v == bv && e < be);
+}
+
+// Sorted candidates for E > 128: cand_e/cand_v[r] = the expert of rank r
+// (larger logit first, lower index first on equal logits) for
+// r < min(E, kCandCap).  Each of the nthr cooperating threads (index tid)
+// ranks its experts by counting the experts that come before it.  The
+// caller synchronises the cooperating threads before using the result.
 __device__ void rank_candidates(const float* L, int E, WarpScratch& sc, int tid, int nthr) {
   for (int e = tid; e < E; e += nthr) {
     const float v = rank_key(L[e]);
@@ -89,32 +98,79 @@ __device__ void rank_candidates(const float* L, int E, WarpScratch& sc, int tid,
   }
 }
 
-// Certified top-k of one token from its sorted candidates.  Whole warp.
-// Writes idx_out[0..k) and w_out[0..k).
-__device__ void select_token(int E, int k, float delta, const uint16_t* xrow,
+// End of the certain set from fully ranked candidates: the first rank
+// j >= k-1 whose gap to rank j+1 exceeds thr; everything below it is
+// certainly below.  Returns -1 when no such rank lies within kCandCap.
+__device__ int certain_end_ranked(const WarpScratch& sc, int E, int k, float thr) {
+  const int lane = threadIdx.x & 31;
+  const int nc = E < kCandCap ? E : kCandCap;
+  int j = lane;
+  bool ok = j >= k - 1 && j + 1 < nc && sc.cand_v[j] - sc.cand_v[j + 1] > thr;
+  const unsigned g0 = __ballot_sync(0xffffffffu, ok);
+  j = lane + 32;
+  ok = j >= k - 1 && j + 1 < nc && sc.cand_v[j] - sc.cand_v[j + 1] > thr;
+  const unsigned g1 = __ballot_sync(0xffffffffu, ok);
+  if (g0) return __ffs(g0) - 1;
+  if (g1) return __ffs(g1) - 1 + 32;
+  return E <= kCandCap ? E - 1 : -1;
+}
+
+// Sorted candidates for E <= 128, extracted in rank order until the certain
+// set is closed.  Each lane keeps its (up to) four logits sorted in
+// registers; a round is one warp arg-max over the lanes' current heads.
+// Writes cand_e/cand_v[0..end+1] and returns end (or -1 for the fallback).
+__device__ int extract_small(const float* L, int E, int k, float thr, WarpScratch& sc) {
+  const int lane = threadIdx.x & 31;
+  float v[4];
+  int id[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = lane + 32 * i;
+    id[i] = e < E ? e : INT_MAX;
+    v[i] = e < E ? rank_key(L[e]) : -INFINITY;
+  }
+  // sort the four (v, id) pairs, best first (5-comparator network)
+#define MOE_CSWAP(a, b)                                                        \
+  if (better(v[b], id[b], v[a], id[a])) {                                      \
+    const float tv = v[a]; v[a] = v[b]; v[b] = tv;                             \
+    const int ti = id[a]; id[a] = id[b]; id[b] = ti;                           \
+  }
+  MOE_CSWAP(0, 1) MOE_CSWAP(2, 3) MOE_CSWAP(0, 2) MOE_CSWAP(1, 3) MOE_CSWAP(1, 2)
+#undef MOE_CSWAP
+  int head = 0;
+  float prev = 0.f;
+  for (int r = 0; r < kCandCap; ++r) {
+    float bv = head == 0 ? v[0] : head == 1 ? v[1] : head == 2 ? v[2] : head == 3 ? v[3] : -INFINITY;
+    int be = head == 0 ? id[0] : head == 1 ? id[1] : head == 2 ? id[2] : head == 3 ? id[3] : INT_MAX;
+    const int mylane = lane;
+    int bl = mylane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      if (better(ov, oe, bv, be)) { bv = ov; be = oe; bl = ol; }
+    }
+    if (lane == bl) ++head;
+    if (lane == 0) { sc.cand_e[r] = be; sc.cand_v[r] = bv; }
+    if (r >= k && prev - bv > thr) return r - 1;   // gap closes the certain set
+    if (r + 1 == E) return r;                       // every expert extracted
+    prev = bv;
+  }
+  return -1;
+}
+
+// Certified top-k of one token from its sorted candidates cand[0..end] (the
+// certain set) -- or, when fallback is set, from fp64 logits of every expert.
+// Whole warp.  Writes idx_out[0..k) and w_out[0..k).
+__device__ void select_token(int E, int k, float delta, int end, const uint16_t* xrow,
                              const uint16_t* gate_w, const float* bias, int H, double* l64_row,
                              WarpScratch& sc, int32_t* idx_out, float* w_out, WsHeader* hdr) {
   const int lane = threadIdx.x & 31;
   const int per_lane = (E + 31) >> 5;
-  const int nc = E < kCandCap ? E : kCandCap;
-  const float thr = 2.0f * delta * 1.001f;
-  // The certain set ends at the first rank j >= k-1 whose gap to rank j+1
-  // exceeds 2*delta: everything below is certainly below it.
-  unsigned gap0, gap1;
-  {
-    int j = lane;
-    bool ok = j >= k - 1 && j + 1 < nc && sc.cand_v[j] - sc.cand_v[j + 1] > thr;
-    gap0 = __ballot_sync(0xffffffffu, ok);
-    j = lane + 32;
-    ok = j >= k - 1 && j + 1 < nc && sc.cand_v[j] - sc.cand_v[j + 1] > thr;
-    gap1 = __ballot_sync(0xffffffffu, ok);
-  }
-  int end;
-  bool fallback = false;
-  if (gap0) end = __ffs(gap0) - 1;
-  else if (gap1) end = __ffs(gap1) - 1 + 32;
-  else if (E <= kCandCap) end = E - 1;
-  else { end = -1; fallback = true; }
+  const float thr = cert_threshold(delta);
+  const bool fallback = end < 0;
+  __syncwarp();
 
   if (!fallback) {
     // Ambiguous candidates: members of an adjacent pair closer than 2*delta.
@@ -130,7 +186,22 @@ __device__ void select_token(int E, int k, float delta, const uint16_t* xrow,
     }
     const unsigned bal0 = __ballot_sync(0xffffffffu, amb0);
     const unsigned bal1 = __ballot_sync(0xffffffffu, amb1);
-    if (lane == 0 && (bal0 | bal1)) atomicAdd(&hdr->router_flagged, 1);
+    if ((bal0 | bal1) == 0) {
+      // the fp32 order is certain: ranks are the candidate positions
+      if (lane < k) {
+        idx_out[lane] = sc.cand_e[lane];
+        sc.ex[lane] = expf(sc.cand_v[lane] - sc.cand_v[0]);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        float sum = 0.0f;
+        for (int s = 0; s < k; ++s) sum += sc.ex[s];
+        for (int s = 0; s < k; ++s) w_out[s] = sc.ex[s] / sum;
+      }
+      __syncwarp();
+      return;
+    }
+    if (lane == 0) atomicAdd(&hdr->router_flagged, 1);
     for (int r = 0; r < 2; ++r) {
       const int i = lane + 32 * r;
       if (i <= end) sc.key[i] = (double)sc.cand_v[i];
@@ -264,11 +335,13 @@ __global__ void __launch_bounds__(256) router_small_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // last CTA of token t: logits to shared memory, ranked by all its threads
+  // last CTA of token t: logits to shared memory, certified selection
   for (int ee = threadIdx.x; ee < E; ee += blockDim.x) sl[ee] = __ldcg(&logits[(size_t)t * E + ee]);
   __syncthreads();
-  rank_candidates(sl, E, scr, threadIdx.x, blockDim.x);
-  __syncthreads();
+  if (E > 128) {   // many experts: every thread of the CTA helps rank them
+    rank_candidates(sl, E, scr, threadIdx.x, blockDim.x);
+    __syncthreads();
+  }
   if (warp != 0) return;
   // ||x_t||, max ||w_e||, max |logit| for the error bound
   float sqx = 0.f;
@@ -294,26 +367,26 @@ __global__ void __launch_bounds__(256) router_small_kernel(
   }
   const float delta = gamma_bound(gamma_terms) * sqrtf(sqx) * wmax * (1.0f + 0x1p-10f) +
                       0x1p-22f * lmax + (float)H * 0x1p-149f;
-  select_token(E, k, delta, xr, gw, bias, H, l64 + (size_t)t * E, scr, idx + (size_t)t * k,
+  const float thr = cert_threshold(delta);
+  const int end = E <= 128 ? extract_small(sl, E, k, thr, scr) : certain_end_ranked(scr, E, k, thr);
+  select_token(E, k, delta, end, xr, gw, bias, H, l64 + (size_t)t * E, scr, idx + (size_t)t * k,
                w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
 }
 
 // ------------------------------------------------------------ large batches
-// One CTA = 64 tokens x all E (<= 128) experts, 128 threads; thread (ty, tx)
-// owns tokens 8ty..8ty+7 and experts 8tx..8tx+7.  K runs in chunks of 64: a
-// chunk's 64 products are summed sequentially from zero (63 roundings) and
-// the chunk sum is added to the running total (H/64 additions): at most
-// 64 + H/64 roundings per product.
-constexpr int kTileT = 64, kTileE = 128, kTileK = 64;
+// Logits: one CTA = 32 tokens x all E (<= 128) experts, 128 threads; thread
+// (ty, tx) owns tokens 4ty..4ty+3 and experts 4tx..4tx+3, 64+4tx..64+4tx+3.  K runs in chunks of
+// 64: a chunk's 64 products are summed sequentially from zero (63 roundings)
+// and the chunk sum is added to the running total (H/64 additions): at most
+// 64 + H/64 roundings per product.  Selection then runs one warp per token.
+constexpr int kTileT = 32, kTileE = 128, kTileK = 64;
 
 __global__ void __launch_bounds__(128) router_tile_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
-    int T, int H, int E, int k, int gamma_terms, const float* __restrict__ wnorm,
-    double* __restrict__ l64, int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
+    int T, int H, int E, float* __restrict__ logits, float* __restrict__ xnorm) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* xs = reinterpret_cast<float*>(smem_raw);           // [2][kTileK][kTileT]
   float* wsm = xs + 2 * kTileK * kTileT;                    // [2][kTileK][kTileE]
-  __shared__ float s_xnorm[kTileT];
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
   const int t0 = blockIdx.x * kTileT;
@@ -321,8 +394,7 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
 
   // ||x_t|| for the tile's tokens: warp-level sums (H/32 + 4 roundings).
   for (int i = 0; i < kTileT / 4; ++i) {
-    const int tl = warp * (kTileT / 4) + i;
-    const int t = t0 + tl;
+    const int t = t0 + warp * (kTileT / 4) + i;
     float sq = 0.f;
     if (t < T) {
       for (int h = lane * 8; h < H; h += 256) {
@@ -337,18 +409,21 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0) s_xnorm[tl] = sqrtf(sq);
+    if (lane == 0 && t < T) xnorm[t] = sqrtf(sq);
   }
 
-  // Global -> register staging of one K chunk: x tile 64x64 (4 uint4 per
+  // Global -> register staging of one K chunk: x tile 32x64 (2 uint4 per
   // thread), w tile 128x64 (8 uint4 per thread), transposed into [k][row].
-  uint4 rx[4], rw[8];
+  uint4 rx[2], rw[8];
   auto load_chunk = [&](int kc) {
     const int k0 = kc * kTileK;
+    // vector v covers row v % rows, columns 8*(v / rows) .. +7, so that the
+    // 32 lanes of a warp hold 32 consecutive rows of one column group and the
+    // transposed shared-memory stores below hit 32 distinct banks
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int v = tid + 128 * i;          // 512 vectors: row v/8, col (v%8)*8
-      const int row = v >> 3, col = (v & 7) * 8;
+    for (int i = 0; i < 2; ++i) {
+      const int v = tid + 128 * i;          // 256 vectors
+      const int row = v % kTileT, col = (v / kTileT) * 8;
       const int t = t0 + row;
       rx[i] = (t < T) ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + col)
                       : make_uint4(0, 0, 0, 0);
@@ -356,7 +431,7 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int v = tid + 128 * i;          // 1024 vectors
-      const int row = v >> 3, col = (v & 7) * 8;
+      const int row = v % kTileE, col = (v / kTileE) * 8;
       rw[i] = (row < E) ? *reinterpret_cast<const uint4*>(gw + (size_t)row * H + k0 + col)
                         : make_uint4(0, 0, 0, 0);
     }
@@ -365,9 +440,9 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
     float* xb = xs + buf * kTileK * kTileT;
     float* wb = wsm + buf * kTileK * kTileE;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       const int v = tid + 128 * i;
-      const int row = v >> 3, col = (v & 7) * 8;
+      const int row = v % kTileT, col = (v / kTileT) * 8;
       const uint32_t u[4] = {rx[i].x, rx[i].y, rx[i].z, rx[i].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -378,7 +453,7 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int v = tid + 128 * i;
-      const int row = v >> 3, col = (v & 7) * 8;
+      const int row = v % kTileE, col = (v / kTileE) * 8;
       const uint32_t u[4] = {rw[i].x, rw[i].y, rw[i].z, rw[i].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -388,9 +463,9 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
     }
   };
 
-  float tot[8][8];
+  float tot[4][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) tot[i][j] = 0.f;
 
@@ -401,66 +476,76 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
   for (int kc = 0; kc < nchunks; ++kc) {
     const int buf = kc & 1;
     if (kc + 1 < nchunks) load_chunk(kc + 1);
-    const float* xb = xs + buf * kTileK * kTileT + ty * 8;
-    const float* wb = wsm + buf * kTileK * kTileE + tx * 8;
-    float part[8][8];
+    const float* xb = xs + buf * kTileK * kTileT + ty * 4;
+    // thread tx owns experts 4tx..4tx+3 and 64+4tx..64+4tx+3: a quarter-warp
+    // then reads 128 contiguous bytes per vector load (no bank conflicts)
+    const float* wb = wsm + buf * kTileK * kTileE + tx * 4;
+    float part[4][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) part[i][j] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int kk = 0; kk < kTileK; ++kk) {
       const float4 xa = *reinterpret_cast<const float4*>(xb + kk * kTileT);
-      const float4 xb4 = *reinterpret_cast<const float4*>(xb + kk * kTileT + 4);
       const float4 wa = *reinterpret_cast<const float4*>(wb + kk * kTileE);
-      const float4 wb4 = *reinterpret_cast<const float4*>(wb + kk * kTileE + 4);
-      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb4.x, xb4.y, xb4.z, xb4.w};
+      const float4 wb4 = *reinterpret_cast<const float4*>(wb + kk * kTileE + 64);
+      const float xv[4] = {xa.x, xa.y, xa.z, xa.w};
       const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb4.x, wb4.y, wb4.z, wb4.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) tot[i][j] += part[i][j];
     if (kc + 1 < nchunks) store_chunk(buf ^ 1);
     __syncthreads();
   }
-
-  // Logits to shared memory [64][E+1] (reusing the staging buffers).
-  const int ld = kTileE + 4;   // rows stay 16-byte aligned for the ranking
-  float* sl = xs;
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int e = tx * 8 + j;
-      if (e < E) sl[(ty * 8 + i) * ld + e] = bias ? tot[i][j] + bias[e] : tot[i][j];
+      const int e = (j < 4 ? 0 : 64) + tx * 4 + (j & 3);
+      if (e < E) logits[(size_t)t * E + e] = bias ? tot[i][j] + bias[e] : tot[i][j];
     }
-  __syncthreads();
-  WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem_raw + sizeof(float) * kTileT * ld + 256);
-  float wmax = 0.f;
-  for (int e = lane; e < E; e += 32) wmax = fmaxf(wmax, wnorm[e]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-  for (int i = 0; i < kTileT / 4; ++i) {
-    const int tl = warp * (kTileT / 4) + i;
-    const int t = t0 + tl;
-    if (t >= T) break;
-    const float* row = sl + tl * ld;
-    float lmax = 0.f;
-    for (int e = lane; e < E; e += 32) lmax = fmaxf(lmax, fabsf(row[e]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
-    const float delta = gamma_bound(gamma_terms) * s_xnorm[tl] * wmax * (1.0f + 0x1p-10f) +
-                        0x1p-22f * lmax + (float)H * 0x1p-149f;
-    rank_candidates(row, E, scr[warp], lane, 32);
-    __syncwarp();
-    select_token(E, k, delta, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, scr[warp],
-                 idx + (size_t)t * k, w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
   }
+}
+
+// Selection for the tiled path: one warp per token.
+__global__ void __launch_bounds__(256) router_select_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
+    int T, int H, int E, int k, int gamma_terms, const float* __restrict__ logits,
+    const float* __restrict__ xnorm, const float* __restrict__ wnorm, double* __restrict__ l64,
+    int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem_raw);
+  float* sl = reinterpret_cast<float*>(smem_raw + sizeof(WarpScratch) * 8) + (size_t)warp * E;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float wmax = 0.f, lmax = 0.f;
+  for (int e = lane; e < E; e += 32) {
+    const float v = logits[(size_t)t * E + e];
+    sl[e] = v;
+    wmax = fmaxf(wmax, wnorm[e]);
+    lmax = fmaxf(lmax, fabsf(v));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+  }
+  __syncwarp();
+  const float delta = gamma_bound(gamma_terms) * xnorm[t] * wmax * (1.0f + 0x1p-10f) +
+                      0x1p-22f * lmax + (float)H * 0x1p-149f;
+  const int end = extract_small(sl, E, k, cert_threshold(delta), scr[warp]);   // E <= 128 here
+  select_token(E, k, delta, end, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, scr[warp],
+               idx + (size_t)t * k, w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
 }
 
 // ||w_e|| for every expert, one warp per expert.
@@ -491,19 +576,24 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
   float* wnorm = ws_ptr<float>(ws, L.wnorm);
   double* l64 = ws_ptr<double>(ws, L.logits64);
   const bool tiled = T >= 2048 && E <= kTileE;
-  if (launches) *launches += tiled ? 2 : 1;
+  if (launches) *launches += tiled ? 3 : 1;
   if (tiled) {
+    float* logits = ws_ptr<float>(ws, L.logits);
+    float* xnorm = ws_ptr<float>(ws, L.xnorm);
     wnorm_kernel<<<(E + 7) / 8, 256, 0, stream>>>(gate_w, H, E, wnorm);
     const size_t smem = sizeof(float) * 2 * kTileK * (kTileT + kTileE);
-    static_assert(sizeof(float) * kTileT * (kTileE + 4) + 256 + 4 * sizeof(WarpScratch) <=
-                      sizeof(float) * 2 * kTileK * (kTileT + kTileE),
-                  "selection scratch fits in the staging buffers");
     cudaError_t err = cudaFuncSetAttribute(router_tile_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
+    router_tile_kernel<<<(T + kTileT - 1) / kTileT, 128, smem, stream>>>(x, gate_w, bias, T, H, E,
+                                                                         logits, xnorm);
+    const size_t smem2 = sizeof(WarpScratch) * 8 + sizeof(float) * 8 * E;
+    err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem2);
+    if (err != cudaSuccess) return err;
     const int gterms = kTileK + H / kTileK + 1;
-    router_tile_kernel<<<(T + kTileT - 1) / kTileT, 128, smem, stream>>>(
-        x, gate_w, bias, T, H, E, k, gterms, wnorm, l64, idx, w, ws);
+    router_select_kernel<<<(T + 7) / 8, 256, smem2, stream>>>(x, gate_w, bias, T, H, E, k, gterms,
+                                                              logits, xnorm, wnorm, l64, idx, w, ws);
     return cudaGetLastError();
   }
   float* logits = ws_ptr<float>(ws, L.logits);

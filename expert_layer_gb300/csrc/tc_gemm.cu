@@ -1,0 +1,462 @@
+// Tensor-core grouped expert GEMMs for large groups (prefill-sized).
+//
+// The "expert kernel" and "activation" phases of the fused-MoE path (page
+// "Decode 吞吐专项实验分析报告", section "下一步 profiling 方向", item 3) for
+// experts that hold many routed rows, where the grouped GEMM is bound by the
+// tensor cores.  Grouping stays on the device (page "第 9 章 prefill：最大的瓶颈",
+// sec. 9.9): tile lists come from the grouping kernels' counts, no host sync.
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0      producer: tiled TMA loads into a 4-stage shared-memory ring:
+//               token rows in grouped order (x gathered through the grouped
+//               permutation by gather_rows, or h) and weight rows
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16 x bf16 -> fp32
+//               in TMEM), M = 128 token rows, N = 256, K = 16 per instruction
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, SwiGLU (gate/up) or
+//               routing-weight scaling (down), stores to global memory
+// TMEM holds two 128 x 256 fp32 accumulators, so the epilogue of one tile
+// overlaps the mainloop of the next.
+//
+// gate/up tile: 128 rows x (128 gate columns j0.. + the matching 128 up
+//               columns I+j0..) over K = H; h[r, j] = bf16(silu(g) * u)
+// down tile:    128 rows x 256 output features over K = I;
+//               partial[f, d] = topk_w[f] * y  (stored at the slot's own row)
+//
+// Operands are K-major with the 128-byte swizzle: TMA writes them in that
+// layout and the UMMA shared-memory descriptors describe it (8-row groups
+// 1024 bytes apart; the K step inside a 128-byte row advances the start
+// address by 32 bytes).
+//
+// Every wait on an mbarrier is bounded; on a timeout the CTA records
+// kStatusTimeout in the workspace status word and leaves its loops.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, NS = 4;
+constexpr int kTileBytesA = BM * BK * 2;                // 16 KB
+constexpr int kTileBytesB = BN * BK * 2;                // 32 KB
+constexpr int kStageBytes = kTileBytesA + kTileBytesB;  // 48 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;                     // two 256-column accumulators
+constexpr uint32_t kSpinLimit = 1u << 22;   // ~1 s of failed tries
+constexpr int kMaxLarge = 1024;
+// stages + alignment slack + barriers + tile metadata (4 int arrays of kMaxLarge+1)
+constexpr size_t kSmemBytes = (size_t)NS * kStageBytes + 1024 + 256 + 4 * 4 * (kMaxLarge + 1);
+
+struct TcArgs {
+  int T, H, E, I, k;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int32_t* active;
+  const int32_t* tiles;
+  const int* num_active;
+  const int* num_large;
+  const float* topk_w;
+  uint16_t* h;
+  void* partial;
+  int partial_f32;
+  int* status;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false after kSpinLimit unsuccessful tries.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Lane 0 waits, the warp follows its verdict (a warp-uniform result).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);          // start address
+  d |= (uint64_t)1 << 16;                           // leading byte offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
+  d |= (uint64_t)1 << 46;                           // descriptor version
+  d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16, bf16 A/B, fp32 D, K-major A and B.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum));
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Per-CTA copy of the large-expert tile metadata (shared memory).
+struct TileMeta {
+  int* tiles;   // [nlarge+1] m-tile prefix
+  int* e;       // [nlarge] expert id
+  int* m;       // [nlarge] rows
+  int* off;     // [nlarge] first grouped row
+};
+
+// Tile t -> (expert, n-tile, m-tile) in (expert, n, m) order, so that
+// co-running CTAs share an expert's weight tile through L2.
+struct TileInfo {
+  int e, m, off, mtile, ntile;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const TileMeta& md, int nlarge, int NTN, int t) {
+  int lo = 0, hi = nlarge;  // find i with tiles[i]*NTN <= t < tiles[i+1]*NTN
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (md.tiles[mid] * NTN <= t) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  const int mt = md.tiles[lo + 1] - md.tiles[lo];
+  const int local = t - md.tiles[lo] * NTN;
+  ti.e = md.e[lo];
+  ti.m = md.m[lo];
+  ti.off = md.off[lo];
+  ti.ntile = local / mt;
+  ti.mtile = local % mt;
+  return ti;
+}
+
+template <bool kDown>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * kStageBytes);
+  uint64_t* empty = full + NS;
+  uint64_t* tfull = empty + NS;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  TileMeta md;
+  md.tiles = reinterpret_cast<int*>(smem + NS * kStageBytes + 256);
+  md.e = md.tiles + (kMaxLarge + 1);
+  md.m = md.e + (kMaxLarge + 1);
+  md.off = md.m + (kMaxLarge + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nlarge = *a.num_large;
+  const int nsmall = *a.num_active - nlarge;
+  const int NTN = kDown ? a.H / BN : a.I / (BN / 2);
+  const int total = a.tiles[nlarge] * NTN;
+  const int K = kDown ? a.I : a.H;
+  const int nkb = K / BK;
+  if ((int)blockIdx.x >= total) return;   // uniform for the whole CTA
+
+  for (int i = threadIdx.x; i <= nlarge; i += kThreads) {
+    md.tiles[i] = a.tiles[i];
+    if (i < nlarge) {
+      const int e = a.active[nsmall + i];
+      md.e[i] = e;
+      md.m[i] = a.counts[e];
+      md.off[i] = a.offsets[e];
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile(md, nlarge, NTN, t);
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % NS;
+        const uint32_t ph = (it / NS) & 1;
+        if (!warp_wait(&empty[s], ph ^ 1)) { atomicOr(abort_flag, 1); break; }
+        if (lane == 0) {
+          unsigned char* sA = smem + s * kStageBytes;
+          unsigned char* sB = sA + kTileBytesA;
+          mbar_expect_tx(&full[s], kStageBytes);
+          tma_load_2d(sA, &tmA, kb * BK, ti.off + ti.mtile * BM, &full[s]);
+          if (kDown) {
+            tma_load_2d(sB, &tmB, kb * BK, ti.e * a.H + ti.ntile * BN, &full[s]);
+          } else {
+            const int row0 = ti.e * 2 * a.I + ti.ntile * (BN / 2);
+            tma_load_2d(sB, &tmB, kb * BK, row0, &full[s]);
+            tma_load_2d(sB + kTileBytesB / 2, &tmB, kb * BK, row0 + a.I, &full[s]);
+          }
+        }
+        __syncwarp();
+      }
+      if (*(volatile int*)abort_flag) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t it = 0, lt = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+      const uint32_t b = lt & 1;
+      const uint32_t tph = (lt >> 1) & 1;
+      if (!warp_wait(&tempty[b], tph ^ 1)) { atomicOr(abort_flag, 1); break; }
+      tc_fence_after();
+      const uint32_t tmem_d = tmem_base + b * BN;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % NS;
+        const uint32_t ph = (it / NS) & 1;
+        if (!warp_wait(&full[s], ph)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sA = smem_u32(smem + s * kStageBytes);
+          const uint32_t sB = sA + kTileBytesA;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(tmem_d, umma_desc(sA + kk * 32), umma_desc(sB + kk * 32),
+                      (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[s]);   // frees the stage when these MMAs finish reading it
+        }
+        __syncwarp();
+      }
+      if (!ok) { atomicOr(abort_flag, 1); break; }
+      if (lane == 0) umma_commit(&tfull[b]);   // accumulator ready
+      __syncwarp();
+      if (*(volatile int*)abort_flag) break;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;              // TMEM lane quadrant of this warp
+    const int row = q * 32 + lane;       // accumulator row = TMEM lane
+    uint32_t lt = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+      const uint32_t b = lt & 1;
+      const uint32_t tph = (lt >> 1) & 1;
+      if (!mbar_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
+      tc_fence_after();
+      const TileInfo ti = decode_tile(md, nlarge, NTN, t);
+      const int r = ti.mtile * BM + row;   // row within the expert's group
+      const bool live = r < ti.m;
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+      if (!kDown) {
+        uint16_t* dst = a.h + (size_t)(ti.off + r) * a.I + ti.ntile * (BN / 2);
+#pragma unroll 1
+        for (int cchunk = 0; cchunk < 4; ++cchunk) {
+          uint32_t gv[32], uv[32];
+          tmem_ld32(tb + cchunk * 32, gv);
+          tmem_ld32(tb + BN / 2 + cchunk * 32, uv);
+          tmem_wait_ld();
+          if (live) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
+              const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
+              pk[j] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cchunk * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      } else {
+        int f = 0;
+        float wt = 0.f;
+        if (live) { f = a.perm[ti.off + r]; wt = a.topk_w[f]; }
+        const size_t obase = (size_t)f * a.H + ti.ntile * BN;
+#pragma unroll 1
+        for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
+          uint32_t yv[32];
+          tmem_ld32(tb + cchunk * 32, yv);
+          tmem_wait_ld();
+          if (live) {
+            if (a.partial_f32) {
+              float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.partial) + obase + cchunk * 32);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                d4[v] = make_float4(wt * __uint_as_float(yv[4 * v]), wt * __uint_as_float(yv[4 * v + 1]),
+                                    wt * __uint_as_float(yv[4 * v + 2]), wt * __uint_as_float(yv[4 * v + 3]));
+            } else {
+              uint32_t pk[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                pk[j] = pack_bf16x2(wt * __uint_as_float(yv[2 * j]), wt * __uint_as_float(yv[2 * j + 1]));
+              uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.partial) + obase + cchunk * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[b]);
+      if (*(volatile int*)abort_flag) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.status, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols));
+  }
+}
+
+// Token rows in grouped order: xp[r] = x[perm[r] / k], one warp per row,
+// 16-byte vectors (x stays in L2; this is one streaming write of S*H bf16).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ perm, int S,
+                                                          int H, int k, uint16_t* __restrict__ xp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (long long r = (long long)blockIdx.x * 8 + warp; r < S; r += (long long)gridDim.x * 8) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(perm[r] / k) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * H);
+    for (int v = lane; v < H / 8; v += 32) dst[v] = src[v];
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;   // resolved once; a pure function pointer
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, int* launches) {
+  TcArgs a{};
+  a.T = p.T; a.H = p.H; a.E = p.E; a.I = p.I; a.k = p.k;
+  a.counts = p.counts; a.offsets = p.offsets; a.perm = p.perm; a.active = p.active;
+  a.tiles = p.tiles; a.num_active = p.num_active; a.num_large = p.num_large;
+  a.topk_w = p.topk_w; a.h = p.h; a.partial = p.partial; a.partial_f32 = p.partial_f32 ? 1 : 0;
+  a.status = p.status;
+  const long long S = (long long)p.T * p.k;
+  if (!down) {
+    const long long blocks = (S + 7) / 8;
+    gather_rows_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
+        p.x, p.perm, (int)S, p.H, p.k, p.xp);
+    if (launches) *launches += 1;
+  }
+  CUtensorMap tmA, tmB;
+  if (!down) {
+    if (!make_map(&tmA, p.xp, S, p.H, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, p.w_gate_up, (uint64_t)p.E * 2 * p.I, p.H, BN / 2)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_map(&tmA, p.h, S, p.I, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, p.w_down, (uint64_t)p.E * p.H, p.I, BN)) return cudaErrorInvalidValue;
+  }
+  const size_t smem = kSmemBytes;
+  cudaError_t err;
+  if (down) err = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  else err = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  if (launches) *launches += 1;
+  const int grid = p.num_sms;
+  if (down) tc_gemm_kernel<true><<<grid, kThreads, smem, stream>>>(tmA, tmB, a);
+  else tc_gemm_kernel<false><<<grid, kThreads, smem, stream>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -42,6 +42,10 @@ SMALL_CASES = {
     "E1024_k32": dict(T=16, H=256, E=1024, k=32, I=128),
     "zipf": dict(T=50, H=512, E=32, k=4, I=256, bias="zipf"),
     "nvfp4_small": dict(T=24, H=256, E=8, k=2, I=128, nvfp4=True),
+    # groups of >= 64 rows run on the tcgen05 kernels
+    "tc_all": dict(T=512, H=256, E=8, k=2, I=128),
+    "tc_mixed": dict(T=300, H=512, E=16, k=2, I=256, bias="zipf"),
+    "tc_ragged": dict(T=200, H=256, E=2, k=1, I=384),
 }
 
 
@@ -51,6 +55,8 @@ def test_forward_small(name):
     inp = _small(c["T"], c["H"], c["E"], c["k"], c["I"], bias=c.get("bias"), nvfp4=c.get("nvfp4", False))
     out, idx, w, ws = gh.run_forward(inp)
     assert moe.read_status(ws) == 0
+    if name.startswith("tc_"):
+        assert moe.read_diagnostics(ws)["num_large"] > 0
     orc = oracle.forward_from_inputs(inp)
     gh.check_routing(inp, idx, w, orc)
     gh.check_output(inp, out, orc)
