@@ -15,6 +15,7 @@ namespace {
 template <bool kF32>
 __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ partial, int T, int H,
                                                       int k, uint16_t* __restrict__ out) {
+  pdl_wait();   // the partials of the down projection are complete
   const long long nvec = (long long)T * (H / 8);
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < nvec;
        v += (long long)gridDim.x * blockDim.x) {
@@ -51,9 +52,19 @@ cudaError_t launch_combine(const void* partial, bool partial_f32, int T, int H, 
   const long long nvec = (long long)T * (H / 8);
   long long grid = (nvec + 255) / 256;
   if (grid > 152 * 8) grid = 152 * 8;
-  if (partial_f32) combine_kernel<true><<<(unsigned)grid, 256, 0, stream>>>(partial, T, H, k, out);
-  else combine_kernel<false><<<(unsigned)grid, 256, 0, stream>>>(partial, T, H, k, out);
-  return cudaGetLastError();
+  // programmatic launch: the combine's CTAs may become resident while the down
+  // projection finishes and start the moment it completes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (partial_f32) return cudaLaunchKernelEx(&cfg, combine_kernel<true>, partial, T, H, k, out);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<false>, partial, T, H, k, out);
 }
 
 }  // namespace moe

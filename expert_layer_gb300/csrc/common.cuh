@@ -22,7 +22,8 @@ struct WsHeader {
   int num_large;          // active experts served by the tensor-core path
   int router_flagged;     // tokens whose ranking needed fp64 logits
   int router_fallback;    // tokens that needed fp64 logits for every expert
-  int pad[59];
+  int tokens_done;        // tokens whose top-k is final (fused grouping)
+  int pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte slot");
 
@@ -110,6 +111,12 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
                : "l"(p));
   return r;
 }
+
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible (a no-op for a normal launch), and
+// allow the next kernel in the stream to start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void set_status(void* ws, int bit) {
   atomicOr(&reinterpret_cast<WsHeader*>(ws)->status, bit);

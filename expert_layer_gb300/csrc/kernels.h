@@ -11,10 +11,20 @@
 
 namespace moe {
 
-// router.cu -- logits, certified top-k, renormalised weights
+// Outputs of the grouping when it runs fused into the small-batch router.
+struct GroupOut {
+  int32_t *counts, *offsets, *perm, *inv_perm, *active, *tiles;
+  int large_threshold, tile_rows;
+  int* zero;     // int region cleared by the grouping CTA (may be null)
+  int nzero;
+};
+
+// router.cu -- logits, certified top-k, renormalised weights; with `group`
+// (only where route_can_group) also the grouping, in the same launch
+bool route_can_group(int T, int E, int k);
 cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
                          int E, int k, int32_t* idx, float* w, void* ws, const WsLayout& L,
-                         cudaStream_t stream, int* launches);
+                         cudaStream_t stream, int* launches, const GroupOut* group);
 
 // permute.cu -- histogram, exclusive scan, stable permutation, active list
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* counts,

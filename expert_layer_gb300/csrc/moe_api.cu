@@ -13,8 +13,11 @@ using namespace moe;
 
 namespace {
 
-// Group size from which an expert runs on the tensor-core kernels.
-constexpr int kLargeGroup = 32;
+// Group size from which an expert runs on the tensor-core kernels: at
+// prefill sizes a 32-row group already pays for a 128-row tile; at decode
+// sizes the streaming kernels serve groups of up to 64 rows better.
+constexpr int kLargeGroupPrefill = 32;
+constexpr int kLargeGroupDecode = 65;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -101,7 +104,8 @@ int moe_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
   return cuda_status(
-      launch_route(x, gate_w, bias, T, H, E, top_k, topk_idx, topk_w, workspace, L, s, nullptr));
+      launch_route(x, gate_w, bias, T, H, E, top_k, topk_idx, topk_w, workspace, L, s, nullptr,
+                   nullptr));
 }
 
 int moe_permute(const int32_t* topk_idx, int T, int E, int top_k, int32_t* counts,
@@ -168,17 +172,30 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   auto mark = [&](int i) -> cudaError_t {
     return events ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
   };
+  // Experts with at least `large` rows go to the tensor-core kernels (bf16
+  // weights, H a multiple of their 256-wide output tiles); a group can never
+  // exceed T rows, so small batches skip them.
+  const int large = (long long)T * top_k >= 8192 ? kLargeGroupPrefill : kLargeGroupDecode;
+  const bool use_tc = !nvfp4 && T >= large && H % 256 == 0;
+  // Small batches fuse the grouping into the router.
+  const bool fuse = !use_tc && route_can_group(T, E, top_k);
+
   MOE_TRY_CUDA(mark(0));
   MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
-  MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches));
-  MOE_TRY_CUDA(mark(1));
-  // Experts with at least kLargeGroup rows go to the tensor-core kernels
-  // (bf16 weights, H a multiple of their 256-wide output tiles); a group can
-  // never exceed T rows, so small batches skip them.
-  const bool use_tc = !nvfp4 && T >= kLargeGroup && H % 256 == 0;
-  MOE_TRY_CUDA(launch_permute(idx, T, E, top_k, counts, offsets, perm, inv_perm, workspace, L,
-                              use_tc ? kLargeGroup : INT_MAX, kTcRows, s, launches));
-  MOE_TRY_CUDA(mark(2));
+  if (fuse) {
+    GroupOut go{counts, offsets, perm, inv_perm, ws_ptr<int32_t>(workspace, L.active),
+                ws_ptr<int32_t>(workspace, L.tiles), INT_MAX, kTcRows, nullptr, 0};
+    MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches, &go));
+    MOE_TRY_CUDA(mark(1));
+    MOE_TRY_CUDA(mark(2));
+  } else {
+    MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches,
+                              nullptr));
+    MOE_TRY_CUDA(mark(1));
+    MOE_TRY_CUDA(launch_permute(idx, T, E, top_k, counts, offsets, perm, inv_perm, workspace, L,
+                                use_tc ? large : INT_MAX, kTcRows, s, launches));
+    MOE_TRY_CUDA(mark(2));
+  }
 
   StreamGemmArgs a{};
   a.T = T; a.H = H; a.E = E; a.I = I; a.k = top_k;

@@ -88,7 +88,7 @@ extern "C" int moe_route_noalloc(const uint16_t* x, const uint16_t* gate_w, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch, 0, moe::zeroed_prefix(L), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (moe::launch_route(x, gate_w, bias, T, H, E, top_k, topk_idx, topk_w, scratch, L, s,
-                        nullptr) != cudaSuccess)
+                        nullptr, nullptr) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

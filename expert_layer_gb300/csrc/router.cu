@@ -19,6 +19,7 @@
 #include <limits.h>
 
 #include "common.cuh"
+#include "grouping.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -286,22 +287,31 @@ __device__ void select_token(int E, int k, float delta, int end, const uint16_t*
 }
 
 // ------------------------------------------------------------ small batches
-// Grid (T, ceil(E/8)), 8 warps, one (token, expert) logit per warp.  Lane l
+// Grid (T, ceil(E/16)), 16 warps, one (token, expert) logit per warp.  Lane l
 // sums the products at h = 8l + 256j + (0..7) sequentially (H/32 terms), then
 // a 5-level xor tree: at most H/32 + 4 roundings per product.  The last CTA to
 // finish a token (integer counter, no waiting) selects that token's top-k.
-__global__ void __launch_bounds__(256) router_small_kernel(
+// With kGroup, the CTA that selects the batch's last token then groups all
+// routed slots (grouping.cuh) in the same launch.
+constexpr int kSmallWarps = 16;
+
+template <bool kGroup>
+__global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
     int T, int H, int E, int k, int gamma_terms, float* __restrict__ logits,
     float* __restrict__ wnorm, double* __restrict__ l64, int* __restrict__ cnt,
-    int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
+    int32_t* __restrict__ idx, float* __restrict__ w, void* ws, GroupOut go) {
+  extern __shared__ int gsmem[];   // grouping scratch (kGroup only)
   __shared__ WarpScratch scr;
   __shared__ __align__(16) float sl[1024];
-  __shared__ int s_last;
+  __shared__ int s_last, s_group;
+  __shared__ int sw[grouping::kWarps];
+  pdl_wait();
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.y * 8 + warp;
+  const int e = blockIdx.y * kSmallWarps + warp;
   const uint16_t* xr = x + (size_t)t * H;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   if (e < E) {
     float acc = 0.f, sq = 0.f;
     const uint16_t* wr = gw + (size_t)e * H;
@@ -327,50 +337,61 @@ __global__ void __launch_bounds__(256) router_small_kernel(
     if (lane == 0) {
       logits[(size_t)t * E + e] = bias ? acc + bias[e] : acc;
       wnorm[e] = sqrtf(sq);   // same value from every token's CTA
+      __threadfence();        // the writer publishes before the CTA signals
     }
   }
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = atomicAdd(&cnt[t], 1) == (int)gridDim.y - 1;
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
-  // last CTA of token t: logits to shared memory, certified selection
+  // last CTA of token t (reads other CTAs' results through L2, ld.cg):
+  // logits to shared memory, certified selection
   for (int ee = threadIdx.x; ee < E; ee += blockDim.x) sl[ee] = __ldcg(&logits[(size_t)t * E + ee]);
   __syncthreads();
   if (E > 128) {   // many experts: every thread of the CTA helps rank them
     rank_candidates(sl, E, scr, threadIdx.x, blockDim.x);
     __syncthreads();
   }
-  if (warp != 0) return;
-  // ||x_t||, max ||w_e||, max |logit| for the error bound
-  float sqx = 0.f;
-  for (int h = lane * 8; h < H; h += 256) {
-    const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+  if (warp == 0) {
+    // ||x_t||, max ||w_e||, max |logit| for the error bound
+    float sqx = 0.f;
+    for (int h = lane * 8; h < H; h += 256) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      sqx = fmaf(bf16lo(xw[i]), bf16lo(xw[i]), sqx);
-      sqx = fmaf(bf16hi(xw[i]), bf16hi(xw[i]), sqx);
+      for (int i = 0; i < 4; ++i) {
+        sqx = fmaf(bf16lo(xw[i]), bf16lo(xw[i]), sqx);
+        sqx = fmaf(bf16hi(xw[i]), bf16hi(xw[i]), sqx);
+      }
     }
-  }
-  float wmax = 0.f, lmax = 0.f;
-  for (int ee = lane; ee < E; ee += 32) {
-    wmax = fmaxf(wmax, __ldcg(&wnorm[ee]));
-    lmax = fmaxf(lmax, fabsf(sl[ee]));
-  }
+    float wmax = 0.f, lmax = 0.f;
+    for (int ee = lane; ee < E; ee += 32) {
+      wmax = fmaxf(wmax, __ldcg(&wnorm[ee]));
+      lmax = fmaxf(lmax, fabsf(sl[ee]));
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
-    wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    for (int o = 16; o > 0; o >>= 1) {
+      sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
+      wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+      lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    }
+    const float delta = gamma_bound(gamma_terms) * sqrtf(sqx) * wmax * (1.0f + 0x1p-10f) +
+                        0x1p-22f * lmax + (float)H * 0x1p-149f;
+    const float thr = cert_threshold(delta);
+    const int end = E <= 128 ? extract_small(sl, E, k, thr, scr) : certain_end_ranked(scr, E, k, thr);
+    select_token(E, k, delta, end, xr, gw, bias, H, l64 + (size_t)t * E, scr, idx + (size_t)t * k,
+                 w + (size_t)t * k, hdr);
   }
-  const float delta = gamma_bound(gamma_terms) * sqrtf(sqx) * wmax * (1.0f + 0x1p-10f) +
-                      0x1p-22f * lmax + (float)H * 0x1p-149f;
-  const float thr = cert_threshold(delta);
-  const int end = E <= 128 ? extract_small(sl, E, k, thr, scr) : certain_end_ranked(scr, E, k, thr);
-  select_token(E, k, delta, end, xr, gw, bias, H, l64 + (size_t)t * E, scr, idx + (size_t)t * k,
-               w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
+  if constexpr (kGroup) {
+    if (warp == 0) __threadfence();   // the selecting warp wrote idx / w
+    __syncthreads();
+    if (threadIdx.x == 0) s_group = atomicAdd(&hdr->tokens_done, 1) == T - 1;
+    __syncthreads();
+    if (!s_group) return;
+    grouping::group_single_block(idx, T * k, E, go.large_threshold, go.tile_rows, go.counts,
+                                 go.offsets, go.perm, go.inv_perm, go.active, go.tiles, ws, gsmem,
+                                 sw, go.zero, go.nzero);
+  }
 }
 
 // ------------------------------------------------------------ large batches
@@ -570,9 +591,11 @@ __global__ void __launch_bounds__(256) wnorm_kernel(const uint16_t* __restrict__
 
 }  // namespace
 
+bool route_can_group(int T, int E, int k) { return !(T >= 2048 && E <= 128) && T * k <= 8 * kPermBlock; }
+
 cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
                          int E, int k, int32_t* idx, float* w, void* ws, const WsLayout& L,
-                         cudaStream_t stream, int* launches) {
+                         cudaStream_t stream, int* launches, const GroupOut* group) {
   float* wnorm = ws_ptr<float>(ws, L.wnorm);
   double* l64 = ws_ptr<double>(ws, L.logits64);
   const bool tiled = T >= 2048 && E <= kTileE;
@@ -598,10 +621,19 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
   }
   float* logits = ws_ptr<float>(ws, L.logits);
   int* cnt = ws_ptr<int>(ws, L.cnt);
-  dim3 g1(T, (E + 7) / 8);
+  dim3 g1(T, (E + kSmallWarps - 1) / kSmallWarps);
   const int gterms = H / 32 + 5;
-  router_small_kernel<<<g1, 256, 0, stream>>>(x, gate_w, bias, T, H, E, k, gterms, logits, wnorm,
-                                              l64, cnt, idx, w, ws);
+  if (group) {
+    const size_t smem = sizeof(int) * grouping::single_block_smem_ints(E);
+    cudaError_t err = cudaFuncSetAttribute(router_small_kernel<true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    router_small_kernel<true><<<g1, kSmallWarps * 32, smem, stream>>>(
+        x, gate_w, bias, T, H, E, k, gterms, logits, wnorm, l64, cnt, idx, w, ws, *group);
+  } else {
+    router_small_kernel<false><<<g1, kSmallWarps * 32, 0, stream>>>(
+        x, gate_w, bias, T, H, E, k, gterms, logits, wnorm, l64, cnt, idx, w, ws, GroupOut{});
+  }
   return cudaGetLastError();
 }
 

@@ -86,13 +86,15 @@ template <bool kFp4>
 struct StreamCfg {
   static constexpr int KB = kFp4 ? 128 : 32;      // K elements per block
   static constexpr int KG = kFp4 ? 2 : 4;         // blocks per pipelined group
-  static constexpr int NS = kFp4 ? 5 : 4;         // groups in the ring (NS-1 in flight)
+  static constexpr int NS = kFp4 ? 4 : 4;         // groups in the ring (NS-1 in flight)
   static constexpr int kWarps = 12;
   // per-warp ring: [NS][KG][2 rows][32 lanes] x 16 B of weights (codes), plus
   // [NS][KG][2][32] x 8 B of scales for NVFP4
   static constexpr int kWBytes = NS * KG * 2 * 32 * 16;
   static constexpr int kSBytes = kFp4 ? NS * KG * 2 * 32 * 8 : 0;
   static constexpr int kWarpBytes = kWBytes + kSBytes;
+  // NVFP4: the byte -> two-bf16 table replicated per lane (conflict-free lookups)
+  static constexpr int kLutBytes = kFp4 ? 256 * 32 * 4 : 0;
   static constexpr int kBRegs = kFp4 ? 16 : 4;    // 32-bit B registers per block
 };
 
@@ -157,8 +159,8 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
   using C = StreamCfg<kFp4>;
   constexpr int KB = C::KB, KG = C::KG, NS = C::NS, NW = C::kWarps;
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ uint32_t lut2[kFp4 ? 256 : 1];
   __shared__ uint16_t lut8[kFp4 ? 256 : 1];
+  uint32_t* lut2 = reinterpret_cast<uint32_t*>(smem + NW * C::kWarpBytes);   // [256][32]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -169,13 +171,18 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
   uint2* sring = reinterpret_cast<uint2*>(smem + warp * C::kWarpBytes + C::kWBytes);
 
   if constexpr (kFp4) {
-    for (int i = threadIdx.x; i < 256; i += NW * 32) {
-      lut2[i] = pack_bf16x2(e2m1_value(i & 15), e2m1_value(i >> 4));
-      lut8[i] = f2bf(e4m3_value(i));
+    for (int i = threadIdx.x; i < 256 * 32; i += NW * 32) {
+      const int b = i >> 5;
+      lut2[i] = pack_bf16x2(e2m1_value(b & 15), e2m1_value(b >> 4));
+      if ((i & 31) == 0) lut8[b] = f2bf(e4m3_value(b));
     }
     __syncthreads();
   }
 
+  // gate/up reads the grouping of the kernel just before it; down may start
+  // early (programmatic launch) and streams its first weights before waiting
+  // for h, since the grouping it needs finished before gate/up began
+  if (!kDown) { pdl_wait(); pdl_trigger(); }
   const int nsmall = *a.num_active - (a.num_large ? *a.num_large : 0);
   const long long U = (long long)nsmall * UPE;
   const long long stride = (long long)gridDim.x * NW;
@@ -225,6 +232,8 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
 #pragma unroll 1
   for (int s = 0; s < NS - 1; ++s) issue_next();
 
+  if (kDown) { pdl_wait(); pdl_trigger(); }   // h is complete; the combine may launch
+
   // ---- consumer side
   Task ct;
   ct.u = (long long)blockIdx.x * NW + warp;
@@ -257,22 +266,28 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
         if constexpr (kFp4) {
           const uint2 slo8 = sring[((slot_r * KG + i) * 2) * 32 + lane];
           const uint2 shi8 = sring[((slot_r * KG + i) * 2 + 1) * 32 + lane];
-          // this thread's two scales: bytes 2c and 2c+1 of the row's 8
+          // this thread's two scales: bytes 2c and 2c+1 of the row's 8, as
+          // bf16 pairs {s, s}; steps 0-3 use the first, steps 4-7 the second
           const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1));
           const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1));
+          uint32_t sl2[2], sh2[2];
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const uint32_t a8 = lut8[(slo >> (8 * hb)) & 0xff];
+            const uint32_t b8 = lut8[(shi >> (8 * hb)) & 0xff];
+            sl2[hb] = a8 | (a8 << 16);
+            sh2[hb] = b8 | (b8 << 16);
+          }
           const uint32_t clo[4] = {alo.x, alo.y, alo.z, alo.w};
           const uint32_t chi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const uint32_t sl = lut8[(slo >> (q < 4 ? 0 : 8)) & 0xff];
-            const uint32_t sh = lut8[(shi >> (q < 4 ? 0 : 8)) & 0xff];
-            const uint32_t sl2 = sl | (sl << 16), sh2 = sh | (sh << 16);
             const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
             const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
-            const uint32_t a0 = bf16x2_mul(lut2[wl & 0xff], sl2);
-            const uint32_t a2 = bf16x2_mul(lut2[(wl >> 8) & 0xff], sl2);
-            const uint32_t a1 = bf16x2_mul(lut2[wh & 0xff], sh2);
-            const uint32_t a3 = bf16x2_mul(lut2[(wh >> 8) & 0xff], sh2);
+            const uint32_t a0 = bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2[q >> 2]);
+            const uint32_t a2 = bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2[q >> 2]);
+            const uint32_t a1 = bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2[q >> 2]);
+            const uint32_t a3 = bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2[q >> 2]);
             mma_bf16_16816(acc, a0, a1, a2, a3, bc[i][2 * q], bc[i][2 * q + 1]);
           }
         } else {
@@ -330,12 +345,21 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   const long long need = (units + C::kWarps - 1) / C::kWarps;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  const int smem = C::kWarpBytes * C::kWarps;
+  const int smem = C::kWarpBytes * C::kWarps + C::kLutBytes;
   cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<kDown, kFp4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  stream_gemm_kernel<kDown, kFp4><<<(unsigned)grid, C::kWarps * 32, smem, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(C::kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kDown ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<kDown, kFp4>, a);
 }
 
 template <bool kDown>
