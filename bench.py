@@ -56,6 +56,35 @@ def parse_args():
     return p.parse_args()
 
 
+STAGE_SOURCES = {
+    "gate_up": ["expert_layer_gb300/csrc/stream_gemm.cu", "expert_layer_gb300/csrc/common.cuh",
+                "expert_layer_gb300/csrc/kernels.h"],
+    "down": ["expert_layer_gb300/csrc/stream_gemm.cu", "expert_layer_gb300/csrc/common.cuh",
+             "expert_layer_gb300/csrc/kernels.h"],
+}
+
+
+def measured_traffic(workload: str, stage: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.txt),
+    or None when none was taken or the kernel sources changed since."""
+    import hashlib
+    srcs = STAGE_SOURCES.get(stage)
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not srcs or not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in srcs:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload and parts[1] == stage:
+                return int(parts[3]) if parts[2] == digest else None
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -390,7 +419,7 @@ def run_ours(args):
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         achieved = byt[dom] / dom_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None}
+                "frac": achieved / peak, "traffic": measured_traffic(args.workload, dom)}
     roof.update({"kernel": dom, "peak_source": f"{peak_src} MEASURED_PEAKS.json" if peak_src == "measured"
                  else "fallback", "algorithmic_bytes": byt[dom], "launch_us": stage_ms[dom] * 1e3})
     step_ms = ms / K
