@@ -28,27 +28,32 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
-// Exclusive scan over the 512 threads of a block; returns the prefix and the
-// block total in *total.  `sw` is shared scratch of kWarps ints.
-__device__ int block_exclusive_scan(int v, int* sw, int* total) {
+// Exclusive scan of four independent int fields over the 512 threads of a
+// block; returns the prefixes and the block totals in *total.  `sw` is shared
+// scratch of kWarps int4.
+__device__ int4 block_exclusive_scan4(int4 v, int4* sw, int4* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  int4 incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
+    const int nx = __shfl_up_sync(0xffffffffu, incl.x, o);
+    const int ny = __shfl_up_sync(0xffffffffu, incl.y, o);
+    const int nz = __shfl_up_sync(0xffffffffu, incl.z, o);
+    const int nw = __shfl_up_sync(0xffffffffu, incl.w, o);
+    if (lane >= o) { incl.x += nx; incl.y += ny; incl.z += nz; incl.w += nw; }
   }
   __syncthreads();
   if (lane == 31) sw[warp] = incl;
   __syncthreads();
-  int base = 0, tot = 0;
+  int4 base = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
   for (int w = 0; w < kWarps; ++w) {
-    const int s = sw[w];
-    if (w < warp) base += s;
-    tot += s;
+    const int4 s = sw[w];
+    if (w < warp) { base.x += s.x; base.y += s.y; base.z += s.z; base.w += s.w; }
+    tot.x += s.x; tot.y += s.y; tot.z += s.z; tot.w += s.w;
   }
   *total = tot;
-  return base + incl - v;
+  return make_int4(base.x + incl.x - v.x, base.y + incl.y - v.y, base.z + incl.z - v.z,
+                   base.w + incl.w - v.w);
 }
 
 // Rank of each slot of one 512-slot block among equal experts, in f order.
@@ -81,81 +86,121 @@ __device__ int block_stable_rank(int e, bool valid, int E, int* tab, const int* 
 }
 
 // Counts -> offsets, active list, tile prefix.  Called by one 512-thread block
-// with counts[] in shared memory; writes the global outputs.
+// with counts[] in shared memory (E <= 1024); writes the global outputs and
+// the offsets to s_off.  One four-field scan carries the offsets, the
+// positions in both halves of the active list and the tile prefix.
 __device__ void finish_scan(const int* s_counts, int E, int S, int large_threshold, int tile_rows,
                             int32_t* counts, int32_t* offsets, int32_t* active, int32_t* tiles,
-                            WsHeader* hdr, int* s_off, int* sw) {
-  // offsets: each thread owns experts 2t, 2t+1
+                            WsHeader* hdr, int* s_off, int4* sw) {
+  // each thread owns experts 2t, 2t+1
   const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
   const int c0 = e0 < E ? s_counts[e0] : 0, c1 = e1 < E ? s_counts[e1] : 0;
-  int tot;
-  const int pre = block_exclusive_scan(c0 + c1, sw, &tot);
-  if (e0 < E) { s_off[e0] = pre; offsets[e0] = pre; counts[e0] = c0; }
-  if (e1 < E) { s_off[e1] = pre + c0; offsets[e1] = pre + c0; counts[e1] = c1; }
-  if (threadIdx.x == 0) offsets[E] = S;
   // active lists: small groups first, then large groups
   const int sm0 = (c0 > 0 && c0 < large_threshold), sm1 = (c1 > 0 && c1 < large_threshold);
   const int lg0 = (c0 >= large_threshold && c0 > 0), lg1 = (c1 >= large_threshold && c1 > 0);
-  int nsmall, nlarge;
-  const int ps = block_exclusive_scan(sm0 + sm1, sw, &nsmall);
-  if (sm0) active[ps] = e0;
-  if (sm1) active[ps + sm0] = e1;
-  const int pl = block_exclusive_scan(lg0 + lg1, sw, &nlarge);
-  if (lg0) active[nsmall + pl] = e0;
-  if (lg1) active[nsmall + pl + lg0] = e1;
-  // row-tile prefix over the large groups, in list order
+  // row tiles of the large groups
   const int t0 = lg0 ? (c0 + tile_rows - 1) / tile_rows : 0;
   const int t1 = lg1 ? (c1 + tile_rows - 1) / tile_rows : 0;
-  int ntiles;
-  const int pt = block_exclusive_scan(t0 + t1, sw, &ntiles);
-  if (lg0) tiles[pl] = pt;
-  if (lg1) tiles[pl + lg0] = pt + t0;
+  int4 tot;
+  const int4 pre = block_exclusive_scan4(make_int4(c0 + c1, sm0 + sm1, lg0 + lg1, t0 + t1), sw, &tot);
+  if (e0 < E) { s_off[e0] = pre.x; offsets[e0] = pre.x; counts[e0] = c0; }
+  if (e1 < E) { s_off[e1] = pre.x + c0; offsets[e1] = pre.x + c0; counts[e1] = c1; }
+  if (threadIdx.x == 0) offsets[E] = S;
+  const int nsmall = tot.y, nlarge = tot.z;
+  if (sm0) active[pre.y] = e0;
+  if (sm1) active[pre.y + sm0] = e1;
+  if (lg0) active[nsmall + pre.z] = e0;
+  if (lg1) active[nsmall + pre.z + lg0] = e1;
+  if (lg0) tiles[pre.z] = pre.w;
+  if (lg1) tiles[pre.z + lg0] = pre.w + t0;
   if (threadIdx.x == 0) {
-    tiles[nlarge] = ntiles;
+    tiles[nlarge] = tot.w;
     hdr->num_active = nsmall + nlarge;
     hdr->num_large = nlarge;
   }
 }
 
-// Dynamic shared memory (ints) that group_single_block needs.
-__host__ __device__ inline size_t single_block_smem_ints(int E) { return (size_t)E * (3 + kWarps); }
+// Largest S that group_single_block serves.
+constexpr int kSingleMaxChunks = 8;
+constexpr int kSingleMaxSlots = kSingleMaxChunks * kThreads;
 
-// The whole grouping for S slots in one 512-thread block.  `dyn` holds
-// single_block_smem_ints(E) ints, `sw` kWarps ints.  `zero`/`nzero`: an int
-// region cleared on the way (counters used later in the same call).
+// Dynamic shared memory (ints) that group_single_block needs for S slots.
+__host__ __device__ inline size_t single_block_smem_ints(int E, int S) {
+  return (size_t)E * (2 + kWarps) + 2 * (size_t)S;
+}
+
+// The whole grouping for S <= kSingleMaxSlots slots in one 512-thread block.
+// `dyn` holds single_block_smem_ints(E, S) ints, `sw` kWarps int4.
+// `zero`/`nzero`: an int region cleared on the way (counters used later in
+// the same call).  Every slot id is read once into shared memory; slot f of
+// chunk c (f = 512c + thread) gets its rank among equal experts from the
+// chunk's stable rank plus the running per-expert count of the earlier
+// chunks, and its position adds the expert's offset once all counts are
+// known.  The chunk loop is kept rolled: this code often runs once, on one
+// SM, where every extra instruction line is fetched cold.
 __device__ void group_single_block(const int32_t* __restrict__ idx, int S, int E,
                                    int large_threshold, int tile_rows, int32_t* counts,
                                    int32_t* offsets, int32_t* perm, int32_t* inv_perm,
-                                   int32_t* active, int32_t* tiles, void* ws, int* dyn, int* sw,
+                                   int32_t* active, int32_t* tiles, void* ws, int* dyn, int4* sw,
                                    int* zero, int nzero) {
-  int* s_cnt = dyn;              // [E]
-  int* s_run = s_cnt + E;        // [E]
-  int* tab = s_run + E;          // [kWarps][E], then [E] block counts
+  int* s_cnt = dyn;              // [E] running counts, then totals
+  int* s_off = s_cnt + E;        // [E] offsets
+  int* tab = s_off + E;          // [kWarps][E]
+  int* s_e = tab + kWarps * E;   // [S] expert of each slot
+  int* s_rel = s_e + S;          // [S] rank of each slot within its expert
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  const int warp = threadIdx.x >> 5;
+  {
+    int ev[kSingleMaxChunks];    // all loads in flight before the first store
+#pragma unroll
+    for (int c = 0; c < kSingleMaxChunks; ++c) {
+      const int f = c * kThreads + threadIdx.x;
+      ev[c] = f < S ? __ldcg(&idx[f]) : -1;
+    }
+#pragma unroll
+    for (int c = 0; c < kSingleMaxChunks; ++c) {
+      const int f = c * kThreads + threadIdx.x;
+      if (f < S) s_e[f] = ev[c];
+    }
+  }
   for (int i = threadIdx.x; i < nzero; i += kThreads) zero[i] = 0;
   for (int e = threadIdx.x; e < E; e += kThreads) s_cnt[e] = 0;
-  __syncthreads();
   bool bad = false;
-  for (int f = threadIdx.x; f < S; f += kThreads) {
-    const int e = __ldcg(&idx[f]);
-    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1); else bad = true;
-  }
-  if (bad) set_status(ws, kStatusBadExpert);
-  __syncthreads();
-  finish_scan(s_cnt, E, S, large_threshold, tile_rows, counts, offsets, active, tiles, hdr, s_run,
-              sw);
-  __syncthreads();
-  int* s_blk = tab + kWarps * E;  // [E]
+#pragma unroll 1
   for (int c0 = 0; c0 < S; c0 += kThreads) {
     const int f = c0 + threadIdx.x;
-    int e = -1;
-    if (f < S) e = __ldcg(&idx[f]);
-    const bool valid = f < S && e >= 0 && e < E;
-    const int pos = block_stable_rank(e, valid, E, tab, s_run, s_blk);
-    if (valid) { perm[pos] = f; inv_perm[f] = pos; }
-    __syncthreads();  // every thread has read its position from tab
-    for (int ee = threadIdx.x; ee < E; ee += kThreads) s_run[ee] += s_blk[ee];
+    const int e = f < S ? s_e[f] : -1;
+    const bool valid = e >= 0 && e < E;
+    if (f < S && !valid) bad = true;
+    if (c0 > 0) __syncthreads();   // every thread has read the previous chunk's ranks
+    for (int i = threadIdx.x; i < kWarps * E; i += kThreads) tab[i] = 0;
     __syncthreads();
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    const int r = __popc(peers & lanemask_lt());
+    if (valid && r == 0) tab[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int ee = threadIdx.x; ee < E; ee += kThreads) {
+      int s = s_cnt[ee];
+      for (int w = 0; w < kWarps; ++w) {
+        const int cw = tab[w * E + ee];
+        tab[w * E + ee] = s;
+        s += cw;
+      }
+      s_cnt[ee] = s;
+    }
+    __syncthreads();
+    if (f < S) s_rel[f] = valid ? tab[warp * E + e] + r : -1;
+  }
+  if (bad) set_status(ws, kStatusBadExpert);
+  finish_scan(s_cnt, E, S, large_threshold, tile_rows, counts, offsets, active, tiles, hdr, s_off,
+              sw);
+  __syncthreads();
+  for (int f = threadIdx.x; f < S; f += kThreads) {
+    const int rel = s_rel[f];
+    if (rel < 0) continue;
+    const int pos = s_off[s_e[f]] + rel;
+    perm[pos] = f;
+    inv_perm[f] = pos;
   }
 }
 

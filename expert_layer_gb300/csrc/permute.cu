@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kThreads) permute_single_kernel(
     int32_t* __restrict__ inv_perm, int32_t* __restrict__ active, int32_t* __restrict__ tiles,
     void* ws) {
   extern __shared__ int smem[];
-  __shared__ int sw[kWarps];
+  __shared__ int4 sw[kWarps];
   grouping::group_single_block(idx, S, E, large_threshold, tile_rows, counts, offsets, perm,
                                inv_perm, active, tiles, ws, smem, sw, nullptr, 0);
 }
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
   extern __shared__ int smem[];
   int* s_cnt = smem;       // [E]
   int* s_off = s_cnt + E;  // [E]
-  __shared__ int sw[kWarps];
+  __shared__ int4 sw[kWarps];
   for (int e = threadIdx.x; e < E; e += kThreads) {
     int s = 0;
     for (int b = 0; b < nblk; ++b) s += blk_cnt[(size_t)b * E + e];
@@ -96,8 +96,8 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* cou
   const int S = T * k;
   int32_t* active = ws_ptr<int32_t>(ws, L.active);
   int32_t* tiles = ws_ptr<int32_t>(ws, L.tiles);
-  if (S <= 8 * kThreads) {
-    const size_t smem = sizeof(int) * grouping::single_block_smem_ints(E);
+  if (S <= grouping::kSingleMaxSlots) {
+    const size_t smem = sizeof(int) * grouping::single_block_smem_ints(E, S);
     cudaError_t err = cudaFuncSetAttribute(permute_single_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

@@ -35,10 +35,11 @@ __host__ __device__ inline float gamma_bound(int n) {
 
 // Exact-product fp64 dot of two bf16 rows of length H (H % 8 == 0), whole warp.
 // Every lane returns the same value (xor butterfly).
+// Four independent fp64 chains per lane keep the (slow) fp64 pipe busy.
 __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
                                int H) {
   const int lane = threadIdx.x & 31;
-  double s = 0.0;
+  double s[4] = {0.0, 0.0, 0.0, 0.0};
   for (int h = lane * 8; h < H; h += 256) {
     uint4 va = *reinterpret_cast<const uint4*>(a + h);
     uint4 vb = *reinterpret_cast<const uint4*>(b + h);
@@ -46,13 +47,14 @@ __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* _
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      s = fma((double)bf16lo(wa[i]), (double)bf16lo(wb[i]), s);
-      s = fma((double)bf16hi(wa[i]), (double)bf16hi(wb[i]), s);
+      s[i] = fma((double)bf16lo(wa[i]), (double)bf16lo(wb[i]), s[i]);
+      s[i] = fma((double)bf16hi(wa[i]), (double)bf16hi(wb[i]), s[i]);
     }
   }
+  double r = (s[0] + s[1]) + (s[2] + s[3]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  return s;
+  for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
 }
 
 struct WarpScratch {
@@ -69,35 +71,6 @@ __device__ __forceinline__ float cert_threshold(float delta) { return 2.0f * del
 
 // Sort key of a logit: NaN ranks below every number.
 __device__ __forceinline__ float rank_key(float v) { return v != v ? -INFINITY : v; }
-
-// (v, e) ordering: larger value first, lower index first on equal values.
-__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
-  return v > bv || (v == bv && e < be);
-}
-
-// Sorted candidates for E > 128: cand_e/cand_v[r] = the expert of rank r
-// (larger logit first, lower index first on equal logits) for
-// r < min(E, kCandCap).  Each of the nthr cooperating threads (index tid)
-// ranks its experts by counting the experts that come before it.  The
-// caller synchronises the cooperating threads before using the result.
-__device__ void rank_candidates(const float* L, int E, WarpScratch& sc, int tid, int nthr) {
-  for (int e = tid; e < E; e += nthr) {
-    const float v = rank_key(L[e]);
-    int r = 0;
-    int j = 0;
-    for (; j + 4 <= E; j += 4) {
-      const float4 q = *reinterpret_cast<const float4*>(L + j);
-      const float q0 = rank_key(q.x), q1 = rank_key(q.y), q2 = rank_key(q.z), q3 = rank_key(q.w);
-      r += (q0 > v || (q0 == v && j < e)) + (q1 > v || (q1 == v && j + 1 < e)) +
-           (q2 > v || (q2 == v && j + 2 < e)) + (q3 > v || (q3 == v && j + 3 < e));
-    }
-    for (; j < E; ++j) {
-      const float q = rank_key(L[j]);
-      r += (q > v || (q == v && j < e));
-    }
-    if (r < kCandCap) { sc.cand_e[r] = e; sc.cand_v[r] = v; }
-  }
-}
 
 // End of the certain set from fully ranked candidates: the first rank
 // j >= k-1 whose gap to rank j+1 exceeds thr; everything below it is
@@ -116,44 +89,50 @@ __device__ int certain_end_ranked(const WarpScratch& sc, int E, int k, float thr
   return E <= kCandCap ? E - 1 : -1;
 }
 
+// Order-preserving map of a non-NaN float to uint32 (-0 and +0 both map to
+// the key of +0, as they compare equal) and its inverse.
+__device__ __forceinline__ uint32_t order_bits(float v) {
+  const uint32_t u = v == 0.0f ? 0u : __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_value(uint32_t m) {
+  return __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
+}
+
 // Sorted candidates for E <= 128, extracted in rank order until the certain
-// set is closed.  Each lane keeps its (up to) four logits sorted in
-// registers; a round is one warp arg-max over the lanes' current heads.
+// set is closed.  Lane l holds the logits of experts l + 32i (i < 4) in v[]
+// (any value for e >= E).  Each lane keeps its four keys sorted in
+// registers; a round is a warp max-reduction over the lanes' current heads
+// followed by a min-reduction over the expert ids that reach that maximum.
 // Writes cand_e/cand_v[0..end+1] and returns end (or -1 for the fallback).
-__device__ int extract_small(const float* L, int E, int k, float thr, WarpScratch& sc) {
+__device__ int extract_regs(const float (&v)[4], int E, int k, float thr, WarpScratch& sc) {
   const int lane = threadIdx.x & 31;
-  float v[4];
-  int id[4];
+  uint32_t key[4];
+  uint32_t id[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int e = lane + 32 * i;
-    id[i] = e < E ? e : INT_MAX;
-    v[i] = e < E ? rank_key(L[e]) : -INFINITY;
+    id[i] = e < E ? (uint32_t)e : 0xffffffffu;
+    key[i] = e < E ? order_bits(rank_key(v[i])) : 0u;   // 0 ranks below -inf
   }
-  // sort the four (v, id) pairs, best first (5-comparator network)
-#define MOE_CSWAP(a, b)                                                        \
-  if (better(v[b], id[b], v[a], id[a])) {                                      \
-    const float tv = v[a]; v[a] = v[b]; v[b] = tv;                             \
-    const int ti = id[a]; id[a] = id[b]; id[b] = ti;                           \
+  // sort the four (key, id) pairs, best first (5-comparator network)
+#define MOE_CSWAP(a, b)                                                              \
+  if (key[b] > key[a] || (key[b] == key[a] && id[b] < id[a])) {                      \
+    const uint32_t tk = key[a]; key[a] = key[b]; key[b] = tk;                        \
+    const uint32_t ti = id[a]; id[a] = id[b]; id[b] = ti;                            \
   }
   MOE_CSWAP(0, 1) MOE_CSWAP(2, 3) MOE_CSWAP(0, 2) MOE_CSWAP(1, 3) MOE_CSWAP(1, 2)
 #undef MOE_CSWAP
   int head = 0;
   float prev = 0.f;
   for (int r = 0; r < kCandCap; ++r) {
-    float bv = head == 0 ? v[0] : head == 1 ? v[1] : head == 2 ? v[2] : head == 3 ? v[3] : -INFINITY;
-    int be = head == 0 ? id[0] : head == 1 ? id[1] : head == 2 ? id[2] : head == 3 ? id[3] : INT_MAX;
-    const int mylane = lane;
-    int bl = mylane;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      if (better(ov, oe, bv, be)) { bv = ov; be = oe; bl = ol; }
-    }
-    if (lane == bl) ++head;
-    if (lane == 0) { sc.cand_e[r] = be; sc.cand_v[r] = bv; }
+    const uint32_t hk = head == 0 ? key[0] : head == 1 ? key[1] : head == 2 ? key[2] : head == 3 ? key[3] : 0u;
+    const uint32_t hid = head == 0 ? id[0] : head == 1 ? id[1] : head == 2 ? id[2] : head == 3 ? id[3] : 0xffffffffu;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t be = __reduce_min_sync(0xffffffffu, hk == m ? hid : 0xffffffffu);
+    if (hk == m && hid == be) ++head;
+    const float bv = order_value(m);
+    if (lane == 0) { sc.cand_e[r] = (int)be; sc.cand_v[r] = bv; }
     if (r >= k && prev - bv > thr) return r - 1;   // gap closes the certain set
     if (r + 1 == E) return r;                       // every expert extracted
     prev = bv;
@@ -161,47 +140,30 @@ __device__ int extract_small(const float* L, int E, int k, float thr, WarpScratc
   return -1;
 }
 
-// Certified top-k of one token from its sorted candidates cand[0..end] (the
-// certain set) -- or, when fallback is set, from fp64 logits of every expert.
-// Whole warp.  Writes idx_out[0..k) and w_out[0..k).
-__device__ void select_token(int E, int k, float delta, int end, const uint16_t* xrow,
-                             const uint16_t* gate_w, const float* bias, int H, double* l64_row,
-                             WarpScratch& sc, int32_t* idx_out, float* w_out, WsHeader* hdr) {
+// extract_regs over logits held in shared memory.
+__device__ int extract_small(const float* L, int E, int k, float thr, WarpScratch& sc) {
   const int lane = threadIdx.x & 31;
-  const int per_lane = (E + 31) >> 5;
-  const float thr = cert_threshold(delta);
-  const bool fallback = end < 0;
-  __syncwarp();
+  float v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? L[e] : 0.0f;
+  }
+  return extract_regs(v, E, k, thr, sc);
+}
 
-  if (!fallback) {
-    // Ambiguous candidates: members of an adjacent pair closer than 2*delta.
-    bool amb0 = false, amb1 = false;
-    for (int r = 0; r < 2; ++r) {
-      const int i = lane + 32 * r;
-      bool a = false;
-      if (i <= end) {
-        if (i > 0 && !(sc.cand_v[i - 1] - sc.cand_v[i] > thr)) a = true;
-        if (i < end && !(sc.cand_v[i] - sc.cand_v[i + 1] > thr)) a = true;
-      }
-      if (r == 0) amb0 = a; else amb1 = a;
-    }
-    const unsigned bal0 = __ballot_sync(0xffffffffu, amb0);
-    const unsigned bal1 = __ballot_sync(0xffffffffu, amb1);
-    if ((bal0 | bal1) == 0) {
-      // the fp32 order is certain: ranks are the candidate positions
-      if (lane < k) {
-        idx_out[lane] = sc.cand_e[lane];
-        sc.ex[lane] = expf(sc.cand_v[lane] - sc.cand_v[0]);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        float sum = 0.0f;
-        for (int s = 0; s < k; ++s) sum += sc.ex[s];
-        for (int s = 0; s < k; ++s) w_out[s] = sc.ex[s] / sum;
-      }
-      __syncwarp();
-      return;
-    }
+// The uncertain cases of select_token, kept out of line so that the common
+// certain case stays short: candidates that sit within rounding of a
+// neighbour get fp64 logits and the certain set is re-ranked (bal0/bal1 flag
+// them, candidate positions lane and lane + 32), or, when end < 0, every
+// expert gets an fp64 logit.  Whole warp; writes idx_out[0..k) and the
+// unnormalised weights sc.ex[0..k).
+__device__ __noinline__ void select_fp64(int E, int k, int end, unsigned bal0, unsigned bal1,
+                                         const uint16_t* xrow, const uint16_t* gate_w,
+                                         const float* bias, int H, double* l64_row,
+                                         WarpScratch& sc, int32_t* idx_out, WsHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  if (end >= 0) {
     if (lane == 0) atomicAdd(&hdr->router_flagged, 1);
     for (int r = 0; r < 2; ++r) {
       const int i = lane + 32 * r;
@@ -243,153 +205,282 @@ __device__ void select_token(int E, int k, float delta, int end, const uint16_t*
       const int i = lane + 32 * r;
       if (rank[r] < k) sc.ex[rank[r]] = expf((float)(sc.key[i] - kmax));
     }
-  } else {
-    // Every expert in fp64 (needs >= 64 experts within rounding of each other).
-    if (lane == 0) { atomicAdd(&hdr->router_flagged, 1); atomicAdd(&hdr->router_fallback, 1); }
-    for (int e = 0; e < E; ++e) {
-      double d = warp_dot_f64(xrow, gate_w + (size_t)e * H, H);
-      if (bias) d += (double)bias[e];
-      if (lane == 0) l64_row[e] = d;
-    }
-    __syncwarp();
-    __threadfence_block();
-    uint32_t taken = 0;
-    double kmax = 0.0;
-    for (int s = 0; s < k; ++s) {
-      double bv = 0.0;
-      int be = INT_MAX;
-      for (int i = 0; i < per_lane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u)) {
-          const double v = l64_row[e];
-          if (be == INT_MAX || v > bv || (v == bv && e < be)) { bv = v; be = e; }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) { bv = ov; be = oe; }
-      }
-      if (be == INT_MAX) be = 0;  // unreachable for k <= E
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (s == 0) kmax = bv;
-      if (lane == 0) { idx_out[s] = be; sc.ex[s] = expf((float)(bv - kmax)); }
-    }
+    return;
+  }
+  // Every expert in fp64 (needs >= 64 experts within rounding of each other).
+  const int per_lane = (E + 31) >> 5;
+  if (lane == 0) { atomicAdd(&hdr->router_flagged, 1); atomicAdd(&hdr->router_fallback, 1); }
+  for (int e = 0; e < E; ++e) {
+    double d = warp_dot_f64(xrow, gate_w + (size_t)e * H, H);
+    if (bias) d += (double)bias[e];
+    if (lane == 0) l64_row[e] = d;
   }
   __syncwarp();
-  if (lane == 0) {
-    float sum = 0.0f;
-    for (int s = 0; s < k; ++s) sum += sc.ex[s];
-    for (int s = 0; s < k; ++s) w_out[s] = sc.ex[s] / sum;
+  __threadfence_block();
+  uint32_t taken = 0;
+  double kmax = 0.0;
+  for (int s = 0; s < k; ++s) {
+    double bv = 0.0;
+    int be = INT_MAX;
+    for (int i = 0; i < per_lane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u)) {
+        const double v = l64_row[e];
+        if (be == INT_MAX || v > bv || (v == bv && e < be)) { bv = v; be = e; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) { bv = ov; be = oe; }
+    }
+    if (be == INT_MAX) be = 0;  // unreachable for k <= E
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (s == 0) kmax = bv;
+    if (lane == 0) { idx_out[s] = be; sc.ex[s] = expf((float)(bv - kmax)); }
   }
+}
+
+// Certified top-k of one token from its sorted candidates cand[0..end] (the
+// certain set) -- or, when end < 0, from fp64 logits of every expert.  Whole
+// warp.  Writes idx_out[0..k) and w_out[0..k).
+__device__ void select_token(int E, int k, float delta, int end, const uint16_t* xrow,
+                             const uint16_t* gate_w, const float* bias, int H, double* l64_row,
+                             WarpScratch& sc, int32_t* idx_out, float* w_out, WsHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  const float thr = cert_threshold(delta);
+  __syncwarp();
+  unsigned bal0 = 0, bal1 = 0;
+  bool certain = false;
+  if (end >= 0) {
+    // Ambiguous candidates: members of an adjacent pair closer than 2*delta.
+    bool amb0 = false, amb1 = false;
+    for (int r = 0; r < 2; ++r) {
+      const int i = lane + 32 * r;
+      bool a = false;
+      if (i <= end) {
+        if (i > 0 && !(sc.cand_v[i - 1] - sc.cand_v[i] > thr)) a = true;
+        if (i < end && !(sc.cand_v[i] - sc.cand_v[i + 1] > thr)) a = true;
+      }
+      if (r == 0) amb0 = a; else amb1 = a;
+    }
+    bal0 = __ballot_sync(0xffffffffu, amb0);
+    bal1 = __ballot_sync(0xffffffffu, amb1);
+    certain = (bal0 | bal1) == 0;
+  }
+  float ex = 0.f;
+  if (certain) {
+    // the fp32 order is certain: ranks are the candidate positions
+    if (lane < k) {
+      idx_out[lane] = sc.cand_e[lane];
+      ex = expf(sc.cand_v[lane] - sc.cand_v[0]);
+    }
+  } else {
+    select_fp64(E, k, end, bal0, bal1, xrow, gate_w, bias, H, l64_row, sc, idx_out, hdr);
+    __syncwarp();
+    if (lane < k) ex = sc.ex[lane];
+  }
+  // renormalise over the k selected (fixed xor-tree order, same on every lane)
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) w_out[lane] = ex / sum;
   __syncwarp();
 }
 
 // ------------------------------------------------------------ small batches
-// Grid (T, ceil(E/16)), 16 warps, one (token, expert) logit per warp.  Lane l
-// sums the products at h = 8l + 256j + (0..7) sequentially (H/32 terms), then
-// a 5-level xor tree: at most H/32 + 4 roundings per product.  The last CTA to
-// finish a token (integer counter, no waiting) selects that token's top-k.
-// With kGroup, the CTA that selects the batch's last token then groups all
-// routed slots (grouping.cuh) in the same launch.
+// Grid (ceil(T / kTT), ceil(E / 16)), 16 warps: warp w of CTA (c, y) computes
+// the logits of expert 16y + w for the kTT tokens of chunk c, reading the gate
+// row once.  Lane l sums the products at h = 8l + 256j + (0..7) sequentially
+// (H/32 terms), then a 5-level xor tree: at most H/32 + 4 roundings per
+// product.  Warp 0 of the y = 0 CTAs also writes ||x_t||.  The last CTA to
+// finish a chunk (integer counter, no waiting) ranks every (token, expert)
+// of the chunk by counting, all threads at once, and then selects each
+// token's top-k with one warp per token.  With kGroup, the CTA that selects
+// the batch's last tokens then groups all routed slots (grouping.cuh) in the
+// same launch.
 constexpr int kSmallWarps = 16;
 
-template <bool kGroup>
+// Shared memory of the small router: grouping scratch (kGroup) then, for the
+// selecting CTA, the chunk's logits [tt][E], ||w_e|| [E] and ||x_t|| [tt].
+__host__ __device__ inline size_t router_small_group_ints(int E, int S, bool group) {
+  return group ? grouping::single_block_smem_ints(E, S) : 0;
+}
+__host__ __device__ inline size_t router_small_smem(int E, int S, int tt, bool group) {
+  return sizeof(int) * router_small_group_ints(E, S, group) + sizeof(float) * ((size_t)(tt + 1) * E + tt);
+}
+
+// Release-acquire integer add at GPU scope: the caller's earlier writes (and
+// those its CTA made before a barrier) are visible to whoever observes the
+// add, and the caller sees every write released to the counter before it.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+template <int kTT, bool kGroup>
 __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
     int T, int H, int E, int k, int gamma_terms, float* __restrict__ logits,
-    float* __restrict__ wnorm, double* __restrict__ l64, int* __restrict__ cnt,
-    int32_t* __restrict__ idx, float* __restrict__ w, void* ws, GroupOut go) {
-  extern __shared__ int gsmem[];   // grouping scratch (kGroup only)
-  __shared__ WarpScratch scr;
-  __shared__ __align__(16) float sl[1024];
+    float* __restrict__ wnorm, float* __restrict__ xnorm, double* __restrict__ l64,
+    int* __restrict__ cnt, int32_t* __restrict__ idx, float* __restrict__ w, void* ws, GroupOut go) {
+  extern __shared__ __align__(16) int dsm[];
+  __shared__ WarpScratch scr[kTT];
   __shared__ int s_last, s_group;
-  __shared__ int sw[grouping::kWarps];
+  __shared__ int4 sw[grouping::kWarps];
   pdl_wait();
-  const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x;
+  const int t0 = chunk * kTT;
+  const int nt = min(kTT, T - t0);
   const int e = blockIdx.y * kSmallWarps + warp;
-  const uint16_t* xr = x + (size_t)t * H;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   if (e < E) {
-    float acc = 0.f, sq = 0.f;
-    const uint16_t* wr = gw + (size_t)e * H;
-#pragma unroll 8
-    for (int h = lane * 8; h < H; h += 256) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
-      const uint4 wv = *reinterpret_cast<const uint4*>(wr + h);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    float acc[kTT], sq = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc = fmaf(bf16lo(xw[i]), bf16lo(ww[i]), acc);
-        acc = fmaf(bf16hi(xw[i]), bf16hi(ww[i]), acc);
-        sq = fmaf(bf16lo(ww[i]), bf16lo(ww[i]), sq);
-        sq = fmaf(bf16hi(ww[i]), bf16hi(ww[i]), sq);
+    for (int tt = 0; tt < kTT; ++tt) acc[tt] = 0.f;
+    const uint16_t* wr = gw + (size_t)e * H;
+    for (int hb = 0; hb < H; hb += 2048) {
+      uint4 wv[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int h = hb + lane * 8 + 256 * v;
+        wv[v] = h < H ? ldg_nc_v4(wr + h) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          sq = fmaf(bf16lo(ww[i]), bf16lo(ww[i]), sq);
+          sq = fmaf(bf16hi(ww[i]), bf16hi(ww[i]), sq);
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < kTT; ++tt) {
+        if (tt >= nt) break;
+        const uint16_t* xr = x + (size_t)(t0 + tt) * H;
+        uint4 xv[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const int h = hb + lane * 8 + 256 * v;
+          xv[v] = h < H ? *reinterpret_cast<const uint4*>(xr + h) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint32_t xw[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
+          const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[tt] = fmaf(bf16lo(xw[i]), bf16lo(ww[i]), acc[tt]);
+            acc[tt] = fmaf(bf16hi(xw[i]), bf16hi(ww[i]), acc[tt]);
+          }
+        }
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      acc += __shfl_xor_sync(0xffffffffu, acc, o);
       sq += __shfl_xor_sync(0xffffffffu, sq, o);
+#pragma unroll
+      for (int tt = 0; tt < kTT; ++tt) acc[tt] += __shfl_xor_sync(0xffffffffu, acc[tt], o);
     }
-    if (lane == 0) {
-      logits[(size_t)t * E + e] = bias ? acc + bias[e] : acc;
-      wnorm[e] = sqrtf(sq);   // same value from every token's CTA
-      __threadfence();        // the writer publishes before the CTA signals
+    float mine = acc[0];
+#pragma unroll
+    for (int tt = 1; tt < kTT; ++tt) if (lane == tt) mine = acc[tt];
+    if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = bias ? mine + bias[e] : mine;
+    if (lane == 31) wnorm[e] = sqrtf(sq);   // the same value from every chunk's CTA
+  }
+  if (blockIdx.y == 0 && warp == 0) {
+    // ||x_t|| of the chunk's tokens (rows just read, mostly cache hits)
+    for (int tt = 0; tt < nt; ++tt) {
+      const uint16_t* xr = x + (size_t)(t0 + tt) * H;
+      float sqx = 0.f;
+      for (int h = lane * 8; h < H; h += 256) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          sqx = fmaf(bf16lo(xw[i]), bf16lo(xw[i]), sqx);
+          sqx = fmaf(bf16hi(xw[i]), bf16hi(xw[i]), sqx);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
+      if (lane == 0) xnorm[t0 + tt] = sqrtf(sqx);
     }
   }
+  // Publish the CTA's results and count the CTA in; the last CTA of the
+  // chunk sees every other CTA's results.
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&cnt[t], 1) == (int)gridDim.y - 1;
+  if (threadIdx.x == 0) s_last = atomic_add_acq_rel(&cnt[chunk], 1) == (int)gridDim.y - 1;
   __syncthreads();
   if (!s_last) return;
-  // last CTA of token t (reads other CTAs' results through L2, ld.cg):
-  // logits to shared memory, certified selection
-  for (int ee = threadIdx.x; ee < E; ee += blockDim.x) sl[ee] = __ldcg(&logits[(size_t)t * E + ee]);
+
+  // ---- last CTA of the chunk: stage logits, ||w_e||, ||x_t|| (one L2 trip)
+  float* sl = reinterpret_cast<float*>(dsm + router_small_group_ints(E, T * k, kGroup));
+  float* swn = sl + (size_t)kTT * E;
+  float* sxn = swn + E;
+  for (int i = threadIdx.x; i < nt * E; i += blockDim.x) sl[i] = __ldcg(logits + (size_t)t0 * E + i);
+  for (int i = threadIdx.x; i < E; i += blockDim.x) swn[i] = __ldcg(wnorm + i);
+  if (threadIdx.x < nt) sxn[threadIdx.x] = __ldcg(xnorm + t0 + threadIdx.x);
   __syncthreads();
-  if (E > 128) {   // many experts: every thread of the CTA helps rank them
-    rank_candidates(sl, E, scr, threadIdx.x, blockDim.x);
-    __syncthreads();
-  }
-  if (warp == 0) {
-    // ||x_t||, max ||w_e||, max |logit| for the error bound
-    float sqx = 0.f;
-    for (int h = lane * 8; h < H; h += 256) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        sqx = fmaf(bf16lo(xw[i]), bf16lo(xw[i]), sqx);
-        sqx = fmaf(bf16hi(xw[i]), bf16hi(xw[i]), sqx);
+  // Rank of every (token, expert) by counting the experts ahead of it:
+  // larger logit first, lower index first on equal logits, NaN last.  Four
+  // threads share an expert, thread q counting over j = q (mod 4).
+  const int nitems = nt * E * 4;
+  for (int base = 0; base < nitems; base += blockDim.x) {
+    const int it = base + threadIdx.x;
+    int r = 0, ee = 0, tt = 0;
+    float v = 0.f;
+    if (it < nitems) {
+      const int q = it & 3, pe = it >> 2;
+      tt = pe / E;
+      ee = pe - tt * E;
+      const float* row = sl + (size_t)tt * E;
+      v = rank_key(row[ee]);
+      for (int j = q; j < E; j += 4) {
+        const float o = rank_key(row[j]);
+        r += (o > v || (o == v && j < ee)) ? 1 : 0;
       }
     }
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    r += __shfl_xor_sync(0xffffffffu, r, 2);
+    if (it < nitems && (it & 3) == 0 && r < kCandCap) {
+      scr[tt].cand_e[r] = ee;
+      scr[tt].cand_v[r] = v;
+    }
+  }
+  __syncthreads();
+
+  if (warp < nt) {
+    const int t = t0 + warp;
+    WarpScratch& sc = scr[warp];
+    const float* row = sl + (size_t)warp * E;
     float wmax = 0.f, lmax = 0.f;
     for (int ee = lane; ee < E; ee += 32) {
-      wmax = fmaxf(wmax, __ldcg(&wnorm[ee]));
-      lmax = fmaxf(lmax, fabsf(sl[ee]));
+      wmax = fmaxf(wmax, swn[ee]);
+      lmax = fmaxf(lmax, fabsf(row[ee]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
       wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
       lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
     }
-    const float delta = gamma_bound(gamma_terms) * sqrtf(sqx) * wmax * (1.0f + 0x1p-10f) +
+    const float delta = gamma_bound(gamma_terms) * sxn[warp] * wmax * (1.0f + 0x1p-10f) +
                         0x1p-22f * lmax + (float)H * 0x1p-149f;
-    const float thr = cert_threshold(delta);
-    const int end = E <= 128 ? extract_small(sl, E, k, thr, scr) : certain_end_ranked(scr, E, k, thr);
-    select_token(E, k, delta, end, xr, gw, bias, H, l64 + (size_t)t * E, scr, idx + (size_t)t * k,
-                 w + (size_t)t * k, hdr);
+    const int end = certain_end_ranked(sc, E, k, cert_threshold(delta));
+    select_token(E, k, delta, end, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, sc,
+                 idx + (size_t)t * k, w + (size_t)t * k, hdr);
   }
   if constexpr (kGroup) {
-    if (warp == 0) __threadfence();   // the selecting warp wrote idx / w
-    __syncthreads();
-    if (threadIdx.x == 0) s_group = atomicAdd(&hdr->tokens_done, 1) == T - 1;
+    __syncthreads();   // the selecting warps' idx / w writes, then one release
+    if (threadIdx.x == 0) s_group = atomic_add_acq_rel(&hdr->tokens_done, nt) + nt == T;
     __syncthreads();
     if (!s_group) return;
     grouping::group_single_block(idx, T * k, E, go.large_threshold, go.tile_rows, go.counts,
-                                 go.offsets, go.perm, go.inv_perm, go.active, go.tiles, ws, gsmem,
+                                 go.offsets, go.perm, go.inv_perm, go.active, go.tiles, ws, dsm,
                                  sw, go.zero, go.nzero);
   }
 }
@@ -591,7 +682,9 @@ __global__ void __launch_bounds__(256) wnorm_kernel(const uint16_t* __restrict__
 
 }  // namespace
 
-bool route_can_group(int T, int E, int k) { return !(T >= 2048 && E <= 128) && T * k <= 8 * kPermBlock; }
+bool route_can_group(int T, int E, int k) {
+  return !(T >= 2048 && E <= 128) && T * k <= grouping::kSingleMaxSlots;
+}
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
                          int E, int k, int32_t* idx, float* w, void* ws, const WsLayout& L,
@@ -619,22 +712,31 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
                                                               logits, xnorm, wnorm, l64, idx, w, ws);
     return cudaGetLastError();
   }
-  float* logits = ws_ptr<float>(ws, L.logits);
-  int* cnt = ws_ptr<int>(ws, L.cnt);
-  dim3 g1(T, (E + kSmallWarps - 1) / kSmallWarps);
   const int gterms = H / 32 + 5;
-  if (group) {
-    const size_t smem = sizeof(int) * grouping::single_block_smem_ints(E);
-    cudaError_t err = cudaFuncSetAttribute(router_small_kernel<true>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const bool grp = group != nullptr;
+  const int tt = T <= 16 ? 1 : T <= 128 ? 4 : 8;
+  const size_t smem = router_small_smem(E, T * k, tt, grp);
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((T + tt - 1) / tt), (unsigned)((E + kSmallWarps - 1) / kSmallWarps));
+  int* cnt = ws_ptr<int>(ws, L.cnt);
+  float* logits = ws_ptr<float>(ws, L.logits);
+  float* xnorm = ws_ptr<float>(ws, L.xnorm);
+  const GroupOut go = grp ? *group : GroupOut{};
+  auto run = [&](auto kern) -> cudaError_t {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    router_small_kernel<true><<<g1, kSmallWarps * 32, smem, stream>>>(
-        x, gate_w, bias, T, H, E, k, gterms, logits, wnorm, l64, cnt, idx, w, ws, *group);
-  } else {
-    router_small_kernel<false><<<g1, kSmallWarps * 32, 0, stream>>>(
-        x, gate_w, bias, T, H, E, k, gterms, logits, wnorm, l64, cnt, idx, w, ws, GroupOut{});
+    kern<<<grid, kSmallWarps * 32, smem, stream>>>(x, gate_w, bias, T, H, E, k, gterms, logits, wnorm,
+                                                   xnorm, l64, cnt, idx, w, ws, go);
+    return cudaGetLastError();
+  };
+  if (grp) {
+    if (tt == 1) return run(router_small_kernel<1, true>);
+    if (tt == 4) return run(router_small_kernel<4, true>);
+    return run(router_small_kernel<8, true>);
   }
-  return cudaGetLastError();
+  if (tt == 1) return run(router_small_kernel<1, false>);
+  if (tt == 4) return run(router_small_kernel<4, false>);
+  return run(router_small_kernel<8, false>);
 }
 
 }  // namespace moe

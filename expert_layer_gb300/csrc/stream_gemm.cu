@@ -81,11 +81,11 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Pipeline shape per variant.
-template <bool kFp4>
+// Pipeline shape per variant (NT = 8-row token tiles per pass).
+template <bool kFp4, int NT = 1>
 struct StreamCfg {
   static constexpr int KB = kFp4 ? 128 : 32;      // K elements per block
-  static constexpr int KG = kFp4 ? 2 : 4;         // blocks per pipelined group
+  static constexpr int KG = kFp4 ? (NT == 1 ? 2 : 1) : 4;   // blocks per pipelined group
   static constexpr int NS = kFp4 ? 4 : 4;         // groups in the ring (NS-1 in flight)
   static constexpr int kWarps = 12;
   // per-warp ring: [NS][KG][2 rows][32 lanes] x 16 B of weights (codes), plus
@@ -99,12 +99,13 @@ struct StreamCfg {
 };
 
 // One (unit, pass) task of a warp: 16 weight rows of one expert over all of K,
-// against 8 of the expert's token rows (pass p covers rows 8p..8p+7).
+// against 8*NT of the expert's token rows (pass p covers rows 8NTp..).
 struct Task {
   long long u;   // unit index, < 0 when the warp has no more work
   int pass, npass, e, blk, m, off;
 };
 
+template <int NT>
 __device__ __forceinline__ void task_load(Task& t, const StreamGemmArgs& a, int UPE, long long U) {
   if (t.u >= U) { t.u = -1; return; }
   t.e = a.active[t.u / UPE];
@@ -112,19 +113,20 @@ __device__ __forceinline__ void task_load(Task& t, const StreamGemmArgs& a, int 
   t.m = a.counts[t.e];
   t.off = a.offsets[t.e];
   t.pass = 0;
-  t.npass = (t.m + 7) / 8;
+  t.npass = (t.m + 8 * NT - 1) / (8 * NT);
 }
 
+template <int NT>
 __device__ __forceinline__ void task_next(Task& t, const StreamGemmArgs& a, int UPE, long long U,
                                           long long stride) {
   if (++t.pass < t.npass) return;
   t.u += stride;
-  task_load(t, a, UPE, U);
+  task_load<NT>(t, a, UPE, U);
 }
 
 // B (token rows) of one K group for this thread: row g of the pass.
 template <bool kFp4, int KG>
-__device__ __forceinline__ void load_b(uint32_t (&b)[KG][StreamCfg<kFp4>::kBRegs],
+__device__ __forceinline__ void load_b(uint32_t (&b)[KG][StreamCfg<kFp4, 1>::kBRegs],
                                        const uint16_t* bsrc, int gi, int nkb, int c) {
 #pragma unroll
   for (int i = 0; i < KG; ++i) {
@@ -154,9 +156,9 @@ __device__ __forceinline__ void load_b(uint32_t (&b)[KG][StreamCfg<kFp4>::kBRegs
 // token rows stay in L1), chunks round-robin over CTAs (so hot experts spread
 // out).  Experts with more than 8 routed rows take several passes; later
 // passes re-read the unit's weights from L2.
-template <bool kDown, bool kFp4>
-__global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_kernel(StreamGemmArgs a) {
-  using C = StreamCfg<kFp4>;
+template <bool kDown, bool kFp4, int NT>
+__global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_gemm_kernel(StreamGemmArgs a) {
+  using C = StreamCfg<kFp4, NT>;
   constexpr int KB = C::KB, KG = C::KG, NS = C::NS, NW = C::kWarps;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ uint16_t lut8[kFp4 ? 256 : 1];
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
   // ---- producer side: the next group to copy
   Task it;
   it.u = (long long)blockIdx.x * NW + warp;
-  task_load(it, a, UPE, U);
+  task_load<NT>(it, a, UPE, U);
   int ig = 0;        // group index within the producer's task
   int slot_w = 0;    // ring slot the producer fills next
   auto issue_next = [&]() {
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
           cp_async16(d + 32, wb + Rhi * K + kc);
         }
       }
-      if (++ig == ngroups) { ig = 0; task_next(it, a, UPE, U, stride); }
+      if (++ig == ngroups) { ig = 0; task_next<NT>(it, a, UPE, U, stride); }
     }
     cp_async_commit();
     slot_w = slot_w + 1 == NS ? 0 : slot_w + 1;
@@ -237,25 +239,34 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
   // ---- consumer side
   Task ct;
   ct.u = (long long)blockIdx.x * NW + warp;
-  task_load(ct, a, UPE, U);
+  task_load<NT>(ct, a, UPE, U);
   int slot_r = 0;
   while (ct.u >= 0) {
-    const int p0 = ct.pass * 8;
-    const uint16_t* bsrc = nullptr;
-    {
-      const int n = p0 + g;
+    const int p0 = ct.pass * 8 * NT;
+    const uint16_t* bsrc[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = p0 + nt * 8 + g;
+      bsrc[nt] = nullptr;
       if (n < ct.m) {
-        if (kDown) bsrc = a.h + (size_t)(ct.off + n) * a.I;
-        else bsrc = a.x + (size_t)(a.perm[ct.off + n] / a.k) * a.H;
+        if (kDown) bsrc[nt] = a.h + (size_t)(ct.off + n) * a.I;
+        else bsrc[nt] = a.x + (size_t)(a.perm[ct.off + n] / a.k) * a.H;
       }
     }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t bc[KG][C::kBRegs], bn[KG][C::kBRegs];
-    load_b<kFp4, KG>(bc, bsrc, 0, nkb, c);
+    const int ntiles = min(NT, (ct.m - p0 + 7) / 8);
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    uint32_t bc[NT][KG][C::kBRegs], bn[NT][KG][C::kBRegs];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) load_b<kFp4, KG>(bc[nt], nt < ntiles ? bsrc[nt] : nullptr, 0, nkb, c);
 
 #pragma unroll 1
     for (int gi = 0; gi < ngroups; ++gi) {
-      if (gi + 1 < ngroups) load_b<kFp4, KG>(bn, bsrc, gi + 1, nkb, c);
+      if (gi + 1 < ngroups) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) load_b<kFp4, KG>(bn[nt], nt < ntiles ? bsrc[nt] : nullptr, gi + 1, nkb, c);
+      }
       cp_async_wait<NS - 2>();
 #pragma unroll
       for (int i = 0; i < KG; ++i) {
@@ -288,19 +299,28 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
             const uint32_t a2 = bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2[q >> 2]);
             const uint32_t a1 = bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2[q >> 2]);
             const uint32_t a3 = bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2[q >> 2]);
-            mma_bf16_16816(acc, a0, a1, a2, a3, bc[i][2 * q], bc[i][2 * q + 1]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              if (nt < ntiles) mma_bf16_16816(acc[nt], a0, a1, a2, a3, bc[nt][i][2 * q], bc[nt][i][2 * q + 1]);
           }
         } else {
-          mma_bf16_16816(acc, alo.x, ahi.x, alo.y, ahi.y, bc[i][0], bc[i][1]);
-          mma_bf16_16816(acc, alo.z, ahi.z, alo.w, ahi.w, bc[i][2], bc[i][3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (nt < ntiles) {
+              mma_bf16_16816(acc[nt], alo.x, ahi.x, alo.y, ahi.y, bc[nt][i][0], bc[nt][i][1]);
+              mma_bf16_16816(acc[nt], alo.z, ahi.z, alo.w, ahi.w, bc[nt][i][2], bc[nt][i][3]);
+            }
+          }
         }
       }
       slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
       issue_next();
 #pragma unroll
-      for (int i = 0; i < KG; ++i)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < C::kBRegs; ++j) bc[i][j] = bn[i][j];
+        for (int i = 0; i < KG; ++i)
+#pragma unroll
+          for (int j = 0; j < C::kBRegs; ++j) bc[nt][i][j] = bn[nt][i][j];
     }
 
     // epilogue straight from the fragments: c0,c1 = row g, tokens 2c,2c+1;
@@ -308,35 +328,39 @@ __global__ void __launch_bounds__(StreamCfg<kFp4>::kWarps * 32, 1) stream_gemm_k
     float gscale = 1.0f;
     if constexpr (kFp4) gscale = kDown ? a.dn_global[ct.e] : a.gu_global[ct.e];
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int n = p0 + 2 * c + h2;
-      if (n < ct.m) {
-        if (!kDown) {
-          const float gv = acc[h2] * gscale, uv = acc[2 + h2] * gscale;
-          a.h[(size_t)(ct.off + n) * a.I + ct.blk * 8 + g] = f2bf(silu(gv) * uv);
-        } else {
-          const int f = a.perm[ct.off + n];
-          const float wt = a.topk_w[f];
-          const float y0 = wt * (acc[h2] * gscale), y1 = wt * (acc[2 + h2] * gscale);
-          const size_t o = (size_t)f * a.H + ct.blk * 16 + g;
-          if (a.partial_f32) {
-            reinterpret_cast<float*>(a.partial)[o] = y0;
-            reinterpret_cast<float*>(a.partial)[o + 8] = y1;
+    for (int nt = 0; nt < NT; ++nt) {
+      if (nt >= ntiles) continue;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int n = p0 + nt * 8 + 2 * c + h2;
+        if (n < ct.m) {
+          if (!kDown) {
+            const float gv = acc[nt][h2] * gscale, uv = acc[nt][2 + h2] * gscale;
+            a.h[(size_t)(ct.off + n) * a.I + ct.blk * 8 + g] = f2bf(silu(gv) * uv);
           } else {
-            reinterpret_cast<uint16_t*>(a.partial)[o] = f2bf(y0);
-            reinterpret_cast<uint16_t*>(a.partial)[o + 8] = f2bf(y1);
+            const int f = a.perm[ct.off + n];
+            const float wt = a.topk_w[f];
+            const float y0 = wt * (acc[nt][h2] * gscale), y1 = wt * (acc[nt][2 + h2] * gscale);
+            const size_t o = (size_t)f * a.H + ct.blk * 16 + g;
+            if (a.partial_f32) {
+              reinterpret_cast<float*>(a.partial)[o] = y0;
+              reinterpret_cast<float*>(a.partial)[o + 8] = y1;
+            } else {
+              reinterpret_cast<uint16_t*>(a.partial)[o] = f2bf(y0);
+              reinterpret_cast<uint16_t*>(a.partial)[o + 8] = f2bf(y1);
+            }
           }
         }
       }
     }
-    task_next(ct, a, UPE, U, stride);
+    task_next<NT>(ct, a, UPE, U, stride);
   }
   cp_async_wait<0>();
 }
 
-template <bool kDown, bool kFp4>
+template <bool kDown, bool kFp4, int NT>
 cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
-  using C = StreamCfg<kFp4>;
+  using C = StreamCfg<kFp4, NT>;
   const long long S = (long long)a.T * a.k;
   const long long max_active = S < a.E ? S : a.E;
   const long long UPE = kDown ? a.H / 16 : a.I / 8;
@@ -346,7 +370,7 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
   const int smem = C::kWarpBytes * C::kWarps + C::kLutBytes;
-  cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<kDown, kFp4>,
+  cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<kDown, kFp4, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -359,14 +383,18 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = kDown ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<kDown, kFp4>, a);
+  return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<kDown, kFp4, NT>, a);
 }
 
 template <bool kDown>
 cudaError_t launch_stream(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
-  if (a.gu_codes != nullptr) return launch_variant<kDown, true>(a, stream);
-  return launch_variant<kDown, false>(a, stream);
+  // a group never holds more rows than the batch has tokens: one 8-row tile
+  // per pass for T <= 8, two above
+  const bool two = a.T > 8;
+  if (a.gu_codes != nullptr)
+    return two ? launch_variant<kDown, true, 2>(a, stream) : launch_variant<kDown, true, 1>(a, stream);
+  return two ? launch_variant<kDown, false, 2>(a, stream) : launch_variant<kDown, false, 1>(a, stream);
 }
 
 }  // namespace
