@@ -37,7 +37,7 @@ if "reference" in sys.argv:
 DEFAULT_WORKLOAD = "decode8"
 WEIGHT_SETS = 4
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-STAGES = ["route", "permute", "gate_up", "down", "combine"]
+STAGES = ["route", "permute", "stream", "tc", "combine"]
 
 
 def parse_args():
@@ -57,10 +57,8 @@ def parse_args():
 
 
 STAGE_SOURCES = {
-    "gate_up": ["expert_layer_gb300/csrc/stream_gemm.cu", "expert_layer_gb300/csrc/common.cuh",
-                "expert_layer_gb300/csrc/kernels.h"],
-    "down": ["expert_layer_gb300/csrc/stream_gemm.cu", "expert_layer_gb300/csrc/common.cuh",
-             "expert_layer_gb300/csrc/kernels.h"],
+    "stream": ["expert_layer_gb300/csrc/stream_gemm.cu", "expert_layer_gb300/csrc/common.cuh",
+               "expert_layer_gb300/csrc/kernels.h"],
 }
 
 
@@ -158,26 +156,40 @@ def pci_bus_id(dev_index: int):
 
 
 # ------------------------------------------------------------------ work model
-def algorithmic_bytes(inp, A: int):
-    """Compulsory HBM bytes per stage for one forward (A active experts)."""
+def group_split(inp, counts):
+    """Experts and routed rows served by the weight-streaming kernel (small
+    groups) and by the tensor-core kernels (large groups), with the same
+    threshold rule as the library."""
+    T, H, k = inp.T, inp.H, inp.top_k
+    thr = 32 if T * k >= 8192 else 65
+    use_tc = inp.nvfp4_gate_up is None and T >= thr and H % 256 == 0
+    act = [int(c) for c in counts if c > 0]
+    large = [c for c in act if use_tc and c >= thr]
+    small = [c for c in act if not (use_tc and c >= thr)]
+    return {"A_s": len(small), "S_s": sum(small), "A_l": len(large), "S_l": sum(large)}
+
+
+def algorithmic_bytes(inp, split):
+    """Compulsory HBM bytes per stage for one forward."""
     T, H, E, k, I = inp.T, inp.H, inp.E, inp.top_k, inp.I
     S = T * k
     wb = 0.5 + 1.0 / 16 if inp.nvfp4_gate_up is not None else 2.0   # bytes per weight
-    partial_b = 4 if S * H * 4 <= (32 << 20) else 2
+    pb = 4 if S * H * 4 <= (32 << 20) else 2                        # bytes per partial
+    per_row = H * 2 + 2 * I * 2 + H * pb   # token row in, h out and back in, partial out
+    A = split["A_s"] + split["A_l"]
     return {
         "route": E * H * 2 + T * H * 2 + S * 8,
         "permute": S * 4 * 4 + E * 12,
-        "gate_up": A * 2 * I * H * wb + T * H * 2 + S * I * 2,
-        "down": A * H * I * wb + S * I * 2 + S * H * partial_b,
-        "combine": S * H * partial_b + T * H * 2,
+        "stream": split["A_s"] * 3 * I * H * wb + split["S_s"] * per_row,
+        "tc": split["A_l"] * 3 * I * H * 2 + split["S_l"] * per_row,
+        "combine": S * H * pb + T * H * 2,
         "weights": A * 3 * I * H * wb,
     }
 
 
-def algorithmic_flops(inp):
-    S = inp.T * inp.top_k
-    return {"route": 2 * inp.T * inp.E * inp.H, "gate_up": 2 * S * 2 * inp.I * inp.H,
-            "down": 2 * S * inp.H * inp.I}
+def algorithmic_flops(inp, split):
+    return {"route": 2 * inp.T * inp.E * inp.H, "stream": 2 * split["S_s"] * 3 * inp.I * inp.H,
+            "tc": 2 * split["S_l"] * 3 * inp.I * inp.H}
 
 
 # ------------------------------------------------------------------ CPU baseline (oracle)
@@ -327,6 +339,10 @@ def run_ours(args):
 
     diag = moe.read_diagnostics(ws)
     A = diag["num_active"]
+    idx_probe = torch.empty((T, k), dtype=torch.int32, device=dev)
+    moe.forward(inp.x, inp.gate_w, inp.bias, inp.w_gate_up, inp.w_down, k, nvfp4_gate_up=inp.nvfp4_gate_up,
+                nvfp4_down=inp.nvfp4_down, workspace=ws, topk_idx=idx_probe)
+    split = group_split(inp, torch.bincount(idx_probe.flatten().long(), minlength=E).cpu().tolist())
     router_diag = {"tokens_fp64_checked": diag["router_flagged"], "tokens_fp64_all": diag["router_fallback"],
                    "experts_on_tensor_cores": diag["num_large"]}
     assert moe.read_status(ws) == 0
@@ -405,12 +421,11 @@ def run_ours(args):
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
-    byt = algorithmic_bytes(inp, A)
-    flops = algorithmic_flops(inp)
-    dom = max(("gate_up", "down", "route", "combine", "permute"), key=lambda s: stage_ms[s])
+    byt = algorithmic_bytes(inp, split)
+    flops = algorithmic_flops(inp, split)
+    dom = max(("stream", "tc", "route", "combine", "permute"), key=lambda s: stage_ms[s])
     dom_s = stage_ms[dom] / 1e3
-    tensor_bound = args.workload.startswith("prefill") and dom in ("gate_up", "down")
-    if tensor_bound:
+    if dom == "tc":
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         achieved = flops[dom] / dom_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -421,11 +436,12 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": measured_traffic(args.workload, dom)}
     roof.update({"kernel": dom, "peak_source": f"{peak_src} MEASURED_PEAKS.json" if peak_src == "measured"
-                 else "fallback", "algorithmic_bytes": byt[dom], "launch_us": stage_ms[dom] * 1e3})
+                 else "fallback", "algorithmic_bytes": byt[dom],
+                 "algorithmic_flops": flops.get(dom), "launch_us": stage_ms[dom] * 1e3})
     step_ms = ms / K
     layer = {"weights_bytes": byt["weights"], "weights_gbs": byt["weights"] / (step_ms / 1e3) / 1e9,
              "weights_frac_of_hbm": byt["weights"] / (step_ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6800.0),
-             "active_experts": A, "stage_us": {s: round(stage_ms[s] * 1e3, 2) for s in STAGES},
+             "active_experts": A, "groups": split, "stage_us": {s: round(stage_ms[s] * 1e3, 2) for s in STAGES},
              "router": router_diag}
 
     cpu = None

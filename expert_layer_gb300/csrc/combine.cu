@@ -4,7 +4,7 @@
 // summed in slot order in fp32, with no atomics, so the result is bitwise
 // reproducible and does not depend on how slots were grouped.  The partials
 // already carry the routing weight.  HBM-bound: one read of S*H partials and
-// one write of T*H outputs, 16-byte vectors, grid-stride over T*H/8.
+// one write of T*H outputs, grid-stride over 16-byte vectors of partials.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -12,35 +12,62 @@ namespace moe {
 
 namespace {
 
+// Thread = V consecutive outputs of one token (one 16-byte vector of
+// partials per slot: V = 4 fp32 or 8 bf16).  The k partial vectors are loaded
+// in batches of 8 before any is added, so a thread waits on memory once per
+// batch rather than once per slot; the additions still run in slot order
+// from zero.
 template <bool kF32>
 __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ partial, int T, int H,
                                                       int k, uint16_t* __restrict__ out) {
+  constexpr int V = kF32 ? 4 : 8;
   pdl_wait();   // the partials of the down projection are complete
-  const long long nvec = (long long)T * (H / 8);
+  const long long nvec = (long long)T * (H / V);
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < nvec;
        v += (long long)gridDim.x * blockDim.x) {
-    const long long t = v / (H / 8);
-    const int d = (int)(v % (H / 8)) * 8;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < k; ++s) {
-      const size_t row = (size_t)(t * k + s) * H + d;
-      if constexpr (kF32) {
-        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(partial) + row);
-        const float4 lo = p[0], hi = p[1];
-        acc[0] += lo.x; acc[1] += lo.y; acc[2] += lo.z; acc[3] += lo.w;
-        acc[4] += hi.x; acc[5] += hi.y; acc[6] += hi.z; acc[7] += hi.w;
-      } else {
-        const uint4 q = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(partial) + row);
-        acc[0] += bf16lo(q.x); acc[1] += bf16hi(q.x); acc[2] += bf16lo(q.y); acc[3] += bf16hi(q.y);
-        acc[4] += bf16lo(q.z); acc[5] += bf16hi(q.z); acc[6] += bf16lo(q.w); acc[7] += bf16hi(q.w);
+    const long long t = v / (H / V);
+    const int d = (int)(v % (H / V)) * V;
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    for (int s0 = 0; s0 < k; s0 += 8) {
+      uint4 q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        q[j] = make_uint4(0, 0, 0, 0);
+        if (s0 + j < k) {
+          const size_t row = (size_t)(t * k + s0 + j) * H + d;
+          q[j] = kF32 ? *reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(partial) + row)
+                      : *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(partial) + row);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j < k) {
+          const uint32_t w4[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+          if constexpr (kF32) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] += __uint_as_float(w4[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { acc[2 * i] += bf16lo(w4[i]); acc[2 * i + 1] += bf16hi(w4[i]); }
+          }
+        }
       }
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(out + (size_t)t * H + d) = o;
+    if constexpr (kF32) {
+      uint2 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      *reinterpret_cast<uint2*>(out + (size_t)t * H + d) = o;
+    } else {
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(out + (size_t)t * H + d) = o;
+    }
   }
 }
 
@@ -49,7 +76,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ p
 cudaError_t launch_combine(const void* partial, bool partial_f32, int T, int H, int k,
                            uint16_t* out, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
-  const long long nvec = (long long)T * (H / 8);
+  const long long nvec = (long long)T * (H / (partial_f32 ? 4 : 8));
   long long grid = (nvec + 255) / 256;
   if (grid > 152 * 8) grid = 152 * 8;
   // programmatic launch: the combine's CTAs may become resident while the down

@@ -29,7 +29,7 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte slot");
 
 // Offsets (bytes) of every workspace region for one shape.
 struct WsLayout {
-  size_t hdr, cnt, xnorm, wnorm, logits, logits64, idx, w, counts, offsets, active, tiles, blk_cnt,
+  size_t hdr, sched, cnt, xnorm, wnorm, logits, logits64, idx, w, counts, offsets, active, tiles, blk_cnt,
       blk_base, lrank, perm, inv_perm, h, partial, xp, total;
   int nblk;               // 512-slot blocks of the grouping kernels
   bool partial_f32;       // fp32 partials (else bf16)
@@ -48,6 +48,7 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
   L.nblk = (int)((S + kPermBlock - 1) / kPermBlock);
   L.partial_f32 = (size_t)S * (size_t)H * 4 <= kPartialF32Limit;
   L.hdr = take(sizeof(WsHeader));
+  L.sched = take(sizeof(int) * (E + 1));   // expert-GEMM queue counter, then per-slot counters
   L.cnt = take(sizeof(int) * T);
   L.xnorm = take(sizeof(float) * T);
   L.wnorm = take(sizeof(float) * E);
@@ -72,7 +73,8 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
 }
 
 // Bytes at the start of the workspace that must be zero when a call starts
-// (header and per-token counters); every entry point clears them on its stream.
+// (header, scheduling counters and per-chunk counters); every entry point
+// clears them on its stream.
 inline size_t zeroed_prefix(const WsLayout& L) { return L.xnorm; }
 
 template <typename T>

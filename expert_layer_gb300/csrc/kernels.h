@@ -19,6 +19,10 @@ struct GroupOut {
   int nzero;
 };
 
+// moe_api.cu -- clears the first `bytes` (a multiple of 16) of the workspace;
+// lets the next kernel (a programmatic dependent) start launching at once
+cudaError_t launch_zero(void* ws, size_t bytes, cudaStream_t stream);
+
 // router.cu -- logits, certified top-k, renormalised weights; with `group`
 // (only where route_can_group) also the grouping, in the same launch
 bool route_can_group(int T, int E, int k);
@@ -57,10 +61,15 @@ struct StreamGemmArgs {
   const float* topk_w;       // [S]
   void* partial;             // [S, H] fp32 or bf16, slot order
   bool partial_f32;
+  // scheduling (zero at launch): unit queue ticket counter and, per active
+  // slot, the number of gate/up units whose h rows are published
+  int* queue;
+  int* dep;
+  int* status;               // workspace status word (kStatusTimeout)
   int num_sms;
 };
-cudaError_t launch_stream_gate_up(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
-cudaError_t launch_stream_down(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
+// gate/up then down of the small groups, one persistent launch
+cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
 
 // tc_gemm.cu -- tcgen05/TMEM grouped GEMMs for experts with many rows (bf16 weights)
 struct TcLaunch {

@@ -11,6 +11,30 @@
 
 using namespace moe;
 
+namespace moe {
+
+namespace {
+// The workspace prefix that must start at zero.  The first thing it does is
+// allow the next kernel (launched as a programmatic dependent) to become
+// resident; that kernel waits for this one's stores before reading anything.
+__global__ void __launch_bounds__(256) zero_kernel(uint4* __restrict__ p, int n16) {
+  pdl_trigger();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x)
+    p[i] = make_uint4(0, 0, 0, 0);
+}
+}  // namespace
+
+cudaError_t launch_zero(void* ws, size_t bytes, cudaStream_t stream) {
+  const int n16 = (int)(bytes / 16);
+  int grid = (n16 + 255) / 256;
+  if (grid > 64) grid = 64;
+  if (grid < 1) grid = 1;
+  zero_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<uint4*>(ws), n16);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
+
 namespace {
 
 // Group size from which an expert runs on the tensor-core kernels: at
@@ -102,7 +126,7 @@ int moe_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int 
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   MOE_TRY(check_device(nullptr));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
+  MOE_TRY_CUDA(launch_zero(workspace, zeroed_prefix(L), s));
   return cuda_status(
       launch_route(x, gate_w, bias, T, H, E, top_k, topk_idx, topk_w, workspace, L, s, nullptr,
                    nullptr));
@@ -123,7 +147,7 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int top_k, int32_t* count
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   MOE_TRY(check_device(nullptr));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
+  MOE_TRY_CUDA(launch_zero(workspace, zeroed_prefix(L), s));
   return cuda_status(launch_permute(topk_idx, T, E, top_k, counts, offsets, perm, inv_perm,
                                     workspace, L, INT_MAX, 128, s, nullptr));
 }
@@ -181,7 +205,8 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   const bool fuse = !use_tc && route_can_group(T, E, top_k);
 
   MOE_TRY_CUDA(mark(0));
-  MOE_TRY_CUDA(cudaMemsetAsync(workspace, 0, zeroed_prefix(L), s));
+  MOE_TRY_CUDA(launch_zero(workspace, zeroed_prefix(L), s));
+  if (launches) *launches += 1;
   if (fuse) {
     GroupOut go{counts, offsets, perm, inv_perm, ws_ptr<int32_t>(workspace, L.active),
                 ws_ptr<int32_t>(workspace, L.tiles), INT_MAX, kTcRows, nullptr, 0};
@@ -214,6 +239,9 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   a.topk_w = w;
   a.partial = ws_ptr<void>(workspace, L.partial);
   a.partial_f32 = L.partial_f32;
+  a.queue = ws_ptr<int>(workspace, L.sched);
+  a.dep = a.queue + 1;
+  a.status = &hdr->status;
   a.num_sms = num_sms;
   TcLaunch tc{};
   tc.T = T; tc.H = H; tc.E = E; tc.I = I; tc.k = top_k;
@@ -224,11 +252,12 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   tc.h = a.h; tc.partial = a.partial; tc.partial_f32 = L.partial_f32;
   tc.status = &hdr->status; tc.num_sms = num_sms;
 
-  MOE_TRY_CUDA(launch_stream_gate_up(a, s, launches));
-  if (use_tc) MOE_TRY_CUDA(launch_tc_gemm(tc, false, s, launches));
+  MOE_TRY_CUDA(launch_stream_gemm(a, s, launches));
   MOE_TRY_CUDA(mark(3));
-  MOE_TRY_CUDA(launch_stream_down(a, s, launches));
-  if (use_tc) MOE_TRY_CUDA(launch_tc_gemm(tc, true, s, launches));
+  if (use_tc) {
+    MOE_TRY_CUDA(launch_tc_gemm(tc, false, s, launches));
+    MOE_TRY_CUDA(launch_tc_gemm(tc, true, s, launches));
+  }
   MOE_TRY_CUDA(mark(4));
   MOE_TRY_CUDA(launch_combine(a.partial, L.partial_f32, T, H, top_k, out, s, launches));
   MOE_TRY_CUDA(mark(5));

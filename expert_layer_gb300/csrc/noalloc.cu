@@ -32,11 +32,11 @@ namespace {
 // Largest T*E the array serves; T itself is also bounded (xnorm holds T floats).
 constexpr long long kNoAllocMaxTE = 65536;
 constexpr long long kNoAllocMaxT = 8192;
-// header + counters[T] + xnorm[T] + wnorm[E] + fp32 logits[T*E] + fp64
-// logits[T*E], each region 256-byte aligned (the router's part of the
-// workspace layout)
-constexpr size_t kNoAllocScratchBytes = 256 + 2 * kNoAllocMaxT * 4 + 1024 * 4 + kNoAllocMaxTE * 4 +
-                                        kNoAllocMaxTE * 8 + 5 * 256;
+// header + scheduling counters[E+1] + counters[T] + xnorm[T] + wnorm[E] +
+// fp32 logits[T*E] + fp64 logits[T*E], each region 256-byte aligned (the
+// router's part of the workspace layout)
+constexpr size_t kNoAllocScratchBytes = 256 + 1025 * 4 + 2 * kNoAllocMaxT * 4 + 1024 * 4 +
+                                        kNoAllocMaxTE * 4 + kNoAllocMaxTE * 8 + 6 * 256;
 
 __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratchBytes];
 
@@ -86,7 +86,7 @@ extern "C" int moe_route_noalloc(const uint16_t* x, const uint16_t* gate_w, cons
   const int rc = scratch_address(&scratch);
   if (rc != MOE_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, moe::zeroed_prefix(L), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_zero(scratch, moe::zeroed_prefix(L), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (moe::launch_route(x, gate_w, bias, T, H, E, top_k, topk_idx, topk_w, scratch, L, s,
                         nullptr, nullptr) != cudaSuccess)
     return MOE_ERR_CUDA;

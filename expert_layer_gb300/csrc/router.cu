@@ -330,7 +330,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
   __shared__ WarpScratch scr[kTT];
   __shared__ int s_last, s_group;
   __shared__ int4 sw[grouping::kWarps];
-  pdl_wait();
+  pdl_wait();      // the workspace counters are cleared
+  pdl_trigger();   // the expert kernel may become resident; it waits for this grid
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x;
   const int t0 = chunk * kTT;
@@ -725,9 +726,20 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
   auto run = [&](auto kern) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kSmallWarps * 32, smem, stream>>>(x, gate_w, bias, T, H, E, k, gterms, logits, wnorm,
-                                                   xnorm, l64, cnt, idx, w, ws, go);
-    return cudaGetLastError();
+    // programmatic launch: the CTAs may become resident while the workspace
+    // is being cleared and wait for it on the device
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kSmallWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, x, gate_w, bias, T, H, E, k, gterms, logits, wnorm, xnorm,
+                              l64, cnt, idx, w, ws, go);
   };
   if (grp) {
     if (tt == 1) return run(router_small_kernel<1, true>);

@@ -98,36 +98,61 @@ struct StreamCfg {
   static constexpr int kBRegs = kFp4 ? 16 : 4;    // 32-bit B registers per block
 };
 
-// One (unit, pass) task of a warp: 16 weight rows of one expert over all of K,
-// against 8*NT of the expert's token rows (pass p covers rows 8NTp..).
-struct Task {
-  long long u;   // unit index, < 0 when the warp has no more work
-  int pass, npass, e, blk, m, off;
+// Bounded waits: polls before a wait gives up (and the kernel records
+// kStatusTimeout); with the sleep between polls this is well over a second.
+constexpr int kSpinLimit = 1 << 22;
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Queue positions [0, Ug) are gate/up units, [Ug, Q) down units, each in
+// active-list order (unit = 16 weight rows of one expert over all of K).
+struct Queue {
+  int UPEg, UPEd, Ug, Q, nkb_g, nkb_d;
 };
 
-template <int NT>
-__device__ __forceinline__ void task_load(Task& t, const StreamGemmArgs& a, int UPE, long long U) {
-  if (t.u >= U) { t.u = -1; return; }
-  t.e = a.active[t.u / UPE];
-  t.blk = (int)(t.u % UPE);
-  t.m = a.counts[t.e];
-  t.off = a.offsets[t.e];
+// One unit of a warp, taken in passes of 8*NT of the expert's token rows
+// (pass p covers rows 8NTp..).
+struct Task {
+  int q;         // queue position, < 0 when the warp has no more work
+  bool down;
+  int slot, e, blk, m, off, pass, npass, nkb, ngroups;
+};
+
+// Rows of the routed-slot permutation kept in shared memory (else read from
+// global memory).
+constexpr int kPermSmem = 4096;
+
+template <int KG, int NT>
+__device__ __forceinline__ void task_load(Task& t, const int4* smeta, const Queue& qs, int q) {
+  if (q < 0 || q >= qs.Q) { t.q = -1; return; }
+  t.q = q;
+  t.down = q >= qs.Ug;
+  const int r = t.down ? q - qs.Ug : q;
+  const int upe = t.down ? qs.UPEd : qs.UPEg;
+  t.slot = r / upe;
+  t.blk = r - t.slot * upe;
+  const int4 md = smeta[t.slot];   // expert, rows, first grouped row
+  t.e = md.x;
+  t.m = md.y;
+  t.off = md.z;
   t.pass = 0;
   t.npass = (t.m + 8 * NT - 1) / (8 * NT);
+  t.nkb = t.down ? qs.nkb_d : qs.nkb_g;
+  t.ngroups = (t.nkb + KG - 1) / KG;
 }
 
-template <int NT>
-__device__ __forceinline__ void task_next(Task& t, const StreamGemmArgs& a, int UPE, long long U,
-                                          long long stride) {
-  if (++t.pass < t.npass) return;
-  t.u += stride;
-  task_load<NT>(t, a, UPE, U);
-}
-
-// B (token rows) of one K group for this thread: row g of the pass.
+// B (token rows) of one K group for this thread: row g of the pass.  Down
+// reads h, written earlier in the same launch, through L2 (ld.cg).
 template <bool kFp4, int KG>
 __device__ __forceinline__ void load_b(uint32_t (&b)[KG][StreamCfg<kFp4, 1>::kBRegs],
-                                       const uint16_t* bsrc, int gi, int nkb, int c) {
+                                       const uint16_t* bsrc, int gi, int nkb, int c, bool cg) {
 #pragma unroll
   for (int i = 0; i < KG; ++i) {
     const int kb = gi * KG + i;
@@ -135,40 +160,53 @@ __device__ __forceinline__ void load_b(uint32_t (&b)[KG][StreamCfg<kFp4, 1>::kBR
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         uint4 t = make_uint4(0, 0, 0, 0);
-        if (bsrc && kb < nkb) t = *reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 128 + 32 * c + 8 * v);
+        if (bsrc && kb < nkb) {
+          const uint4* p = reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 128 + 32 * c + 8 * v);
+          t = cg ? __ldcg(p) : *p;
+        }
         b[i][4 * v + 0] = t.x; b[i][4 * v + 1] = t.y; b[i][4 * v + 2] = t.z; b[i][4 * v + 3] = t.w;
       }
     } else {
       uint4 t = make_uint4(0, 0, 0, 0);
-      if (bsrc) t = *reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 32 + 8 * c);
+      if (bsrc && kb < nkb) {
+        const uint4* p = reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 32 + 8 * c);
+        t = cg ? __ldcg(p) : *p;
+      }
       b[i][0] = t.x; b[i][1] = t.y; b[i][2] = t.z; b[i][3] = t.w;
     }
   }
 }
 
-// Each warp owns whole work units (16 weight rows x all of K): no cross-warp
-// reduction.  Weights stream through a private per-thread ring in shared
-// memory filled by cp.async (each thread copies exactly the 16-byte pieces it
-// will later read, so no barrier is needed), NS-1 groups ahead of the mma,
-// across unit boundaries; the token rows (B) of the next group are loaded into
-// registers one group ahead.  Units are dealt in chunks of kWarps consecutive
-// units (one per warp, so the warps of a CTA mostly share an expert and its
-// token rows stay in L1), chunks round-robin over CTAs (so hot experts spread
-// out).  Experts with more than 8 routed rows take several passes; later
-// passes re-read the unit's weights from L2.
-template <bool kDown, bool kFp4, int NT>
+// Gate/up and down of the small groups in one persistent launch.  Each warp
+// owns whole units: no cross-warp reduction, so results do not depend on the
+// launch shape.  A warp takes its first unit by its global index and every
+// later one from an atomic queue counter, requested one unit early so the
+// atomic's latency is hidden; the dynamic queue keeps the warps busy to the
+// end of the layer instead of to the end of each projection.  A down unit of
+// expert e waits until every gate/up unit of e has published its h rows (a
+// per-expert counter, release / acquire).  All gate/up positions precede all
+// down positions and a warp takes positions in increasing order, so no warp
+// holds a gate/up unit behind a waiting down unit: every wait ends.
+// Weights stream through a private per-thread ring in shared memory filled by
+// cp.async (each thread copies exactly the 16-byte pieces it will later
+// read), NS-1 groups ahead of the mma and across unit boundaries; the token
+// rows (B) of the next group are loaded into registers one group ahead.
+// Experts with more than 8*NT routed rows take several passes; later passes
+// re-read the unit's weights from L2.
+template <bool kFp4, int NT>
 __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_gemm_kernel(StreamGemmArgs a) {
   using C = StreamCfg<kFp4, NT>;
   constexpr int KB = C::KB, KG = C::KG, NS = C::NS, NW = C::kWarps;
+  constexpr int kFifo = 8;   // > NS: unit ids the producer may hold ahead of the consumer
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ uint16_t lut8[kFp4 ? 256 : 1];
+  __shared__ int fifo[NW][kFifo];
   uint32_t* lut2 = reinterpret_cast<uint32_t*>(smem + NW * C::kWarpBytes);   // [256][32]
+  int4* smeta = reinterpret_cast<int4*>(smem + NW * C::kWarpBytes + C::kLutBytes);   // [E]
+  int* sperm = reinterpret_cast<int*>(smeta + a.E);                                 // [S]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int K = kDown ? a.I : a.H;
-  const int NR = kDown ? a.H : 2 * a.I;     // weight rows per expert
-  const int UPE = kDown ? a.H / 16 : a.I / 8;
   uint4* ring = reinterpret_cast<uint4*>(smem + warp * C::kWarpBytes);
   uint2* sring = reinterpret_cast<uint2*>(smem + warp * C::kWarpBytes + C::kWBytes);
 
@@ -181,51 +219,95 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
     __syncthreads();
   }
 
-  // gate/up reads the grouping of the kernel just before it; down may start
-  // early (programmatic launch) and streams its first weights before waiting
-  // for h, since the grouping it needs finished before gate/up began
-  if (!kDown) { pdl_wait(); pdl_trigger(); }
+  // the grouping is complete once the kernel before this one is; the
+  // combine may start launching
+  pdl_wait();
+  pdl_trigger();
+  Queue qs;
   const int nsmall = *a.num_active - (a.num_large ? *a.num_large : 0);
-  const long long U = (long long)nsmall * UPE;
-  const long long stride = (long long)gridDim.x * NW;
-  const int nkb = K / KB;
-  const int ngroups = (nkb + KG - 1) / KG;
+  qs.UPEg = a.I / 8;
+  qs.UPEd = a.H / 16;
+  qs.Ug = nsmall * qs.UPEg;
+  qs.Q = qs.Ug + nsmall * qs.UPEd;
+  qs.nkb_g = a.H / KB;
+  qs.nkb_d = a.I / KB;
+  const int nwarps = (int)gridDim.x * NW;
+  // the small groups' metadata, and the slot permutation when it is short,
+  // once per CTA: no dependent global loads when a warp changes unit
+  const int S = a.T * a.k;
+  const bool perm_smem = S <= kPermSmem;
+  for (int i = threadIdx.x; i < nsmall; i += blockDim.x) {
+    const int e = a.active[i];
+    smeta[i] = make_int4(e, a.counts[e], a.offsets[e], 0);
+  }
+  if (perm_smem)
+    for (int i = threadIdx.x; i < S; i += blockDim.x) sperm[i] = a.perm[i];
+  __syncthreads();
+  const int* permp = perm_smem ? sperm : a.perm;
+
+  // unit ids: the first by global warp index, later ones nwarps + ticket
+  int pending = 0;   // lane 0: the next ticket, requested one unit early
+  if (lane == 0) pending = nwarps + atomicAdd(a.queue, 1);
+  int first = (int)blockIdx.x * NW + warp;
+  auto fetch = [&]() -> int {
+    if (first >= 0) { const int q = first; first = -1; return q; }
+    const int q = __shfl_sync(0xffffffffu, pending, 0);
+    if (lane == 0 && q < qs.Q) pending = nwarps + atomicAdd(a.queue, 1);
+    return q;
+  };
+  int pw = 0, pr = 0;   // fifo push / pop counts (same in every lane)
+  auto push = [&](int q) {
+    if (lane == 0) fifo[warp][pw % kFifo] = q;
+    ++pw;
+  };
 
   // ---- producer side: the next group to copy
   Task it;
-  it.u = (long long)blockIdx.x * NW + warp;
-  task_load<NT>(it, a, UPE, U);
-  int ig = 0;        // group index within the producer's task
+  {
+    const int q = fetch();
+    push(q);
+    task_load<KG, NT>(it, smeta, qs, q);
+  }
+  int ig = 0;        // group index within the producer's pass
   int slot_w = 0;    // ring slot the producer fills next
   auto issue_next = [&]() {
-    if (it.u >= 0) {
+    if (it.q >= 0) {
+      const int K = it.down ? a.I : a.H;
+      const int NR = it.down ? a.H : 2 * a.I;
       int rlo, rhi;
-      if (kDown) { rlo = it.blk * 16 + g; rhi = rlo + 8; }
+      if (it.down) { rlo = it.blk * 16 + g; rhi = rlo + 8; }
       else { rlo = it.blk * 8 + g; rhi = a.I + it.blk * 8 + g; }
       const size_t Rlo = (size_t)it.e * NR + rlo, Rhi = (size_t)it.e * NR + rhi;
 #pragma unroll
       for (int i = 0; i < KG; ++i) {
         const int kb = ig * KG + i;
         uint4* d = ring + ((slot_w * KG + i) * 2) * 32 + lane;
-        if constexpr (kFp4) {
-          if (kb < nkb) {
-            const uint8_t* cb = kDown ? a.dn_codes : a.gu_codes;
-            const uint8_t* sb = kDown ? a.dn_scales : a.gu_scales;
+        if (kb < it.nkb) {
+          if constexpr (kFp4) {
+            const uint8_t* cb = it.down ? a.dn_codes : a.gu_codes;
+            const uint8_t* sb = it.down ? a.dn_scales : a.gu_scales;
             const size_t kc = (size_t)kb * 64 + 16 * c;
             cp_async16(d, cb + Rlo * (K / 2) + kc);
             cp_async16(d + 32, cb + Rhi * (K / 2) + kc);
             uint2* ds = sring + ((slot_w * KG + i) * 2) * 32 + lane;
             cp_async8(ds, sb + Rlo * (K / 16) + (size_t)kb * 8);
             cp_async8(ds + 32, sb + Rhi * (K / 16) + (size_t)kb * 8);
+          } else {
+            const uint16_t* wb = it.down ? a.w_down : a.w_gate_up;
+            const size_t kc = (size_t)kb * 32 + 8 * c;
+            cp_async16(d, wb + Rlo * K + kc);
+            cp_async16(d + 32, wb + Rhi * K + kc);
           }
-        } else {
-          const uint16_t* wb = kDown ? a.w_down : a.w_gate_up;
-          const size_t kc = (size_t)kb * 32 + 8 * c;
-          cp_async16(d, wb + Rlo * K + kc);
-          cp_async16(d + 32, wb + Rhi * K + kc);
         }
       }
-      if (++ig == ngroups) { ig = 0; task_next<NT>(it, a, UPE, U, stride); }
+      if (++ig == it.ngroups) {
+        ig = 0;
+        if (++it.pass >= it.npass) {
+          const int q = fetch();
+          push(q);
+          task_load<KG, NT>(it, smeta, qs, q);
+        }
+      }
     }
     cp_async_commit();
     slot_w = slot_w + 1 == NS ? 0 : slot_w + 1;
@@ -234,14 +316,28 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
 #pragma unroll 1
   for (int s = 0; s < NS - 1; ++s) issue_next();
 
-  if (kDown) { pdl_wait(); pdl_trigger(); }   // h is complete; the combine may launch
-
   // ---- consumer side
   Task ct;
-  ct.u = (long long)blockIdx.x * NW + warp;
-  task_load<NT>(ct, a, UPE, U);
+  auto pop = [&]() {
+    __syncwarp();   // lane 0's fifo store is visible to the warp
+    const int q = fifo[warp][pr % kFifo];
+    ++pr;
+    task_load<KG, NT>(ct, smeta, qs, q);
+  };
+  pop();
   int slot_r = 0;
-  while (ct.u >= 0) {
+  while (ct.q >= 0) {
+    if (ct.down && ct.pass == 0) {
+      // h of this expert is complete once every gate/up unit of it published
+      if (lane == 0) {
+        int n = 0;
+        while (ld_acquire(a.dep + ct.slot) < qs.UPEg) {
+          if (++n > kSpinLimit) { atomicOr(a.status, kStatusTimeout); break; }
+          __nanosleep(128);
+        }
+      }
+      __syncwarp();
+    }
     const int p0 = ct.pass * 8 * NT;
     const uint16_t* bsrc[NT];
 #pragma unroll
@@ -249,29 +345,46 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
       const int n = p0 + nt * 8 + g;
       bsrc[nt] = nullptr;
       if (n < ct.m) {
-        if (kDown) bsrc[nt] = a.h + (size_t)(ct.off + n) * a.I;
-        else bsrc[nt] = a.x + (size_t)(a.perm[ct.off + n] / a.k) * a.H;
+        if (ct.down) bsrc[nt] = a.h + (size_t)(ct.off + n) * a.I;
+        else bsrc[nt] = a.x + (size_t)(permp[ct.off + n] / a.k) * a.H;
       }
     }
+    // down: the epilogue's slots and routing weights, fetched now
+    int ef[NT][2];
+    float ew[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int n = p0 + nt * 8 + 2 * c + h2;
+        ef[nt][h2] = 0;
+        ew[nt][h2] = 0.f;
+        if (ct.down && n < ct.m) {
+          ef[nt][h2] = permp[ct.off + n];
+          ew[nt][h2] = a.topk_w[ef[nt][h2]];
+        }
+      }
     const int ntiles = min(NT, (ct.m - p0 + 7) / 8);
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     uint32_t bc[NT][KG][C::kBRegs], bn[NT][KG][C::kBRegs];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) load_b<kFp4, KG>(bc[nt], nt < ntiles ? bsrc[nt] : nullptr, 0, nkb, c);
+    for (int nt = 0; nt < NT; ++nt)
+      load_b<kFp4, KG>(bc[nt], nt < ntiles ? bsrc[nt] : nullptr, 0, ct.nkb, c, ct.down);
 
 #pragma unroll 1
-    for (int gi = 0; gi < ngroups; ++gi) {
-      if (gi + 1 < ngroups) {
+    for (int gi = 0; gi < ct.ngroups; ++gi) {
+      if (gi + 1 < ct.ngroups) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) load_b<kFp4, KG>(bn[nt], nt < ntiles ? bsrc[nt] : nullptr, gi + 1, nkb, c);
+        for (int nt = 0; nt < NT; ++nt)
+          load_b<kFp4, KG>(bn[nt], nt < ntiles ? bsrc[nt] : nullptr, gi + 1, ct.nkb, c, ct.down);
       }
       cp_async_wait<NS - 2>();
 #pragma unroll
       for (int i = 0; i < KG; ++i) {
         const int kb = gi * KG + i;
-        if (kFp4 && kb >= nkb) continue;
+        if (kb >= ct.nkb) continue;
         const uint4 alo = ring[((slot_r * KG + i) * 2) * 32 + lane];
         const uint4 ahi = ring[((slot_r * KG + i) * 2 + 1) * 32 + lane];
         if constexpr (kFp4) {
@@ -326,7 +439,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
     // epilogue straight from the fragments: c0,c1 = row g, tokens 2c,2c+1;
     // c2,c3 = row g+8, same tokens
     float gscale = 1.0f;
-    if constexpr (kFp4) gscale = kDown ? a.dn_global[ct.e] : a.gu_global[ct.e];
+    if constexpr (kFp4) gscale = ct.down ? a.dn_global[ct.e] : a.gu_global[ct.e];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       if (nt >= ntiles) continue;
@@ -334,12 +447,12 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
       for (int h2 = 0; h2 < 2; ++h2) {
         const int n = p0 + nt * 8 + 2 * c + h2;
         if (n < ct.m) {
-          if (!kDown) {
+          if (!ct.down) {
             const float gv = acc[nt][h2] * gscale, uv = acc[nt][2 + h2] * gscale;
             a.h[(size_t)(ct.off + n) * a.I + ct.blk * 8 + g] = f2bf(silu(gv) * uv);
           } else {
-            const int f = a.perm[ct.off + n];
-            const float wt = a.topk_w[f];
+            const int f = ef[nt][h2];
+            const float wt = ew[nt][h2];
             const float y0 = wt * (acc[nt][h2] * gscale), y1 = wt * (acc[nt][2 + h2] * gscale);
             const size_t o = (size_t)f * a.H + ct.blk * 16 + g;
             if (a.partial_f32) {
@@ -353,24 +466,30 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
         }
       }
     }
-    task_next<NT>(ct, a, UPE, U, stride);
+    if (++ct.pass < ct.npass) continue;
+    if (!ct.down) {
+      // publish this unit's h rows to the down units of the expert
+      __syncwarp();
+      if (lane == 0) red_release_add(a.dep + ct.slot, 1);
+    }
+    pop();
   }
   cp_async_wait<0>();
 }
 
-template <bool kDown, bool kFp4, int NT>
+template <bool kFp4, int NT>
 cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   using C = StreamCfg<kFp4, NT>;
   const long long S = (long long)a.T * a.k;
   const long long max_active = S < a.E ? S : a.E;
-  const long long UPE = kDown ? a.H / 16 : a.I / 8;
-  const long long units = max_active * UPE;
+  const long long units = max_active * (a.I / 8 + a.H / 16);
   long long grid = a.num_sms;
   const long long need = (units + C::kWarps - 1) / C::kWarps;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  const int smem = C::kWarpBytes * C::kWarps + C::kLutBytes;
-  cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<kDown, kFp4, NT>,
+  const int smem = C::kWarpBytes * C::kWarps + C::kLutBytes + 16 * a.E +
+                   (S <= kPermSmem ? 4 * (int)S : 0);
+  cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<kFp4, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -380,30 +499,22 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = kDown ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<kDown, kFp4, NT>, a);
+  return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<kFp4, NT>, a);
 }
 
-template <bool kDown>
-cudaError_t launch_stream(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
+}  // namespace
+
+cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
   // a group never holds more rows than the batch has tokens: one 8-row tile
   // per pass for T <= 8, two above
   const bool two = a.T > 8;
   if (a.gu_codes != nullptr)
-    return two ? launch_variant<kDown, true, 2>(a, stream) : launch_variant<kDown, true, 1>(a, stream);
-  return two ? launch_variant<kDown, false, 2>(a, stream) : launch_variant<kDown, false, 1>(a, stream);
-}
-
-}  // namespace
-
-cudaError_t launch_stream_gate_up(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
-  return launch_stream<false>(a, stream, launches);
-}
-cudaError_t launch_stream_down(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
-  return launch_stream<true>(a, stream, launches);
+    return two ? launch_variant<true, 2>(a, stream) : launch_variant<true, 1>(a, stream);
+  return two ? launch_variant<false, 2>(a, stream) : launch_variant<false, 1>(a, stream);
 }
 
 }  // namespace moe

@@ -147,8 +147,11 @@ int moe_forward(const uint16_t *x, const uint16_t *gate_w, const float *bias,
  * moe_forward with timing hooks, for benchmarks and profilers: identical
  * arguments and results, and additionally records events[i] (cudaEvent_t,
  * created by the caller) on `stream` at the stage boundaries
- *   [0] start  [1] after routing  [2] after grouping  [3] after gate/up+SwiGLU
- *   [4] after down projection  [5] after combine
+ *   [0] start  [1] after routing  [2] after grouping
+ *   [3] after the weight-streaming expert kernel (gate/up, SwiGLU and down of
+ *       the experts with few rows, one launch)
+ *   [4] after the tensor-core expert kernels (gate/up+SwiGLU, then down, of
+ *       the experts with many rows; none for small batches)  [5] after combine
  * and stores in *kernels_launched (HOST pointer, may be NULL) the number of
  * kernels this call launched.  `events` is a HOST array of 6 non-null events.
  */
