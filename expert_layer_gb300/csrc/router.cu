@@ -33,23 +33,71 @@ __host__ __device__ inline float gamma_bound(int n) {
   return (float)(n * u / (1.0 - n * u));
 }
 
-// Exact-product fp64 dot of two bf16 rows of length H (H % 8 == 0), whole warp.
-// Every lane returns the same value (xor butterfly).
-// Four independent fp64 chains per lane keep the (slow) fp64 pipe busy.
+// fp64 value of a finite nonzero-exponent fp32 number, or of a signed zero,
+// assembled with integer operations (exact: fp64 holds every fp32 value).
+__device__ __forceinline__ double f32_as_f64(uint32_t u) {
+  const uint32_t e = (u >> 23) & 0xffu;
+  const uint32_t hi = e ? (u & 0x80000000u) | ((e + 896u) << 20) | ((u >> 3) & 0xfffffu)
+                        : (u & 0x80000000u);
+  return __hiloint2double((int)hi, e ? (int)(u << 29) : 0);
+}
+
+// fp64 dot of two bf16 rows of length H (H % 8 == 0), whole warp; every lane
+// returns the same value (xor butterfly).  A bf16 x bf16 product has at most
+// 16 significant bits, so its fp32 value is exact unless it under- or
+// overflows fp32; then each exact product is added in fp64.  That is the
+// same arithmetic as an fp64 fma of the two factors, with one operation on
+// the (slow) fp64 pipe per element instead of three.  A batch of 8 elements
+// in which any lane meets an fp32 product that is not exact goes the fp64 way
+// for the whole warp.  Four independent chains per lane.
 __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
                                int H) {
   const int lane = threadIdx.x & 31;
   double s[4] = {0.0, 0.0, 0.0, 0.0};
-  for (int h = lane * 8; h < H; h += 256) {
-    uint4 va = *reinterpret_cast<const uint4*>(a + h);
-    uint4 vb = *reinterpret_cast<const uint4*>(b + h);
+  constexpr int kB = 4;   // iterations whose loads are issued together
+  for (int hb = 0; hb < H; hb += 256 * kB) {
+   uint4 va4[kB], vb4[kB];
+#pragma unroll
+   for (int it = 0; it < kB; ++it) {
+     const int h = hb + lane * 8 + 256 * it;
+     va4[it] = h < H ? *reinterpret_cast<const uint4*>(a + h) : make_uint4(0, 0, 0, 0);
+     vb4[it] = h < H ? *reinterpret_cast<const uint4*>(b + h) : make_uint4(0, 0, 0, 0);
+   }
+#pragma unroll
+   for (int it = 0; it < kB; ++it) {
+    const uint4 va = va4[it], vb = vb4[it];
     const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+    uint32_t pu[8];
+    bool inexact = false;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      s[i] = fma((double)bf16lo(wa[i]), (double)bf16lo(wb[i]), s[i]);
-      s[i] = fma((double)bf16hi(wa[i]), (double)bf16hi(wb[i]), s[i]);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float fa = j ? bf16hi(wa[i]) : bf16lo(wa[i]);
+        const float fb = j ? bf16hi(wb[i]) : bf16lo(wb[i]);
+        const uint32_t u = __float_as_uint(__fmul_rn(fa, fb));
+        const uint32_t e = (u >> 23) & 0xffu;
+        // exponent 255: overflow (or inf / nan); exponent 0 with two nonzero
+        // factors: underflow
+        inexact |= e == 0xffu || (e == 0 && fa != 0.0f && fb != 0.0f);
+        pu[2 * i + j] = u;
+      }
     }
+    if (__any_sync(0xffffffffu, inexact)) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s[i] = fma((double)bf16lo(wa[i]), (double)bf16lo(wb[i]), s[i]);
+        s[i] = fma((double)bf16hi(wa[i]), (double)bf16hi(wb[i]), s[i]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s[i] += f32_as_f64(pu[2 * i]);
+        s[i] += f32_as_f64(pu[2 * i + 1]);
+      }
+    }
+   }
   }
   double r = (s[0] + s[1]) + (s[2] + s[3]);
 #pragma unroll
@@ -63,6 +111,9 @@ struct WarpScratch {
   double key[kCandCap];
   float ex[32];
   double kmax;
+  int dpos[kCandCap];   // candidate positions that need an fp64 logit
+  int nd;               // fp64 logits this token needs (0: selection done)
+  int end;              // last rank of the certain set, -1: every expert in fp64
 };
 
 // Two logits whose fp32 values differ by more than this are ordered like the
@@ -152,36 +203,113 @@ __device__ int extract_small(const float* L, int E, int k, float thr, WarpScratc
   return extract_regs(v, E, k, thr, sc);
 }
 
-// The uncertain cases of select_token, kept out of line so that the common
-// certain case stays short: candidates that sit within rounding of a
-// neighbour get fp64 logits and the certain set is re-ranked (bal0/bal1 flag
-// them, candidate positions lane and lane + 32), or, when end < 0, every
-// expert gets an fp64 logit.  Whole warp; writes idx_out[0..k) and the
-// unnormalised weights sc.ex[0..k).
-__device__ __noinline__ void select_fp64(int E, int k, int end, unsigned bal0, unsigned bal1,
-                                         const uint16_t* xrow, const uint16_t* gate_w,
-                                         const float* bias, int H, double* l64_row,
-                                         WarpScratch& sc, int32_t* idx_out, WsHeader* hdr) {
+// Selection of one token from its sorted candidates cand[0..end] (the
+// certain set), in three phases so that the rare fp64 work can be shared by
+// every warp of the CTA:
+//   select_begin  (one warp per token) certain order -> writes the top-k and
+//                 the weights and sets nd = 0; else lists in dpos[0..nd) the
+//                 candidates that sit within rounding of a neighbour (or, when
+//                 end < 0, asks for all E experts) and sets nd
+//   select_dots   (all warps of the CTA) the listed fp64 logits
+//   select_end    (one warp per token with nd > 0) ranks by the fp64 keys
+// Weights: softmax over all E renormalised over the k selected, i.e.
+// exp(l_s - l_max) over the selected set divided by its sum.
+
+// Renormalised weights from the unnormalised ones in lanes < k (fixed xor-tree
+// sum, the same on every lane).
+__device__ __forceinline__ void write_weights(float ex, int k, float* w_out) {
   const int lane = threadIdx.x & 31;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) w_out[lane] = ex / sum;
+}
+
+__device__ void select_begin(int E, int k, float delta, int end, WarpScratch& sc, int32_t* idx_out,
+                             float* w_out, WsHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  const float thr = cert_threshold(delta);
+  __syncwarp();
+  if (end < 0) {
+    // every expert in fp64 (needs >= 64 experts within rounding of each other)
+    if (lane == 0) {
+      atomicAdd(&hdr->router_flagged, 1);
+      atomicAdd(&hdr->router_fallback, 1);
+      sc.nd = E;
+      sc.end = -1;
+    }
+    __syncwarp();
+    return;
+  }
+  // ambiguous candidates: members of an adjacent pair closer than 2*delta
+  bool amb[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = lane + 32 * r;
+    bool a = false;
+    if (i <= end) {
+      if (i > 0 && !(sc.cand_v[i - 1] - sc.cand_v[i] > thr)) a = true;
+      if (i < end && !(sc.cand_v[i] - sc.cand_v[i + 1] > thr)) a = true;
+    }
+    amb[r] = a;
+  }
+  const unsigned bal0 = __ballot_sync(0xffffffffu, amb[0]);
+  const unsigned bal1 = __ballot_sync(0xffffffffu, amb[1]);
+  if ((bal0 | bal1) == 0) {
+    // the fp32 order is certain: ranks are the candidate positions
+    float ex = 0.f;
+    if (lane < k) {
+      idx_out[lane] = sc.cand_e[lane];
+      ex = expf(sc.cand_v[lane] - sc.cand_v[0]);
+    }
+    write_weights(ex, k, w_out);
+    if (lane == 0) sc.nd = 0;
+    __syncwarp();
+    return;
+  }
+  if (lane == 0) atomicAdd(&hdr->router_flagged, 1);
+  const unsigned lt = (1u << lane) - 1u;
+  const int n0 = __popc(bal0);
+  if (amb[0]) sc.dpos[__popc(bal0 & lt)] = lane;
+  if (amb[1]) sc.dpos[n0 + __popc(bal1 & lt)] = lane + 32;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = lane + 32 * r;
+    if (i <= end) sc.key[i] = (double)sc.cand_v[i];
+  }
+  if (lane == 0) {
+    sc.nd = n0 + __popc(bal1);
+    sc.end = end;
+  }
+  __syncwarp();
+}
+
+// fp64 logits listed by select_begin for the tokens t0 .. t0+nt-1 (scratch
+// scr[0..nt)), one warp per logit, spread over all warps of the block.
+__device__ void select_dots(WarpScratch* scr, int nt, int t0, const uint16_t* x,
+                            const uint16_t* gate_w, const float* bias, int H, int E, double* l64) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  int total = 0;
+  for (int tt = 0; tt < nt; ++tt) total += scr[tt].nd;
+  for (int j = warp; j < total; j += nw) {
+    int tt = 0, r = j;
+    while (r >= scr[tt].nd) { r -= scr[tt].nd; ++tt; }
+    WarpScratch& sc = scr[tt];
+    const int e = sc.end < 0 ? r : sc.cand_e[sc.dpos[r]];
+    double d = warp_dot_f64(x + (size_t)(t0 + tt) * H, gate_w + (size_t)e * H, H);
+    if (bias) d += (double)bias[e];
+    if (lane == 0) {
+      if (sc.end < 0) l64[(size_t)(t0 + tt) * E + e] = d;
+      else sc.key[sc.dpos[r]] = d;
+    }
+  }
+}
+
+__device__ void select_end(int E, int k, WarpScratch& sc, const double* l64_row, int32_t* idx_out,
+                           float* w_out) {
+  const int lane = threadIdx.x & 31;
+  const int end = sc.end;
   if (end >= 0) {
-    if (lane == 0) atomicAdd(&hdr->router_flagged, 1);
-    for (int r = 0; r < 2; ++r) {
-      const int i = lane + 32 * r;
-      if (i <= end) sc.key[i] = (double)sc.cand_v[i];
-    }
-    __syncwarp();
-    for (int r = 0; r < 2; ++r) {
-      unsigned bal = r == 0 ? bal0 : bal1;
-      while (bal) {
-        const int i = __ffs(bal) - 1 + 32 * r;
-        bal &= bal - 1;
-        const int e = sc.cand_e[i];
-        double d = warp_dot_f64(xrow, gate_w + (size_t)e * H, H);
-        if (bias) d += (double)bias[e];
-        if (lane == 0) sc.key[i] = d;
-      }
-    }
-    __syncwarp();
     // rank of each candidate by (key desc, index asc)
     int rank[2] = {INT_MAX, INT_MAX};
     for (int r = 0; r < 2; ++r) {
@@ -205,87 +333,34 @@ __device__ __noinline__ void select_fp64(int E, int k, int end, unsigned bal0, u
       const int i = lane + 32 * r;
       if (rank[r] < k) sc.ex[rank[r]] = expf((float)(sc.key[i] - kmax));
     }
-    return;
-  }
-  // Every expert in fp64 (needs >= 64 experts within rounding of each other).
-  const int per_lane = (E + 31) >> 5;
-  if (lane == 0) { atomicAdd(&hdr->router_flagged, 1); atomicAdd(&hdr->router_fallback, 1); }
-  for (int e = 0; e < E; ++e) {
-    double d = warp_dot_f64(xrow, gate_w + (size_t)e * H, H);
-    if (bias) d += (double)bias[e];
-    if (lane == 0) l64_row[e] = d;
-  }
-  __syncwarp();
-  __threadfence_block();
-  uint32_t taken = 0;
-  double kmax = 0.0;
-  for (int s = 0; s < k; ++s) {
-    double bv = 0.0;
-    int be = INT_MAX;
-    for (int i = 0; i < per_lane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        const double v = l64_row[e];
-        if (be == INT_MAX || v > bv || (v == bv && e < be)) { bv = v; be = e; }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) { bv = ov; be = oe; }
-    }
-    if (be == INT_MAX) be = 0;  // unreachable for k <= E
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (s == 0) kmax = bv;
-    if (lane == 0) { idx_out[s] = be; sc.ex[s] = expf((float)(bv - kmax)); }
-  }
-}
-
-// Certified top-k of one token from its sorted candidates cand[0..end] (the
-// certain set) -- or, when end < 0, from fp64 logits of every expert.  Whole
-// warp.  Writes idx_out[0..k) and w_out[0..k).
-__device__ void select_token(int E, int k, float delta, int end, const uint16_t* xrow,
-                             const uint16_t* gate_w, const float* bias, int H, double* l64_row,
-                             WarpScratch& sc, int32_t* idx_out, float* w_out, WsHeader* hdr) {
-  const int lane = threadIdx.x & 31;
-  const float thr = cert_threshold(delta);
-  __syncwarp();
-  unsigned bal0 = 0, bal1 = 0;
-  bool certain = false;
-  if (end >= 0) {
-    // Ambiguous candidates: members of an adjacent pair closer than 2*delta.
-    bool amb0 = false, amb1 = false;
-    for (int r = 0; r < 2; ++r) {
-      const int i = lane + 32 * r;
-      bool a = false;
-      if (i <= end) {
-        if (i > 0 && !(sc.cand_v[i - 1] - sc.cand_v[i] > thr)) a = true;
-        if (i < end && !(sc.cand_v[i] - sc.cand_v[i + 1] > thr)) a = true;
-      }
-      if (r == 0) amb0 = a; else amb1 = a;
-    }
-    bal0 = __ballot_sync(0xffffffffu, amb0);
-    bal1 = __ballot_sync(0xffffffffu, amb1);
-    certain = (bal0 | bal1) == 0;
-  }
-  float ex = 0.f;
-  if (certain) {
-    // the fp32 order is certain: ranks are the candidate positions
-    if (lane < k) {
-      idx_out[lane] = sc.cand_e[lane];
-      ex = expf(sc.cand_v[lane] - sc.cand_v[0]);
-    }
   } else {
-    select_fp64(E, k, end, bal0, bal1, xrow, gate_w, bias, H, l64_row, sc, idx_out, hdr);
-    __syncwarp();
-    if (lane < k) ex = sc.ex[lane];
-  }
-  // renormalise over the k selected (fixed xor-tree order, same on every lane)
-  float sum = ex;
+    const int per_lane = (E + 31) >> 5;
+    uint32_t taken = 0;
+    double kmax = 0.0;
+    for (int s = 0; s < k; ++s) {
+      double bv = 0.0;
+      int be = INT_MAX;
+      for (int i = 0; i < per_lane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u)) {
+          const double v = l64_row[e];
+          if (be == INT_MAX || v > bv || (v == bv && e < be)) { bv = v; be = e; }
+        }
+      }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < k) w_out[lane] = ex / sum;
+      for (int o = 16; o > 0; o >>= 1) {
+        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) { bv = ov; be = oe; }
+      }
+      if (be == INT_MAX) be = 0;  // unreachable for k <= E
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (s == 0) kmax = bv;
+      if (lane == 0) { idx_out[s] = be; sc.ex[s] = expf((float)(bv - kmax)); }
+    }
+  }
+  __syncwarp();
+  write_weights(lane < k ? sc.ex[lane] : 0.f, k, w_out);
   __syncwarp();
 }
 
@@ -308,7 +383,8 @@ __host__ __device__ inline size_t router_small_group_ints(int E, int S, bool gro
   return group ? grouping::single_block_smem_ints(E, S) : 0;
 }
 __host__ __device__ inline size_t router_small_smem(int E, int S, int tt, bool group) {
-  return sizeof(int) * router_small_group_ints(E, S, group) + sizeof(float) * ((size_t)(tt + 1) * E + tt);
+  return sizeof(int) * router_small_group_ints(E, S, group) + sizeof(uint64_t) * (size_t)tt * E +
+         sizeof(float) * ((size_t)(tt + 1) * E + tt);
 }
 
 // Release-acquire integer add at GPU scope: the caller's earlier writes (and
@@ -359,24 +435,33 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
           sq = fmaf(bf16hi(ww[i]), bf16hi(ww[i]), sq);
         }
       }
+      // token rows two at a time, all loads of a pair issued before its
+      // products (rows past the chunk read as zero and are never stored)
+      constexpr int kPair = kTT < 2 ? kTT : 2;
 #pragma unroll
-      for (int tt = 0; tt < kTT; ++tt) {
-        if (tt >= nt) break;
-        const uint16_t* xr = x + (size_t)(t0 + tt) * H;
-        uint4 xv[8];
+      for (int tp = 0; tp < kTT; tp += kPair) {
+        uint4 xv[kPair][8];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const int h = hb + lane * 8 + 256 * v;
-          xv[v] = h < H ? *reinterpret_cast<const uint4*>(xr + h) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kPair; ++u) {
+          const uint16_t* xr = x + (size_t)(t0 + tp + u) * H;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const int h = hb + lane * 8 + 256 * v;
+            xv[u][v] = (tp + u < nt && h < H) ? *reinterpret_cast<const uint4*>(xr + h)
+                                              : make_uint4(0, 0, 0, 0);
+          }
         }
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint32_t xw[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
-          const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
+        for (int u = 0; u < kPair; ++u) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[tt] = fmaf(bf16lo(xw[i]), bf16lo(ww[i]), acc[tt]);
-            acc[tt] = fmaf(bf16hi(xw[i]), bf16hi(ww[i]), acc[tt]);
+          for (int v = 0; v < 8; ++v) {
+            const uint32_t xw[4] = {xv[u][v].x, xv[u][v].y, xv[u][v].z, xv[u][v].w};
+            const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[tp + u] = fmaf(bf16lo(xw[i]), bf16lo(ww[i]), acc[tp + u]);
+              acc[tp + u] = fmaf(bf16hi(xw[i]), bf16hi(ww[i]), acc[tp + u]);
+            }
           }
         }
       }
@@ -393,24 +478,30 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = bias ? mine + bias[e] : mine;
     if (lane == 31) wnorm[e] = sqrtf(sq);   // the same value from every chunk's CTA
   }
-  if (blockIdx.y == 0 && warp == 0) {
-    // ||x_t|| of the chunk's tokens (rows just read, mostly cache hits)
-    for (int tt = 0; tt < nt; ++tt) {
-      const uint16_t* xr = x + (size_t)(t0 + tt) * H;
-      float sqx = 0.f;
-      for (int h = lane * 8; h < H; h += 256) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(xr + h);
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+  if (blockIdx.y == 0 && warp < nt) {
+    // ||x_t|| of token t0 + warp (a row just read, mostly cache hits)
+    const uint16_t* xr = x + (size_t)(t0 + warp) * H;
+    float sqx = 0.f;
+    for (int hb = 0; hb < H; hb += 2048) {
+      uint4 xv[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int h = hb + lane * 8 + 256 * v;
+        xv[v] = h < H ? *reinterpret_cast<const uint4*>(xr + h) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint32_t xw[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           sqx = fmaf(bf16lo(xw[i]), bf16lo(xw[i]), sqx);
           sqx = fmaf(bf16hi(xw[i]), bf16hi(xw[i]), sqx);
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
-      if (lane == 0) xnorm[t0 + tt] = sqrtf(sqx);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
+    if (lane == 0) xnorm[t0 + warp] = sqrtf(sqx);
   }
   // Publish the CTA's results and count the CTA in; the last CTA of the
   // chunk sees every other CTA's results.
@@ -420,37 +511,42 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
   if (!s_last) return;
 
   // ---- last CTA of the chunk: stage logits, ||w_e||, ||x_t|| (one L2 trip)
-  float* sl = reinterpret_cast<float*>(dsm + router_small_group_ints(E, T * k, kGroup));
+  // (the grouping scratch is an even number of ints: the keys are 8-byte aligned)
+  uint64_t* skey = reinterpret_cast<uint64_t*>(dsm + router_small_group_ints(E, T * k, kGroup));
+  float* sl = reinterpret_cast<float*>(skey + (size_t)kTT * E);
   float* swn = sl + (size_t)kTT * E;
   float* sxn = swn + E;
-  for (int i = threadIdx.x; i < nt * E; i += blockDim.x) sl[i] = __ldcg(logits + (size_t)t0 * E + i);
+  // sort keys: order-preserving bits of the logit (NaN lowest, -0 = +0) above
+  // the inverted expert index, so a larger key is a better (logit, index)
+  for (int i = threadIdx.x; i < nt * E; i += blockDim.x) {
+    const float v = __ldcg(logits + (size_t)t0 * E + i);
+    sl[i] = v;
+    const uint32_t e = (uint32_t)(i % E);
+    skey[i] = ((uint64_t)order_bits(rank_key(v)) << 32) | (uint64_t)(0xffffffffu - e);
+  }
   for (int i = threadIdx.x; i < E; i += blockDim.x) swn[i] = __ldcg(wnorm + i);
   if (threadIdx.x < nt) sxn[threadIdx.x] = __ldcg(xnorm + t0 + threadIdx.x);
   __syncthreads();
   // Rank of every (token, expert) by counting the experts ahead of it:
   // larger logit first, lower index first on equal logits, NaN last.  Four
   // threads share an expert, thread q counting over j = q (mod 4).
-  const int nitems = nt * E * 4;
-  for (int base = 0; base < nitems; base += blockDim.x) {
-    const int it = base + threadIdx.x;
-    int r = 0, ee = 0, tt = 0;
-    float v = 0.f;
-    if (it < nitems) {
-      const int q = it & 3, pe = it >> 2;
-      tt = pe / E;
-      ee = pe - tt * E;
-      const float* row = sl + (size_t)tt * E;
-      v = rank_key(row[ee]);
-      for (int j = q; j < E; j += 4) {
-        const float o = rank_key(row[j]);
-        r += (o > v || (o == v && j < ee)) ? 1 : 0;
+  for (int tt = 0; tt < nt; ++tt) {
+    const uint64_t* krow = skey + (size_t)tt * E;
+    for (int base = 0; base < 4 * E; base += blockDim.x) {   // uniform trip count
+      const int it = base + threadIdx.x;
+      const int q = it & 3, ee = it >> 2;
+      int r = 0;
+      if (ee < E) {
+        const uint64_t key = krow[ee];
+#pragma unroll 8
+        for (int j = q; j < E; j += 4) r += krow[j] > key ? 1 : 0;
       }
-    }
-    r += __shfl_xor_sync(0xffffffffu, r, 1);
-    r += __shfl_xor_sync(0xffffffffu, r, 2);
-    if (it < nitems && (it & 3) == 0 && r < kCandCap) {
-      scr[tt].cand_e[r] = ee;
-      scr[tt].cand_v[r] = v;
+      r += __shfl_xor_sync(0xffffffffu, r, 1);
+      r += __shfl_xor_sync(0xffffffffu, r, 2);
+      if (ee < E && q == 0 && r < kCandCap) {
+        scr[tt].cand_e[r] = ee;
+        scr[tt].cand_v[r] = rank_key(sl[(size_t)tt * E + ee]);
+      }
     }
   }
   __syncthreads();
@@ -472,8 +568,17 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     const float delta = gamma_bound(gamma_terms) * sxn[warp] * wmax * (1.0f + 0x1p-10f) +
                         0x1p-22f * lmax + (float)H * 0x1p-149f;
     const int end = certain_end_ranked(sc, E, k, cert_threshold(delta));
-    select_token(E, k, delta, end, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, sc,
-                 idx + (size_t)t * k, w + (size_t)t * k, hdr);
+    select_begin(E, k, delta, end, sc, idx + (size_t)t * k, w + (size_t)t * k, hdr);
+  }
+  __syncthreads();
+  int ndots = 0;
+  for (int tt = 0; tt < nt; ++tt) ndots += scr[tt].nd;
+  if (ndots > 0) {   // uniform over the block
+    select_dots(scr, nt, t0, x, gw, bias, H, E, l64);
+    __syncthreads();
+    if (warp < nt && scr[warp].nd > 0)
+      select_end(E, k, scr[warp], l64 + (size_t)(t0 + warp) * E, idx + (size_t)(t0 + warp) * k,
+                 w + (size_t)(t0 + warp) * k);
   }
   if constexpr (kGroup) {
     __syncthreads();   // the selecting warps' idx / w writes, then one release
@@ -639,26 +744,37 @@ __global__ void __launch_bounds__(256) router_select_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem_raw);
   float* sl = reinterpret_cast<float*>(smem_raw + sizeof(WarpScratch) * 8) + (size_t)warp * E;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  float wmax = 0.f, lmax = 0.f;
-  for (int e = lane; e < E; e += 32) {
-    const float v = logits[(size_t)t * E + e];
-    sl[e] = v;
-    wmax = fmaxf(wmax, wnorm[e]);
-    lmax = fmaxf(lmax, fabsf(v));
-  }
+  const int t0 = blockIdx.x * 8;
+  const int nt = min(8, T - t0);
+  const int t = t0 + warp;
+  if (warp < nt) {
+    float wmax = 0.f, lmax = 0.f;
+    for (int e = lane; e < E; e += 32) {
+      const float v = logits[(size_t)t * E + e];
+      sl[e] = v;
+      wmax = fmaxf(wmax, wnorm[e]);
+      lmax = fmaxf(lmax, fabsf(v));
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    for (int o = 16; o > 0; o >>= 1) {
+      wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+      lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    }
+    __syncwarp();
+    const float delta = gamma_bound(gamma_terms) * xnorm[t] * wmax * (1.0f + 0x1p-10f) +
+                        0x1p-22f * lmax + (float)H * 0x1p-149f;
+    const int end = extract_small(sl, E, k, cert_threshold(delta), scr[warp]);   // E <= 128 here
+    select_begin(E, k, delta, end, scr[warp], idx + (size_t)t * k, w + (size_t)t * k,
+                 reinterpret_cast<WsHeader*>(ws));
   }
-  __syncwarp();
-  const float delta = gamma_bound(gamma_terms) * xnorm[t] * wmax * (1.0f + 0x1p-10f) +
-                      0x1p-22f * lmax + (float)H * 0x1p-149f;
-  const int end = extract_small(sl, E, k, cert_threshold(delta), scr[warp]);   // E <= 128 here
-  select_token(E, k, delta, end, x + (size_t)t * H, gw, bias, H, l64 + (size_t)t * E, scr[warp],
-               idx + (size_t)t * k, w + (size_t)t * k, reinterpret_cast<WsHeader*>(ws));
+  __syncthreads();
+  int ndots = 0;
+  for (int tt = 0; tt < nt; ++tt) ndots += scr[tt].nd;
+  if (ndots == 0) return;   // uniform over the block
+  select_dots(scr, nt, t0, x, gw, bias, H, E, l64);
+  __syncthreads();
+  if (warp < nt && scr[warp].nd > 0)
+    select_end(E, k, scr[warp], l64 + (size_t)t * E, idx + (size_t)t * k, w + (size_t)t * k);
 }
 
 // ||w_e|| for every expert, one warp per expert.
