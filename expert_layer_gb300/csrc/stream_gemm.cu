@@ -81,21 +81,27 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Pipeline shape per variant (NT = 8-row token tiles per pass).
+// Pipeline shape per variant (NT = 8-row token tiles per pass).  A unit is
+// FR fragments of 16 weight rows.  NVFP4 units are two or four fragments
+// tall: each token-row fragment a thread loads then feeds FR mma instead of
+// one, which matters because 4-bit weights make the token rows (bf16) the
+// larger stream whenever an expert holds more than a few rows.  With four
+// token tiles (32 rows per pass, for batches above 16 tokens) the unit is two
+// fragments tall, so that an expert of up to 32 rows decodes its weights once.
 template <bool kFp4, int NT = 1>
 struct StreamCfg {
   static constexpr int KB = kFp4 ? 128 : 32;      // K elements per block
-  static constexpr int KG = kFp4 ? (NT == 1 ? 2 : 1) : 4;   // blocks per pipelined group
-  static constexpr int NS = kFp4 ? 4 : 4;         // groups in the ring (NS-1 in flight)
-  static constexpr int kWarps = 12;
-  // per-warp ring: [NS][KG][2 rows][32 lanes] x 16 B of weights (codes), plus
-  // [NS][KG][2][32] x 8 B of scales for NVFP4
-  static constexpr int kWBytes = NS * KG * 2 * 32 * 16;
-  static constexpr int kSBytes = kFp4 ? NS * KG * 2 * 32 * 8 : 0;
+  static constexpr int KG = kFp4 ? 1 : 4;         // blocks per pipelined group
+  static constexpr int FR = kFp4 ? (NT >= 4 ? 2 : 4) : 1;   // 16-row fragments per unit
+  static constexpr int NS = kFp4 ? (NT >= 4 ? 5 : 3) : 4;   // groups in the ring (NS-1 in flight)
+  static constexpr int kWarps = kFp4 ? 8 : 12;
+  // per-warp ring: [NS][KG][FR][2 rows][32 lanes] x 16 B of weights (codes),
+  // plus [NS][KG][FR][2][32] x 8 B of scales for NVFP4
+  static constexpr int kWBytes = NS * KG * FR * 2 * 32 * 16;
+  static constexpr int kSBytes = kFp4 ? NS * KG * FR * 2 * 32 * 8 : 0;
   static constexpr int kWarpBytes = kWBytes + kSBytes;
   // NVFP4: the byte -> two-bf16 table replicated per lane (conflict-free lookups)
   static constexpr int kLutBytes = kFp4 ? 256 * 32 * 4 : 0;
-  static constexpr int kBRegs = kFp4 ? 16 : 4;    // 32-bit B registers per block
 };
 
 // Bounded waits: polls before a wait gives up (and the kernel records
@@ -148,32 +154,21 @@ __device__ __forceinline__ void task_load(Task& t, const int4* smeta, const Queu
   t.ngroups = (t.nkb + KG - 1) / KG;
 }
 
-// B (token rows) of one K group for this thread: row g of the pass.  Down
-// reads h, written earlier in the same launch, through L2 (ld.cg).
-template <bool kFp4, int KG>
-__device__ __forceinline__ void load_b(uint32_t (&b)[KG][StreamCfg<kFp4, 1>::kBRegs],
-                                       const uint16_t* bsrc, int gi, int nkb, int c, bool cg) {
+// B (token rows) of one K group for this thread (bf16 weights): row g of
+// the pass, k = 8c..8c+7 of each 32-wide block.  Down reads h, written
+// earlier in the same launch, through L2 (ld.cg).
+template <int KG>
+__device__ __forceinline__ void load_b(uint32_t (&b)[KG][4], const uint16_t* bsrc, int gi, int nkb,
+                                       int c, bool cg) {
 #pragma unroll
   for (int i = 0; i < KG; ++i) {
     const int kb = gi * KG + i;
-    if constexpr (kFp4) {
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint4 t = make_uint4(0, 0, 0, 0);
-        if (bsrc && kb < nkb) {
-          const uint4* p = reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 128 + 32 * c + 8 * v);
-          t = cg ? __ldcg(p) : *p;
-        }
-        b[i][4 * v + 0] = t.x; b[i][4 * v + 1] = t.y; b[i][4 * v + 2] = t.z; b[i][4 * v + 3] = t.w;
-      }
-    } else {
-      uint4 t = make_uint4(0, 0, 0, 0);
-      if (bsrc && kb < nkb) {
-        const uint4* p = reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 32 + 8 * c);
-        t = cg ? __ldcg(p) : *p;
-      }
-      b[i][0] = t.x; b[i][1] = t.y; b[i][2] = t.z; b[i][3] = t.w;
+    uint4 t = make_uint4(0, 0, 0, 0);
+    if (bsrc && kb < nkb) {
+      const uint4* p = reinterpret_cast<const uint4*>(bsrc + (size_t)kb * 32 + 8 * c);
+      t = cg ? __ldcg(p) : *p;
     }
+    b[i][0] = t.x; b[i][1] = t.y; b[i][2] = t.z; b[i][3] = t.w;
   }
 }
 
@@ -225,8 +220,9 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
   pdl_trigger();
   Queue qs;
   const int nsmall = *a.num_active - (a.num_large ? *a.num_large : 0);
-  qs.UPEg = a.I / 8;
-  qs.UPEd = a.H / 16;
+  constexpr int FR = C::FR;
+  qs.UPEg = a.I / (8 * FR);
+  qs.UPEd = a.H / (16 * FR);
   qs.Ug = nsmall * qs.UPEg;
   qs.Q = qs.Ug + nsmall * qs.UPEd;
   qs.nkb_g = a.H / KB;
@@ -274,14 +270,16 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
     if (it.q >= 0) {
       const int K = it.down ? a.I : a.H;
       const int NR = it.down ? a.H : 2 * a.I;
+#pragma unroll
+      for (int f = 0; f < FR; ++f) {
       int rlo, rhi;
-      if (it.down) { rlo = it.blk * 16 + g; rhi = rlo + 8; }
-      else { rlo = it.blk * 8 + g; rhi = a.I + it.blk * 8 + g; }
+      if (it.down) { rlo = (it.blk * FR + f) * 16 + g; rhi = rlo + 8; }
+      else { rlo = (it.blk * FR + f) * 8 + g; rhi = a.I + rlo; }
       const size_t Rlo = (size_t)it.e * NR + rlo, Rhi = (size_t)it.e * NR + rhi;
 #pragma unroll
       for (int i = 0; i < KG; ++i) {
         const int kb = ig * KG + i;
-        uint4* d = ring + ((slot_w * KG + i) * 2) * 32 + lane;
+        uint4* d = ring + (((slot_w * KG + i) * FR + f) * 2) * 32 + lane;
         if (kb < it.nkb) {
           if constexpr (kFp4) {
             const uint8_t* cb = it.down ? a.dn_codes : a.gu_codes;
@@ -289,7 +287,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
             const size_t kc = (size_t)kb * 64 + 16 * c;
             cp_async16(d, cb + Rlo * (K / 2) + kc);
             cp_async16(d + 32, cb + Rhi * (K / 2) + kc);
-            uint2* ds = sring + ((slot_w * KG + i) * 2) * 32 + lane;
+            uint2* ds = sring + (((slot_w * KG + i) * FR + f) * 2) * 32 + lane;
             cp_async8(ds, sb + Rlo * (K / 16) + (size_t)kb * 8);
             cp_async8(ds + 32, sb + Rhi * (K / 16) + (size_t)kb * 8);
           } else {
@@ -299,6 +297,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
             cp_async16(d + 32, wb + Rhi * K + kc);
           }
         }
+      }
       }
       if (++ig == it.ngroups) {
         ig = 0;
@@ -365,81 +364,149 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
         }
       }
     const int ntiles = min(NT, (ct.m - p0 + 7) / 8);
-    float acc[NT][4];
+    float acc[FR][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    uint32_t bc[NT][KG][C::kBRegs], bn[NT][KG][C::kBRegs];
+    for (int f = 0; f < FR; ++f)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      load_b<kFp4, KG>(bc[nt], nt < ntiles ? bsrc[nt] : nullptr, 0, ct.nkb, c, ct.down);
-
+      for (int nt = 0; nt < NT; ++nt) acc[f][nt][0] = acc[f][nt][1] = acc[f][nt][2] = acc[f][nt][3] = 0.f;
+    if constexpr (kFp4) {
+      // NVFP4: token rows double-buffered in half blocks (64 K elements = the
+      // four mma steps that use one scale byte of each row)
+      uint32_t bh[2][NT][8];
+      auto load_half = [&](uint32_t (&b)[NT][8], int kb, int hf) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            uint4 t = make_uint4(0, 0, 0, 0);
+            if (nt < ntiles && bsrc[nt] && kb < ct.nkb) {
+              const uint4* pp = reinterpret_cast<const uint4*>(bsrc[nt] + (size_t)kb * 128 + 32 * c +
+                                                               8 * (2 * hf + v));
+              t = ct.down ? __ldcg(pp) : *pp;
+            }
+            b[nt][4 * v + 0] = t.x; b[nt][4 * v + 1] = t.y; b[nt][4 * v + 2] = t.z; b[nt][4 * v + 3] = t.w;
+          }
+        }
+      };
+      load_half(bh[0], 0, 0);
 #pragma unroll 1
-    for (int gi = 0; gi < ct.ngroups; ++gi) {
-      if (gi + 1 < ct.ngroups) {
+      for (int gi = 0; gi < ct.ngroups; ++gi) {   // KG = 1: group gi = block gi
+        load_half(bh[1], gi, 1);
+        cp_async_wait<NS - 2>();
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          load_b<kFp4, KG>(bn[nt], nt < ntiles ? bsrc[nt] : nullptr, gi + 1, ct.nkb, c, ct.down);
-      }
-      cp_async_wait<NS - 2>();
+        for (int hf = 0; hf < 2; ++hf) {
+          if (hf == 1) load_half(bh[0], gi + 1, 0);
 #pragma unroll
-      for (int i = 0; i < KG; ++i) {
-        const int kb = gi * KG + i;
-        if (kb >= ct.nkb) continue;
-        const uint4 alo = ring[((slot_r * KG + i) * 2) * 32 + lane];
-        const uint4 ahi = ring[((slot_r * KG + i) * 2 + 1) * 32 + lane];
-        if constexpr (kFp4) {
-          const uint2 slo8 = sring[((slot_r * KG + i) * 2) * 32 + lane];
-          const uint2 shi8 = sring[((slot_r * KG + i) * 2 + 1) * 32 + lane];
-          // this thread's two scales: bytes 2c and 2c+1 of the row's 8, as
-          // bf16 pairs {s, s}; steps 0-3 use the first, steps 4-7 the second
-          const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1));
-          const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1));
-          uint32_t sl2[2], sh2[2];
+          for (int f = 0; f < FR; ++f) {
+            const int rs = ((slot_r * FR + f) * 2) * 32 + lane;
+            const uint4 alo = ring[rs];
+            const uint4 ahi = ring[rs + 32];
+            const uint2 slo8 = sring[rs];
+            const uint2 shi8 = sring[rs + 32];
+            // this thread's scale for this half: byte 2c + hf of the row's 8, as a
+            // bf16 pair {s, s}
+            const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1) + 8 * hf);
+            const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1) + 8 * hf);
+            const uint32_t a8 = lut8[slo & 0xff], b8 = lut8[shi & 0xff];
+            const uint32_t sl2 = a8 | (a8 << 16), sh2 = b8 | (b8 << 16);
+            const uint32_t clo[2] = {hf ? alo.z : alo.x, hf ? alo.w : alo.y};
+            const uint32_t chi[2] = {hf ? ahi.z : ahi.x, hf ? ahi.w : ahi.y};
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const uint32_t a8 = lut8[(slo >> (8 * hb)) & 0xff];
-            const uint32_t b8 = lut8[(shi >> (8 * hb)) & 0xff];
-            sl2[hb] = a8 | (a8 << 16);
-            sh2[hb] = b8 | (b8 << 16);
-          }
-          const uint32_t clo[4] = {alo.x, alo.y, alo.z, alo.w};
-          const uint32_t chi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
+              const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
+              const uint32_t a0 = bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2);
+              const uint32_t a2 = bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2);
+              const uint32_t a1 = bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2);
+              const uint32_t a3 = bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
-            const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
-            const uint32_t a0 = bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2[q >> 2]);
-            const uint32_t a2 = bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2[q >> 2]);
-            const uint32_t a1 = bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2[q >> 2]);
-            const uint32_t a3 = bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2[q >> 2]);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              if (nt < ntiles) mma_bf16_16816(acc[nt], a0, a1, a2, a3, bc[nt][i][2 * q], bc[nt][i][2 * q + 1]);
-          }
-        } else {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            if (nt < ntiles) {
-              mma_bf16_16816(acc[nt], alo.x, ahi.x, alo.y, ahi.y, bc[nt][i][0], bc[nt][i][1]);
-              mma_bf16_16816(acc[nt], alo.z, ahi.z, alo.w, ahi.w, bc[nt][i][2], bc[nt][i][3]);
+              for (int nt = 0; nt < NT; ++nt)
+                if (nt < ntiles) mma_bf16_16816(acc[f][nt], a0, a1, a2, a3, bh[hf][nt][2 * q], bh[hf][nt][2 * q + 1]);
             }
           }
         }
+        slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
+        issue_next();
       }
-      slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
-      issue_next();
-#pragma unroll
+    } else {
+    uint32_t bc[NT][KG][4], bn[NT][KG][4];
+  #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < KG; ++i)
-#pragma unroll
-          for (int j = 0; j < C::kBRegs; ++j) bc[nt][i][j] = bn[nt][i][j];
-    }
+        load_b<KG>(bc[nt], nt < ntiles ? bsrc[nt] : nullptr, 0, ct.nkb, c, ct.down);
 
+  #pragma unroll 1
+      for (int gi = 0; gi < ct.ngroups; ++gi) {
+        if (gi + 1 < ct.ngroups) {
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            load_b<KG>(bn[nt], nt < ntiles ? bsrc[nt] : nullptr, gi + 1, ct.nkb, c, ct.down);
+        }
+        cp_async_wait<NS - 2>();
+  #pragma unroll
+        for (int i = 0; i < KG; ++i) {
+          const int kb = gi * KG + i;
+          if (kb >= ct.nkb) continue;
+  #pragma unroll
+          for (int f = 0; f < FR; ++f) {
+          const uint4 alo = ring[(((slot_r * KG + i) * FR + f) * 2) * 32 + lane];
+          const uint4 ahi = ring[(((slot_r * KG + i) * FR + f) * 2 + 1) * 32 + lane];
+          if constexpr (kFp4) {
+            const uint2 slo8 = sring[(((slot_r * KG + i) * FR + f) * 2) * 32 + lane];
+            const uint2 shi8 = sring[(((slot_r * KG + i) * FR + f) * 2 + 1) * 32 + lane];
+            // this thread's two scales: bytes 2c and 2c+1 of the row's 8, as
+            // bf16 pairs {s, s}; steps 0-3 use the first, steps 4-7 the second
+            const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1));
+            const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1));
+            uint32_t sl2[2], sh2[2];
+  #pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const uint32_t a8 = lut8[(slo >> (8 * hb)) & 0xff];
+              const uint32_t b8 = lut8[(shi >> (8 * hb)) & 0xff];
+              sl2[hb] = a8 | (a8 << 16);
+              sh2[hb] = b8 | (b8 << 16);
+            }
+            const uint32_t clo[4] = {alo.x, alo.y, alo.z, alo.w};
+            const uint32_t chi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+  #pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
+              const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
+              const uint32_t a0 = bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2[q >> 2]);
+              const uint32_t a2 = bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2[q >> 2]);
+              const uint32_t a1 = bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2[q >> 2]);
+              const uint32_t a3 = bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2[q >> 2]);
+  #pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                if (nt < ntiles) mma_bf16_16816(acc[f][nt], a0, a1, a2, a3, bc[nt][i][2 * q], bc[nt][i][2 * q + 1]);
+            }
+          } else {
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              if (nt < ntiles) {
+                mma_bf16_16816(acc[f][nt], alo.x, ahi.x, alo.y, ahi.y, bc[nt][i][0], bc[nt][i][1]);
+                mma_bf16_16816(acc[f][nt], alo.z, ahi.z, alo.w, ahi.w, bc[nt][i][2], bc[nt][i][3]);
+              }
+            }
+          }
+          }
+        }
+        slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
+        issue_next();
+  #pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+          for (int i = 0; i < KG; ++i)
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) bc[nt][i][j] = bn[nt][i][j];
+      }
+  
+    }
     // epilogue straight from the fragments: c0,c1 = row g, tokens 2c,2c+1;
     // c2,c3 = row g+8, same tokens
     float gscale = 1.0f;
     if constexpr (kFp4) gscale = ct.down ? a.dn_global[ct.e] : a.gu_global[ct.e];
+#pragma unroll
+    for (int fr = 0; fr < FR; ++fr)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       if (nt >= ntiles) continue;
@@ -448,13 +515,13 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
         const int n = p0 + nt * 8 + 2 * c + h2;
         if (n < ct.m) {
           if (!ct.down) {
-            const float gv = acc[nt][h2] * gscale, uv = acc[nt][2 + h2] * gscale;
-            a.h[(size_t)(ct.off + n) * a.I + ct.blk * 8 + g] = f2bf(silu(gv) * uv);
+            const float gv = acc[fr][nt][h2] * gscale, uv = acc[fr][nt][2 + h2] * gscale;
+            a.h[(size_t)(ct.off + n) * a.I + (ct.blk * FR + fr) * 8 + g] = f2bf(silu(gv) * uv);
           } else {
             const int f = ef[nt][h2];
             const float wt = ew[nt][h2];
-            const float y0 = wt * (acc[nt][h2] * gscale), y1 = wt * (acc[nt][2 + h2] * gscale);
-            const size_t o = (size_t)f * a.H + ct.blk * 16 + g;
+            const float y0 = wt * (acc[fr][nt][h2] * gscale), y1 = wt * (acc[fr][nt][2 + h2] * gscale);
+            const size_t o = (size_t)f * a.H + (ct.blk * FR + fr) * 16 + g;
             if (a.partial_f32) {
               reinterpret_cast<float*>(a.partial)[o] = y0;
               reinterpret_cast<float*>(a.partial)[o + 8] = y1;
@@ -482,7 +549,7 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   using C = StreamCfg<kFp4, NT>;
   const long long S = (long long)a.T * a.k;
   const long long max_active = S < a.E ? S : a.E;
-  const long long units = max_active * (a.I / 8 + a.H / 16);
+  const long long units = max_active * (a.I / (8 * C::FR) + a.H / (16 * C::FR));
   long long grid = a.num_sms;
   const long long need = (units + C::kWarps - 1) / C::kWarps;
   if (grid > need) grid = need;
@@ -510,10 +577,12 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
 cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
   // a group never holds more rows than the batch has tokens: one 8-row tile
-  // per pass for T <= 8, two above
+  // per pass for T <= 8, two above (and four for NVFP4 above 16 tokens)
   const bool two = a.T > 8;
-  if (a.gu_codes != nullptr)
+  if (a.gu_codes != nullptr) {
+    if (a.T > 16) return launch_variant<true, 4>(a, stream);
     return two ? launch_variant<true, 2>(a, stream) : launch_variant<true, 1>(a, stream);
+  }
   return two ? launch_variant<false, 2>(a, stream) : launch_variant<false, 1>(a, stream);
 }
 
