@@ -95,6 +95,10 @@ struct TcLaunch {
 constexpr int kTcRows = 128;             // token rows per tensor-core tile
 cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, int* launches);
 
+// tc_gemm.cu -- xp[r] = x[perm[r] / k]: token rows in grouped order
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int S, int H, int k,
+                               uint16_t* xp, cudaStream_t stream, int* launches);
+
 // combine.cu -- out[t] = sum_s partial[t*k+s] in slot order
 cudaError_t launch_combine(const void* partial, bool partial_f32, int T, int H, int k,
                            uint16_t* out, cudaStream_t stream, int* launches);

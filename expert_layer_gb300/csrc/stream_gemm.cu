@@ -38,36 +38,12 @@
 // accumulator in the epilogue.
 #include "common.cuh"
 #include "kernels.h"
+#include "nvfp4.cuh"
 
 namespace moe {
 
 namespace {
 
-
-// e2m1 code -> value, from the format: sign, 2-bit exponent (bias 1), 1-bit
-// mantissa; exponent 0 is subnormal (m * 0.5).
-__device__ float e2m1_value(int code) {
-  const int e = (code >> 1) & 3, m = code & 1;
-  const float mag = e == 0 ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, e - 1);
-  return (code & 8) ? -mag : mag;
-}
-
-// e4m3 byte -> value: sign, 4-bit exponent (bias 7), 3-bit mantissa; exponent 0
-// is subnormal (m/8 * 2^-6); S.1111.111 is NaN.
-__device__ float e4m3_value(int b) {
-  const int e = (b >> 3) & 15, m = b & 7;
-  float mag;
-  if (e == 15 && m == 7) mag = __int_as_float(0x7fc00000);
-  else if (e == 0) mag = ldexpf((float)m / 8.0f, -6);
-  else mag = ldexpf(1.0f + (float)m / 8.0f, e - 7);
-  return (b & 0x80) ? -mag : mag;
-}
-
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
@@ -206,11 +182,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
   uint2* sring = reinterpret_cast<uint2*>(smem + warp * C::kWarpBytes + C::kWBytes);
 
   if constexpr (kFp4) {
-    for (int i = threadIdx.x; i < 256 * 32; i += NW * 32) {
-      const int b = i >> 5;
-      lut2[i] = pack_bf16x2(e2m1_value(b & 15), e2m1_value(b >> 4));
-      if ((i & 31) == 0) lut8[b] = f2bf(e4m3_value(b));
-    }
+    nvfp4::fill_tables(lut2, lut8, threadIdx.x, NW * 32);
     __syncthreads();
   }
 
@@ -415,10 +387,10 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
             for (int q = 0; q < 4; ++q) {
               const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
               const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
-              const uint32_t a0 = bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2);
-              const uint32_t a2 = bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2);
-              const uint32_t a1 = bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2);
-              const uint32_t a3 = bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2);
+              const uint32_t a0 = nvfp4::bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2);
+              const uint32_t a2 = nvfp4::bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2);
+              const uint32_t a1 = nvfp4::bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2);
+              const uint32_t a3 = nvfp4::bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
                 if (nt < ntiles) mma_bf16_16816(acc[f][nt], a0, a1, a2, a3, bh[hf][nt][2 * q], bh[hf][nt][2 * q + 1]);
@@ -471,10 +443,10 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
             for (int q = 0; q < 8; ++q) {
               const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
               const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
-              const uint32_t a0 = bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2[q >> 2]);
-              const uint32_t a2 = bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2[q >> 2]);
-              const uint32_t a1 = bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2[q >> 2]);
-              const uint32_t a3 = bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2[q >> 2]);
+              const uint32_t a0 = nvfp4::bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2[q >> 2]);
+              const uint32_t a2 = nvfp4::bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2[q >> 2]);
+              const uint32_t a1 = nvfp4::bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2[q >> 2]);
+              const uint32_t a3 = nvfp4::bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2[q >> 2]);
   #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
                 if (nt < ntiles) mma_bf16_16816(acc[f][nt], a0, a1, a2, a3, bc[nt][i][2 * q], bc[nt][i][2 * q + 1]);

@@ -7,7 +7,8 @@
 // sec. 9.9): tile lists come from the grouping kernels' counts, no host sync.
 //
 // One persistent CTA per SM, 6 warps:
-//   warp 0      producer: tiled TMA loads into a 4-stage shared-memory ring:
+//   warp 0      producer (one thread): tiled TMA loads into a 4-stage
+//               shared-memory ring:
 //               token rows in grouped order (x gathered through the grouped
 //               permutation by gather_rows, or h) and weight rows
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16 x bf16 -> fp32
@@ -33,10 +34,13 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
 namespace {
+
+using namespace tcx;
 
 constexpr int BM = 128, BN = 256, BK = 64, NS = 4;
 constexpr int kTileBytesA = BM * BK * 2;                // 16 KB
@@ -44,7 +48,6 @@ constexpr int kTileBytesB = BN * BK * 2;                // 32 KB
 constexpr int kStageBytes = kTileBytesA + kTileBytesB;  // 48 KB
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;                     // two 256-column accumulators
-constexpr uint32_t kSpinLimit = 1u << 22;   // ~1 s of failed tries
 constexpr int kMaxLarge = 1024;
 // stages + alignment slack + barriers + tile metadata (4 int arrays of kMaxLarge+1)
 constexpr size_t kSmemBytes = (size_t)NS * kStageBytes + 1024 + 256 + 4 * 4 * (kMaxLarge + 1);
@@ -65,65 +68,6 @@ struct TcArgs {
   int* status;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false after kSpinLimit unsuccessful tries.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-// Lane 0 waits, the warp follows its verdict (a warp-uniform result).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
-      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);          // start address
-  d |= (uint64_t)1 << 16;                           // leading byte offset (unused here)
-  d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
-  d |= (uint64_t)1 << 46;                           // descriptor version
-  d |= (uint64_t)2 << 61;                           // 128-byte swizzle
-  return d;
-}
-
 // Instruction descriptor: kind::f16, bf16 A/B, fp32 D, K-major A and B.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                             ((uint32_t)(BM >> 4) << 24);
@@ -135,26 +79,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint6
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum));
 }
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
 // Per-CTA copy of the large-expert tile metadata (shared memory).
 struct TileMeta {
   int* tiles;   // [nlarge+1] m-tile prefix
@@ -242,14 +166,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile(md, nlarge, NTN, t);
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % NS;
-        const uint32_t ph = (it / NS) & 1;
-        if (!warp_wait(&empty[s], ph ^ 1)) { atomicOr(abort_flag, 1); break; }
-        if (lane == 0) {
+    // one thread: no warp-wide synchronisation per stage
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(md, nlarge, NTN, t);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % NS;
+          const uint32_t ph = (it / NS) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
           unsigned char* sA = smem + s * kStageBytes;
           unsigned char* sB = sA + kTileBytesA;
           mbar_expect_tx(&full[s], kStageBytes);
@@ -262,26 +188,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sB + kTileBytesB / 2, &tmB, kb * BK, row0 + a.I, &full[s]);
           }
         }
-        __syncwarp();
+        if (*(volatile int*)abort_flag) ok = false;
       }
-      if (*(volatile int*)abort_flag) break;
+      if (!ok) atomicOr(abort_flag, 1);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    uint32_t it = 0, lt = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
-      const uint32_t b = lt & 1;
-      const uint32_t tph = (lt >> 1) & 1;
-      if (!warp_wait(&tempty[b], tph ^ 1)) { atomicOr(abort_flag, 1); break; }
-      tc_fence_after();
-      const uint32_t tmem_d = tmem_base + b * BN;
+    // one thread issues every MMA; the stage loop has no warp-wide
+    // synchronisation, so that issuing keeps ahead of the tensor pipe
+    if (lane == 0) {
+      uint32_t it = 0, lt = 0;
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % NS;
-        const uint32_t ph = (it / NS) & 1;
-        if (!warp_wait(&full[s], ph)) { ok = false; break; }
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
+        const uint32_t b = lt & 1;
+        const uint32_t tph = (lt >> 1) & 1;
+        if (!mbar_wait(&tempty[b], tph ^ 1)) { ok = false; break; }
         tc_fence_after();
-        if (lane == 0) {
+        const uint32_t tmem_d = tmem_base + b * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % NS;
+          const uint32_t ph = (it / NS) & 1;
+          if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+          tc_fence_after();
           const uint32_t sA = smem_u32(smem + s * kStageBytes);
           const uint32_t sB = sA + kTileBytesA;
 #pragma unroll
@@ -290,13 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (kb | kk) != 0 ? 1u : 0u);
           umma_commit(&empty[s]);   // frees the stage when these MMAs finish reading it
         }
-        __syncwarp();
+        if (!ok) break;
+        umma_commit(&tfull[b]);     // accumulator ready
+        if (*(volatile int*)abort_flag) ok = false;
       }
-      if (!ok) { atomicOr(abort_flag, 1); break; }
-      if (lane == 0) umma_commit(&tfull[b]);   // accumulator ready
-      __syncwarp();
-      if (*(volatile int*)abort_flag) break;
+      if (!ok) atomicOr(abort_flag, 1);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quadrant of this warp
@@ -305,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       const uint32_t b = lt & 1;
       const uint32_t tph = (lt >> 1) & 1;
-      if (!mbar_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
+      if (!warp_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
       tc_fence_after();
       const TileInfo ti = decode_tile(md, nlarge, NTN, t);
       const int r = ti.mtile * BM + row;   // row within the expert's group
@@ -391,39 +320,20 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;   // resolved once; a pure function pointer
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_map_2d(m, base, rows, cols, 2, BK, box_rows, true);
 }
 
 }  // namespace
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int S, int H, int k,
+                               uint16_t* xp, cudaStream_t stream, int* launches) {
+  const long long blocks = ((long long)S + 7) / 8;
+  gather_rows_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(x, perm, S, H, k, xp);
+  if (launches) *launches += 1;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, int* launches) {
   TcArgs a{};
@@ -434,10 +344,8 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
   a.status = p.status;
   const long long S = (long long)p.T * p.k;
   if (!down) {
-    const long long blocks = (S + 7) / 8;
-    gather_rows_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
-        p.x, p.perm, (int)S, p.H, p.k, p.xp);
-    if (launches) *launches += 1;
+    const cudaError_t gerr = launch_gather_rows(p.x, p.perm, (int)S, p.H, p.k, p.xp, stream, launches);
+    if (gerr != cudaSuccess) return gerr;
   }
   CUtensorMap tmA, tmB;
   if (!down) {

@@ -42,6 +42,11 @@ SMALL_CASES = {
     "E1024_k32": dict(T=16, H=256, E=1024, k=32, I=128),
     "zipf": dict(T=50, H=512, E=32, k=4, I=256, bias="zipf"),
     "nvfp4_small": dict(T=24, H=256, E=8, k=2, I=128, nvfp4=True),
+    # NVFP4 streaming with several 32-row passes per group, and with H = 1280
+    # (scale rows of 80 bytes)
+    "nvfp4_t96": dict(T=96, H=256, E=8, k=2, I=256, nvfp4=True),
+    "nvfp4_passes": dict(T=300, H=256, E=4, k=2, I=256, nvfp4=True),
+    "nvfp4_h1280": dict(T=80, H=1280, E=8, k=2, I=256, nvfp4=True),
     # groups of >= 64 rows run on the tcgen05 kernels
     "tc_all": dict(T=512, H=256, E=8, k=2, I=128),
     "tc_mixed": dict(T=300, H=512, E=16, k=2, I=256, bias="zipf"),
