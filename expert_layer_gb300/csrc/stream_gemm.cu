@@ -36,6 +36,8 @@
 // Both steps are exact (an e2m1 value times an e4m3 value has at most 6
 // significant bits); the per-expert fp32 global scale multiplies the fp32
 // accumulator in the epilogue.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "nvfp4.cuh"
@@ -310,200 +312,182 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
       __syncwarp();
     }
     const int p0 = ct.pass * 8 * NT;
-    const uint16_t* bsrc[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int n = p0 + nt * 8 + g;
-      bsrc[nt] = nullptr;
-      if (n < ct.m) {
-        if (ct.down) bsrc[nt] = a.h + (size_t)(ct.off + n) * a.I;
-        else bsrc[nt] = a.x + (size_t)(permp[ct.off + n] / a.k) * a.H;
-      }
-    }
-    // down: the epilogue's slots and routing weights, fetched now
-    int ef[NT][2];
-    float ew[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int n = p0 + nt * 8 + 2 * c + h2;
-        ef[nt][h2] = 0;
-        ew[nt][h2] = 0.f;
-        if (ct.down && n < ct.m) {
-          ef[nt][h2] = permp[ct.off + n];
-          ew[nt][h2] = a.topk_w[ef[nt][h2]];
-        }
-      }
-    const int ntiles = min(NT, (ct.m - p0 + 7) / 8);
-    float acc[FR][NT][4];
-#pragma unroll
-    for (int f = 0; f < FR; ++f)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[f][nt][0] = acc[f][nt][1] = acc[f][nt][2] = acc[f][nt][3] = 0.f;
-    if constexpr (kFp4) {
-      // NVFP4: token rows double-buffered in half blocks (64 K elements = the
-      // four mma steps that use one scale byte of each row)
-      uint32_t bh[2][NT][8];
-      auto load_half = [&](uint32_t (&b)[NT][8], int kb, int hf) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int v = 0; v < 2; ++v) {
-            uint4 t = make_uint4(0, 0, 0, 0);
-            if (nt < ntiles && bsrc[nt] && kb < ct.nkb) {
-              const uint4* pp = reinterpret_cast<const uint4*>(bsrc[nt] + (size_t)kb * 128 + 32 * c +
-                                                               8 * (2 * hf + v));
-              t = ct.down ? __ldcg(pp) : *pp;
-            }
-            b[nt][4 * v + 0] = t.x; b[nt][4 * v + 1] = t.y; b[nt][4 * v + 2] = t.z; b[nt][4 * v + 3] = t.w;
-          }
-        }
-      };
-      load_half(bh[0], 0, 0);
-#pragma unroll 1
-      for (int gi = 0; gi < ct.ngroups; ++gi) {   // KG = 1: group gi = block gi
-        load_half(bh[1], gi, 1);
-        cp_async_wait<NS - 2>();
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          if (hf == 1) load_half(bh[0], gi + 1, 0);
-#pragma unroll
-          for (int f = 0; f < FR; ++f) {
-            const int rs = ((slot_r * FR + f) * 2) * 32 + lane;
-            const uint4 alo = ring[rs];
-            const uint4 ahi = ring[rs + 32];
-            const uint2 slo8 = sring[rs];
-            const uint2 shi8 = sring[rs + 32];
-            // this thread's scale for this half: byte 2c + hf of the row's 8, as a
-            // bf16 pair {s, s}
-            const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1) + 8 * hf);
-            const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1) + 8 * hf);
-            const uint32_t a8 = lut8[slo & 0xff], b8 = lut8[shi & 0xff];
-            const uint32_t sl2 = a8 | (a8 << 16), sh2 = b8 | (b8 << 16);
-            const uint32_t clo[2] = {hf ? alo.z : alo.x, hf ? alo.w : alo.y};
-            const uint32_t chi[2] = {hf ? ahi.z : ahi.x, hf ? ahi.w : ahi.y};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
-              const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
-              const uint32_t a0 = nvfp4::bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2);
-              const uint32_t a2 = nvfp4::bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2);
-              const uint32_t a1 = nvfp4::bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2);
-              const uint32_t a3 = nvfp4::bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                if (nt < ntiles) mma_bf16_16816(acc[f][nt], a0, a1, a2, a3, bh[hf][nt][2 * q], bh[hf][nt][2 * q + 1]);
-            }
-          }
-        }
-        slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
-        issue_next();
-      }
-    } else {
-    uint32_t bc[NT][KG][4], bn[NT][KG][4];
+    // one pass over K against NP token tiles (8 rows each) starting at p0
+    auto run_pass = [&](auto np_tag) {
+      constexpr int NP = decltype(np_tag)::value;
+      const uint16_t* bsrc[NP];
   #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        load_b<KG>(bc[nt], nt < ntiles ? bsrc[nt] : nullptr, 0, ct.nkb, c, ct.down);
-
+      for (int nt = 0; nt < NP; ++nt) {
+        const int n = p0 + nt * 8 + g;
+        bsrc[nt] = nullptr;
+        if (n < ct.m) {
+          if (ct.down) bsrc[nt] = a.h + (size_t)(ct.off + n) * a.I;
+          else bsrc[nt] = a.x + (size_t)(permp[ct.off + n] / a.k) * a.H;
+        }
+      }
+      // down: the epilogue's slots and routing weights, fetched now
+      int ef[NP][2];
+      float ew[NP][2];
+  #pragma unroll
+      for (int nt = 0; nt < NP; ++nt)
+  #pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int n = p0 + nt * 8 + 2 * c + h2;
+          ef[nt][h2] = 0;
+          ew[nt][h2] = 0.f;
+          if (ct.down && n < ct.m) {
+            ef[nt][h2] = permp[ct.off + n];
+            ew[nt][h2] = a.topk_w[ef[nt][h2]];
+          }
+        }
+      const int ntiles = min(NP, (ct.m - p0 + 7) / 8);
+      float acc[FR][NP][4];
+  #pragma unroll
+      for (int f = 0; f < FR; ++f)
+  #pragma unroll
+        for (int nt = 0; nt < NP; ++nt) acc[f][nt][0] = acc[f][nt][1] = acc[f][nt][2] = acc[f][nt][3] = 0.f;
+      if constexpr (kFp4) {
+        // NVFP4: token rows double-buffered in half blocks (64 K elements = the
+        // four mma steps that use one scale byte of each row)
+        uint32_t bh[2][NP][8];
+        auto load_half = [&](uint32_t (&b)[NP][8], int kb, int hf) {
+  #pragma unroll
+          for (int nt = 0; nt < NP; ++nt) {
+  #pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              uint4 t = make_uint4(0, 0, 0, 0);
+              if (nt < ntiles && bsrc[nt] && kb < ct.nkb) {
+                const uint4* pp = reinterpret_cast<const uint4*>(bsrc[nt] + (size_t)kb * 128 + 32 * c +
+                                                                 8 * (2 * hf + v));
+                t = ct.down ? __ldcg(pp) : *pp;
+              }
+              b[nt][4 * v + 0] = t.x; b[nt][4 * v + 1] = t.y; b[nt][4 * v + 2] = t.z; b[nt][4 * v + 3] = t.w;
+            }
+          }
+        };
+        load_half(bh[0], 0, 0);
   #pragma unroll 1
-      for (int gi = 0; gi < ct.ngroups; ++gi) {
-        if (gi + 1 < ct.ngroups) {
+        for (int gi = 0; gi < ct.ngroups; ++gi) {   // KG = 1: group gi = block gi
+          load_half(bh[1], gi, 1);
+          cp_async_wait<NS - 2>();
   #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            load_b<KG>(bn[nt], nt < ntiles ? bsrc[nt] : nullptr, gi + 1, ct.nkb, c, ct.down);
-        }
-        cp_async_wait<NS - 2>();
+          for (int hf = 0; hf < 2; ++hf) {
+            if (hf == 1) load_half(bh[0], gi + 1, 0);
   #pragma unroll
-        for (int i = 0; i < KG; ++i) {
-          const int kb = gi * KG + i;
-          if (kb >= ct.nkb) continue;
+            for (int f = 0; f < FR; ++f) {
+              const int rs = ((slot_r * FR + f) * 2) * 32 + lane;
+              const uint4 alo = ring[rs];
+              const uint4 ahi = ring[rs + 32];
+              const uint2 slo8 = sring[rs];
+              const uint2 shi8 = sring[rs + 32];
+              // this thread's scale for this half: byte 2c + hf of the row's 8, as a
+              // bf16 pair {s, s}
+              const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1) + 8 * hf);
+              const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1) + 8 * hf);
+              const uint32_t a8 = lut8[slo & 0xff], b8 = lut8[shi & 0xff];
+              const uint32_t sl2 = a8 | (a8 << 16), sh2 = b8 | (b8 << 16);
+              const uint32_t clo[2] = {hf ? alo.z : alo.x, hf ? alo.w : alo.y};
+              const uint32_t chi[2] = {hf ? ahi.z : ahi.x, hf ? ahi.w : ahi.y};
   #pragma unroll
-          for (int f = 0; f < FR; ++f) {
-          const uint4 alo = ring[(((slot_r * KG + i) * FR + f) * 2) * 32 + lane];
-          const uint4 ahi = ring[(((slot_r * KG + i) * FR + f) * 2 + 1) * 32 + lane];
-          if constexpr (kFp4) {
-            const uint2 slo8 = sring[(((slot_r * KG + i) * FR + f) * 2) * 32 + lane];
-            const uint2 shi8 = sring[(((slot_r * KG + i) * FR + f) * 2 + 1) * 32 + lane];
-            // this thread's two scales: bytes 2c and 2c+1 of the row's 8, as
-            // bf16 pairs {s, s}; steps 0-3 use the first, steps 4-7 the second
-            const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1));
-            const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1));
-            uint32_t sl2[2], sh2[2];
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
+                const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
+                const uint32_t a0 = nvfp4::bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2);
+                const uint32_t a2 = nvfp4::bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2);
+                const uint32_t a1 = nvfp4::bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2);
+                const uint32_t a3 = nvfp4::bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2);
   #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-              const uint32_t a8 = lut8[(slo >> (8 * hb)) & 0xff];
-              const uint32_t b8 = lut8[(shi >> (8 * hb)) & 0xff];
-              sl2[hb] = a8 | (a8 << 16);
-              sh2[hb] = b8 | (b8 << 16);
-            }
-            const uint32_t clo[4] = {alo.x, alo.y, alo.z, alo.w};
-            const uint32_t chi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
-  #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
-              const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
-              const uint32_t a0 = nvfp4::bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2[q >> 2]);
-              const uint32_t a2 = nvfp4::bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2[q >> 2]);
-              const uint32_t a1 = nvfp4::bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2[q >> 2]);
-              const uint32_t a3 = nvfp4::bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2[q >> 2]);
-  #pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                if (nt < ntiles) mma_bf16_16816(acc[f][nt], a0, a1, a2, a3, bc[nt][i][2 * q], bc[nt][i][2 * q + 1]);
-            }
-          } else {
-  #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              if (nt < ntiles) {
-                mma_bf16_16816(acc[f][nt], alo.x, ahi.x, alo.y, ahi.y, bc[nt][i][0], bc[nt][i][1]);
-                mma_bf16_16816(acc[f][nt], alo.z, ahi.z, alo.w, ahi.w, bc[nt][i][2], bc[nt][i][3]);
+                for (int nt = 0; nt < NP; ++nt)
+                  if (nt < ntiles) mma_bf16_16816(acc[f][nt], a0, a1, a2, a3, bh[hf][nt][2 * q], bh[hf][nt][2 * q + 1]);
               }
             }
           }
-          }
+          slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
+          issue_next();
         }
-        slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
-        issue_next();
-  #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-  #pragma unroll
-          for (int i = 0; i < KG; ++i)
-  #pragma unroll
-            for (int j = 0; j < 4; ++j) bc[nt][i][j] = bn[nt][i][j];
-      }
+      } else {
+      uint32_t bc[NP][KG][4], bn[NP][KG][4];
+    #pragma unroll
+        for (int nt = 0; nt < NP; ++nt)
+          load_b<KG>(bc[nt], nt < ntiles ? bsrc[nt] : nullptr, 0, ct.nkb, c, ct.down);
+
+    #pragma unroll 1
+        for (int gi = 0; gi < ct.ngroups; ++gi) {
+          if (gi + 1 < ct.ngroups) {
+    #pragma unroll
+            for (int nt = 0; nt < NP; ++nt)
+              load_b<KG>(bn[nt], nt < ntiles ? bsrc[nt] : nullptr, gi + 1, ct.nkb, c, ct.down);
+          }
+          cp_async_wait<NS - 2>();
+    #pragma unroll
+          for (int i = 0; i < KG; ++i) {
+            const int kb = gi * KG + i;
+            if (kb >= ct.nkb) continue;
+    #pragma unroll
+            for (int f = 0; f < FR; ++f) {
+            const uint4 alo = ring[(((slot_r * KG + i) * FR + f) * 2) * 32 + lane];
+            const uint4 ahi = ring[(((slot_r * KG + i) * FR + f) * 2 + 1) * 32 + lane];
+            {
+    #pragma unroll
+              for (int nt = 0; nt < NP; ++nt) {
+                if (nt < ntiles) {
+                  mma_bf16_16816(acc[f][nt], alo.x, ahi.x, alo.y, ahi.y, bc[nt][i][0], bc[nt][i][1]);
+                  mma_bf16_16816(acc[f][nt], alo.z, ahi.z, alo.w, ahi.w, bc[nt][i][2], bc[nt][i][3]);
+                }
+              }
+            }
+            }
+          }
+          slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
+          issue_next();
+    #pragma unroll
+          for (int nt = 0; nt < NP; ++nt)
+    #pragma unroll
+            for (int i = 0; i < KG; ++i)
+    #pragma unroll
+              for (int j = 0; j < 4; ++j) bc[nt][i][j] = bn[nt][i][j];
+        }
   
-    }
-    // epilogue straight from the fragments: c0,c1 = row g, tokens 2c,2c+1;
-    // c2,c3 = row g+8, same tokens
-    float gscale = 1.0f;
-    if constexpr (kFp4) gscale = ct.down ? a.dn_global[ct.e] : a.gu_global[ct.e];
-#pragma unroll
-    for (int fr = 0; fr < FR; ++fr)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      if (nt >= ntiles) continue;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int n = p0 + nt * 8 + 2 * c + h2;
-        if (n < ct.m) {
-          if (!ct.down) {
-            const float gv = acc[fr][nt][h2] * gscale, uv = acc[fr][nt][2 + h2] * gscale;
-            a.h[(size_t)(ct.off + n) * a.I + (ct.blk * FR + fr) * 8 + g] = f2bf(silu(gv) * uv);
-          } else {
-            const int f = ef[nt][h2];
-            const float wt = ew[nt][h2];
-            const float y0 = wt * (acc[fr][nt][h2] * gscale), y1 = wt * (acc[fr][nt][2 + h2] * gscale);
-            const size_t o = (size_t)f * a.H + (ct.blk * FR + fr) * 16 + g;
-            if (a.partial_f32) {
-              reinterpret_cast<float*>(a.partial)[o] = y0;
-              reinterpret_cast<float*>(a.partial)[o + 8] = y1;
+      }
+      // epilogue straight from the fragments: c0,c1 = row g, tokens 2c,2c+1;
+      // c2,c3 = row g+8, same tokens
+      float gscale = 1.0f;
+      if constexpr (kFp4) gscale = ct.down ? a.dn_global[ct.e] : a.gu_global[ct.e];
+  #pragma unroll
+      for (int fr = 0; fr < FR; ++fr)
+  #pragma unroll
+      for (int nt = 0; nt < NP; ++nt) {
+        if (nt >= ntiles) continue;
+  #pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int n = p0 + nt * 8 + 2 * c + h2;
+          if (n < ct.m) {
+            if (!ct.down) {
+              const float gv = acc[fr][nt][h2] * gscale, uv = acc[fr][nt][2 + h2] * gscale;
+              a.h[(size_t)(ct.off + n) * a.I + (ct.blk * FR + fr) * 8 + g] = f2bf(silu(gv) * uv);
             } else {
-              reinterpret_cast<uint16_t*>(a.partial)[o] = f2bf(y0);
-              reinterpret_cast<uint16_t*>(a.partial)[o + 8] = f2bf(y1);
+              const int f = ef[nt][h2];
+              const float wt = ew[nt][h2];
+              const float y0 = wt * (acc[fr][nt][h2] * gscale), y1 = wt * (acc[fr][nt][2 + h2] * gscale);
+              const size_t o = (size_t)f * a.H + (ct.blk * FR + fr) * 16 + g;
+              if (a.partial_f32) {
+                reinterpret_cast<float*>(a.partial)[o] = y0;
+                reinterpret_cast<float*>(a.partial)[o + 8] = y1;
+              } else {
+                reinterpret_cast<uint16_t*>(a.partial)[o] = f2bf(y0);
+                reinterpret_cast<uint16_t*>(a.partial)[o + 8] = f2bf(y1);
+              }
             }
           }
         }
       }
+    };
+    if constexpr (!kFp4 && NT > 1) {
+      // a pass with at most 8 rows left runs the one-tile loop
+      if (ct.m - p0 <= 8) run_pass(std::integral_constant<int, 1>{});
+      else run_pass(std::integral_constant<int, NT>{});
+    } else {
+      run_pass(std::integral_constant<int, NT>{});
     }
     if (++ct.pass < ct.npass) continue;
     if (!ct.down) {
