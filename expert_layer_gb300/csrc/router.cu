@@ -592,85 +592,82 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
 }
 
 // ------------------------------------------------------------ large batches
-// Logits: one CTA = 32 tokens x all E (<= 128) experts, 128 threads; thread
-// (ty, tx) owns tokens 4ty..4ty+3 and experts 4tx..4tx+3, 64+4tx..64+4tx+3.  K runs in chunks of
-// 64: a chunk's 64 products are summed sequentially from zero (63 roundings)
-// and the chunk sum is added to the running total (H/64 additions): at most
-// 64 + H/64 roundings per product.  Selection then runs one warp per token.
-constexpr int kTileT = 32, kTileE = 128, kTileK = 64;
+// Logits: one CTA = 32 tokens x all E (<= 128) experts, 4 warps.  K runs in
+// chunks of 32; the even chunks go to warps 0-1 and the odd chunks to warps
+// 2-3 (each pair has its own double-buffered tiles and named barrier).  In a
+// pair, warp w covers tokens 16(w mod 2) .. +15: lane l owns the 8 tokens
+// 8(l / 16) .. +7 of them and the 8 experts 4(l mod 16) .. +3 and
+// 64 + 4(l mod 16) .. +3, so a step is 64 FMAs from four 16-byte shared loads
+// (the token loads are broadcasts) -- register blocking that keeps the FMA
+// pipe, not shared memory, the limit.  A chunk's 32 products are summed
+// sequentially from zero (31 roundings); each pair adds its chunk sums in
+// order (H/64 additions) and the two pairs' totals are added once: at most
+// 32 + H/32 roundings per product.  Selection then runs one warp per token.
+constexpr int kTileT = 32, kTileE = 128, kTileK = 32, kTileThreads = 128;
+constexpr int kTileBuf = kTileK * (kTileT + kTileE);   // floats of one chunk's tiles
 
-__global__ void __launch_bounds__(128) router_tile_kernel(
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
     int T, int H, int E, float* __restrict__ logits, float* __restrict__ xnorm) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* xs = reinterpret_cast<float*>(smem_raw);           // [2][kTileK][kTileT]
-  float* wsm = xs + 2 * kTileK * kTileT;                    // [2][kTileK][kTileE]
+  // [pair][buf]: x tile [kTileK][kTileT] then w tile [kTileK][kTileE], fp32
+  float* tiles = reinterpret_cast<float*>(smem_raw);
+  __shared__ float s_sq[2][kTileT * 4];   // ||x_t||^2 partials of each pair
   const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;
   const int t0 = blockIdx.x * kTileT;
   const int warp = tid >> 5, lane = tid & 31;
+  const int pair = warp >> 1;             // chunks kc with kc % 2 == pair
+  const int ptid = tid & 63;              // thread index within the pair
+  const int tw = (warp & 1) * 16 + (lane >> 4) * 8;   // this lane's first token
+  const int ew = 4 * (lane & 15);                     // this lane's first expert (+64)
 
-  // ||x_t|| for the tile's tokens: warp-level sums (H/32 + 4 roundings).
-  for (int i = 0; i < kTileT / 4; ++i) {
-    const int t = t0 + warp * (kTileT / 4) + i;
-    float sq = 0.f;
-    if (t < T) {
-      for (int h = lane * 8; h < H; h += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          sq = fmaf(bf16lo(u[q]), bf16lo(u[q]), sq);
-          sq = fmaf(bf16hi(u[q]), bf16hi(u[q]), sq);
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0 && t < T) xnorm[t] = sqrtf(sq);
-  }
-
-  // Global -> register staging of one K chunk: x tile 32x64 (2 uint4 per
-  // thread), w tile 128x64 (8 uint4 per thread), transposed into [k][row].
+  // staging of one chunk by the 64 threads of a pair: x 32x32 (128 vectors,
+  // 2 per thread), w 128x32 (512 vectors, 8 per thread); vector v covers row
+  // v % rows and columns 8*(v / rows) .. +7 (consecutive lanes -> consecutive
+  // rows: the transposed stores hit 32 distinct banks)
   uint4 rx[2], rw[8];
+  float sqacc[2] = {0.f, 0.f};   // squares of the staged x values, per vector slot
   auto load_chunk = [&](int kc) {
     const int k0 = kc * kTileK;
-    // vector v covers row v % rows, columns 8*(v / rows) .. +7, so that the
-    // 32 lanes of a warp hold 32 consecutive rows of one column group and the
-    // transposed shared-memory stores below hit 32 distinct banks
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const int v = tid + 128 * i;          // 256 vectors
+      const int v = ptid + 64 * i;
       const int row = v % kTileT, col = (v / kTileT) * 8;
       const int t = t0 + row;
-      rx[i] = (t < T) ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + col)
-                      : make_uint4(0, 0, 0, 0);
+      rx[i] = (t < T) ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + col) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int v = tid + 128 * i;          // 1024 vectors
+      const int v = ptid + 64 * i;
       const int row = v % kTileE, col = (v / kTileE) * 8;
       rw[i] = (row < E) ? *reinterpret_cast<const uint4*>(gw + (size_t)row * H + k0 + col)
                         : make_uint4(0, 0, 0, 0);
     }
   };
   auto store_chunk = [&](int buf) {
-    float* xb = xs + buf * kTileK * kTileT;
-    float* wb = wsm + buf * kTileK * kTileE;
+    float* xb = tiles + (size_t)(pair * 2 + buf) * kTileBuf;
+    float* wb = xb + kTileK * kTileT;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const int v = tid + 128 * i;
+      const int v = ptid + 64 * i;
       const int row = v % kTileT, col = (v / kTileT) * 8;
       const uint32_t u[4] = {rx[i].x, rx[i].y, rx[i].z, rx[i].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        xb[(col + 2 * q) * kTileT + row] = bf16lo(u[q]);
-        xb[(col + 2 * q + 1) * kTileT + row] = bf16hi(u[q]);
+        const float lo = bf16lo(u[q]), hi = bf16hi(u[q]);
+        xb[(col + 2 * q) * kTileT + row] = lo;
+        xb[(col + 2 * q + 1) * kTileT + row] = hi;
+        sqacc[i] = fmaf(lo, lo, sqacc[i]);
+        sqacc[i] = fmaf(hi, hi, sqacc[i]);
       }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int v = tid + 128 * i;
+      const int v = ptid + 64 * i;
       const int row = v % kTileE, col = (v / kTileE) * 8;
       const uint32_t u[4] = {rw[i].x, rw[i].y, rw[i].z, rw[i].w};
 #pragma unroll
@@ -681,56 +678,85 @@ __global__ void __launch_bounds__(128) router_tile_kernel(
     }
   };
 
-  float tot[4][8];
+  float tot[8][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) tot[i][j] = 0.f;
 
   const int nchunks = H / kTileK;
-  load_chunk(0);
-  store_chunk(0);
-  __syncthreads();
-  for (int kc = 0; kc < nchunks; ++kc) {
-    const int buf = kc & 1;
-    if (kc + 1 < nchunks) load_chunk(kc + 1);
-    const float* xb = xs + buf * kTileK * kTileT + ty * 4;
-    // thread tx owns experts 4tx..4tx+3 and 64+4tx..64+4tx+3: a quarter-warp
-    // then reads 128 contiguous bytes per vector load (no bank conflicts)
-    const float* wb = wsm + buf * kTileK * kTileE + tx * 4;
-    float part[4][8];
+  int buf = 0;
+  if (pair < nchunks) {
+    load_chunk(pair);
+    store_chunk(0);
+  }
+  named_sync(1 + pair, 64);
+  for (int kc = pair; kc < nchunks; kc += 2) {
+    const bool more = kc + 2 < nchunks;
+    if (more) load_chunk(kc + 2);
+    const float* xb = tiles + (size_t)(pair * 2 + buf) * kTileBuf + tw;
+    const float* wb = tiles + (size_t)(pair * 2 + buf) * kTileBuf + kTileK * kTileT + ew;
+    float part[8][8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) part[i][j] = 0.f;
-#pragma unroll 8
+#pragma unroll 4
     for (int kk = 0; kk < kTileK; ++kk) {
       const float4 xa = *reinterpret_cast<const float4*>(xb + kk * kTileT);
+      const float4 xc = *reinterpret_cast<const float4*>(xb + kk * kTileT + 4);
       const float4 wa = *reinterpret_cast<const float4*>(wb + kk * kTileE);
-      const float4 wb4 = *reinterpret_cast<const float4*>(wb + kk * kTileE + 64);
-      const float xv[4] = {xa.x, xa.y, xa.z, xa.w};
-      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb4.x, wb4.y, wb4.z, wb4.w};
+      const float4 wc = *reinterpret_cast<const float4*>(wb + kk * kTileE + 64);
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wc.x, wc.y, wc.z, wc.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) tot[i][j] += part[i][j];
-    if (kc + 1 < nchunks) store_chunk(buf ^ 1);
-    __syncthreads();
+    if (more) store_chunk(buf ^ 1);
+    named_sync(1 + pair, 64);
+    buf ^= 1;
+  }
+  __syncthreads();   // both pairs are done with their tiles
+  // pair 1 hands its totals to pair 0 (through the tile memory), which adds
+  // them once and writes the logits
+  float* xfer = tiles;   // [64 threads][64]
+  if (pair == 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) xfer[(i * 8 + j) * 64 + ptid] = tot[i][j];
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
-    if (t >= T) continue;
+  for (int i = 0; i < 2; ++i) s_sq[pair][ptid + 64 * i] = sqacc[i];
+  __syncthreads();
+  if (pair == 0) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = (j < 4 ? 0 : 64) + tx * 4 + (j & 3);
-      if (e < E) logits[(size_t)t * E + e] = bias ? tot[i][j] + bias[e] : tot[i][j];
+    for (int i = 0; i < 8; ++i) {
+      const int t = t0 + tw + i;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float v = tot[i][j] + xfer[(i * 8 + j) * 64 + ptid];
+        const int e = (j < 4 ? 0 : 64) + ew + (j & 3);
+        if (t < T && e < E) logits[(size_t)t * E + e] = bias ? v + bias[e] : v;
+      }
     }
+  }
+  // ||x_t||: row t's partials are the vector slots v = t + 32c (c = 0..3) of
+  // both pairs, added in a fixed order (any order serves the error bound,
+  // which allows for the norm's own rounding)
+  if (tid < kTileT && t0 + tid < T) {
+    float sq = 0.f;
+#pragma unroll
+    for (int p2 = 0; p2 < 2; ++p2)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sq += s_sq[p2][tid + kTileT * c];
+    xnorm[t0 + tid] = sqrtf(sq);
   }
 }
 
@@ -814,11 +840,11 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
     float* logits = ws_ptr<float>(ws, L.logits);
     float* xnorm = ws_ptr<float>(ws, L.xnorm);
     wnorm_kernel<<<(E + 7) / 8, 256, 0, stream>>>(gate_w, H, E, wnorm);
-    const size_t smem = sizeof(float) * 2 * kTileK * (kTileT + kTileE);
+    const size_t smem = sizeof(float) * 4 * kTileBuf;
     cudaError_t err = cudaFuncSetAttribute(router_tile_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    router_tile_kernel<<<(T + kTileT - 1) / kTileT, 128, smem, stream>>>(x, gate_w, bias, T, H, E,
+    router_tile_kernel<<<(T + kTileT - 1) / kTileT, kTileThreads, smem, stream>>>(x, gate_w, bias, T, H, E,
                                                                          logits, xnorm);
     const size_t smem2 = sizeof(WarpScratch) * 8 + sizeof(float) * 8 * E;
     err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -38,7 +38,7 @@ def weight_bound(inp, orc_logits) -> np.ndarray:
     schemes) enters twice through the softmax ratio, plus fp32 rounding of the
     exponentials and the normalisation."""
     H = inp.H
-    n = max(H // 32 + 5, 64 + H // 64 + 1)
+    n = max(H // 32 + 5, 32 + H // 32 + 1)
     u = 2.0 ** -24
     gam = n * u / (1 - n * u)
     x = oracle.bf16_to_f64(moe_inputs.bf16_bits(inp.x))
