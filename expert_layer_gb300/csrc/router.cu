@@ -42,8 +42,8 @@ __device__ __forceinline__ double f32_as_f64(uint32_t u) {
   return __hiloint2double((int)hi, e ? (int)(u << 29) : 0);
 }
 
-// fp64 dot of two bf16 rows of length H (H % 8 == 0), whole warp; every lane
-// returns the same value (xor butterfly).  A bf16 x bf16 product has at most
+// fp64 dot of two bf16 rows over columns [h0, h1) (h0 % 256 == 0, h1 % 8 ==
+// 0), whole warp; every lane returns the same value (xor butterfly).  A bf16 x bf16 product has at most
 // 16 significant bits, so its fp32 value is exact unless it under- or
 // overflows fp32; then each exact product is added in fp64.  That is the
 // same arithmetic as an fp64 fma of the two factors, with one operation on
@@ -51,20 +51,21 @@ __device__ __forceinline__ double f32_as_f64(uint32_t u) {
 // in which any lane meets an fp32 product that is not exact goes the fp64 way
 // for the whole warp.  Four independent chains per lane.
 __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
-                               int H) {
+                               int h0, int h1) {
   const int lane = threadIdx.x & 31;
   double s[4] = {0.0, 0.0, 0.0, 0.0};
   constexpr int kB = 4;   // iterations whose loads are issued together
-  for (int hb = 0; hb < H; hb += 256 * kB) {
+  for (int hb = h0; hb < h1; hb += 256 * kB) {
    uint4 va4[kB], vb4[kB];
 #pragma unroll
    for (int it = 0; it < kB; ++it) {
      const int h = hb + lane * 8 + 256 * it;
-     va4[it] = h < H ? *reinterpret_cast<const uint4*>(a + h) : make_uint4(0, 0, 0, 0);
-     vb4[it] = h < H ? *reinterpret_cast<const uint4*>(b + h) : make_uint4(0, 0, 0, 0);
+     va4[it] = h < h1 ? *reinterpret_cast<const uint4*>(a + h) : make_uint4(0, 0, 0, 0);
+     vb4[it] = h < h1 ? *reinterpret_cast<const uint4*>(b + h) : make_uint4(0, 0, 0, 0);
    }
 #pragma unroll
    for (int it = 0; it < kB; ++it) {
+    if (hb + 256 * it >= h1) break;   // whole warp: past the range
     const uint4 va = va4[it], vb = vb4[it];
     const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
@@ -284,24 +285,51 @@ __device__ void select_begin(int E, int k, float delta, int end, WarpScratch& sc
   __syncwarp();
 }
 
-// fp64 logits listed by select_begin for the tokens t0 .. t0+nt-1 (scratch
-// scr[0..nt)), one warp per logit, spread over all warps of the block.
+// The fp64 logits listed by select_begin for the tokens t0 .. t0+nt-1
+// (scratch scr[0..nt)), shared by all warps of the block.  Each dot is split
+// into kDotParts slices of its 256-column blocks, one warp per slice, so that
+// one dot keeps the fp64 pipes of all four SM sub-partitions busy (warps w .. w+3 sit on different
+// sub-partitions); the slice sums are added in slice order.  s_part holds one
+// double per warp.  Called by every thread of the block.
+constexpr int kDotParts = 4;
+
+__device__ void dot_target(const WarpScratch* scr, int j, int& tt, int& r, int& e) {
+  tt = 0;
+  r = j;
+  while (r >= scr[tt].nd) { r -= scr[tt].nd; ++tt; }
+  e = scr[tt].end < 0 ? r : scr[tt].cand_e[scr[tt].dpos[r]];
+}
+
 __device__ void select_dots(WarpScratch* scr, int nt, int t0, const uint16_t* x,
-                            const uint16_t* gate_w, const float* bias, int H, int E, double* l64) {
+                            const uint16_t* gate_w, const float* bias, int H, int E, double* l64,
+                            double* s_part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int per = nw / kDotParts;   // dots per round
+  const int nb = (H + 255) / 256;
   int total = 0;
   for (int tt = 0; tt < nt; ++tt) total += scr[tt].nd;
-  for (int j = warp; j < total; j += nw) {
-    int tt = 0, r = j;
-    while (r >= scr[tt].nd) { r -= scr[tt].nd; ++tt; }
-    WarpScratch& sc = scr[tt];
-    const int e = sc.end < 0 ? r : sc.cand_e[sc.dpos[r]];
-    double d = warp_dot_f64(x + (size_t)(t0 + tt) * H, gate_w + (size_t)e * H, H);
-    if (bias) d += (double)bias[e];
-    if (lane == 0) {
-      if (sc.end < 0) l64[(size_t)(t0 + tt) * E + e] = d;
-      else sc.key[sc.dpos[r]] = d;
+  for (int base = 0; base < total; base += per) {   // uniform trip count
+    const int j = base + warp / kDotParts, q = warp % kDotParts;
+    double d = 0.0;
+    if (j < total) {
+      int tt, r, e;
+      dot_target(scr, j, tt, r, e);
+      const int h0 = 256 * (q * nb / kDotParts), h1 = min(H, 256 * ((q + 1) * nb / kDotParts));
+      d = warp_dot_f64(x + (size_t)(t0 + tt) * H, gate_w + (size_t)e * H, h0, h1);
     }
+    if (lane == 0) s_part[warp] = d;
+    __syncthreads();
+    if (lane == 0 && warp < per && base + warp < total) {
+      int tt, r, e;
+      dot_target(scr, base + warp, tt, r, e);
+      const double* p = s_part + kDotParts * warp;
+      double v = (p[0] + p[1]) + (p[2] + p[3]);
+      if (bias) v += (double)bias[e];
+      WarpScratch& sc = scr[tt];
+      if (sc.end < 0) l64[(size_t)(t0 + tt) * E + e] = v;
+      else sc.key[sc.dpos[r]] = v;
+    }
+    __syncthreads();
   }
 }
 
@@ -365,26 +393,44 @@ __device__ void select_end(int E, int k, WarpScratch& sc, const double* l64_row,
 }
 
 // ------------------------------------------------------------ small batches
-// Grid (ceil(T / kTT), ceil(E / 16)), 16 warps: warp w of CTA (c, y) computes
-// the logits of expert 16y + w for the kTT tokens of chunk c, reading the gate
-// row once.  Lane l sums the products at h = 8l + 256j + (0..7) sequentially
-// (H/32 terms), then a 5-level xor tree: at most H/32 + 4 roundings per
-// product.  Warp 0 of the y = 0 CTAs also writes ||x_t||.  The last CTA to
-// finish a chunk (integer counter, no waiting) ranks every (token, expert)
-// of the chunk by counting, all threads at once, and then selects each
-// token's top-k with one warp per token.  With kGroup, the CTA that selects
-// the batch's last tokens then groups all routed slots (grouping.cuh) in the
-// same launch.
+// Grid (ceil(T / kTT), ceil(E / (16 kEPW))), 16 warps: warp w of CTA (c, y)
+// computes the logits of kEPW experts (16y + w for kTT = 1; 32y + 2w, +1 for
+// chunks of 4 or 8 tokens) for the kTT tokens of chunk c, holding its gate
+// rows in registers.  Lane l sums the products at h = 8l + 256j + (0..7)
+// sequentially (H/32 terms), then a 5-level xor tree: at most H/32 + 4
+// roundings per product.  With kTT = 1 the warp reads the token row from
+// global memory; larger chunks first stage the chunk's token rows (2048
+// columns at a time) in shared memory, so each warp's token loads are
+// shared-memory reads.  Warps w < #tokens of the y = 0 CTAs also write
+// ||x_t||.  The last CTA to finish a chunk (integer counter, no waiting)
+// orders each token's experts: one warp per token extracting in rank order
+// (chunks of 4 or 8 tokens, E <= 128), or all threads ranking every
+// (token, expert) by counting (one-token chunks, or E > 128); then one warp
+// per token selects.  With kGroup, the CTA that selects the batch's last
+// tokens then groups all routed slots (grouping.cuh) in the same launch.
 constexpr int kSmallWarps = 16;
+constexpr int kXCols = 2048;   // token-row columns staged per block
 
-// Shared memory of the small router: grouping scratch (kGroup) then, for the
-// selecting CTA, the chunk's logits [tt][E], ||w_e|| [E] and ||x_t|| [tt].
+template <int kTT>
+struct SmallCfg {
+  static constexpr int kEPW = kTT >= 4 ? 2 : 1;            // experts per warp
+  static constexpr int kExperts = kSmallWarps * kEPW;     // experts per CTA
+  static constexpr bool kStaged = kTT >= 4;                // token rows in shared memory
+};
+
+// Shared memory of the small router: grouping scratch (kGroup); for the
+// selecting CTA, the chunk's sort keys [tt][E], logits [tt][E], ||w_e|| [E]
+// and ||x_t|| [tt]; then (staged chunks) the token rows [tt][kXCols] bf16.
 __host__ __device__ inline size_t router_small_group_ints(int E, int S, bool group) {
   return group ? grouping::single_block_smem_ints(E, S) : 0;
 }
-__host__ __device__ inline size_t router_small_smem(int E, int S, int tt, bool group) {
+__host__ __device__ inline size_t router_small_select_bytes(int E, int S, int tt, bool group) {
   return sizeof(int) * router_small_group_ints(E, S, group) + sizeof(uint64_t) * (size_t)tt * E +
          sizeof(float) * ((size_t)(tt + 1) * E + tt);
+}
+__host__ __device__ inline size_t router_small_smem(int E, int S, int tt, bool group) {
+  const size_t sel = (router_small_select_bytes(E, S, tt, group) + 15) & ~size_t(15);
+  return tt >= 4 ? sel + sizeof(uint16_t) * (size_t)tt * kXCols : sel;
 }
 
 // Release-acquire integer add at GPU scope: the caller's earlier writes (and
@@ -396,14 +442,47 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
   return old;
 }
 
+// c + a.lo * b.lo, then + a.hi * b.hi: two fp32 fmas whose factors are the
+// bf16 halves of a and b (each product exact, one rounding per fma).
+__device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float c) {
+  asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+      " fma.rn.f32.bf16 %0, al, bl, %0;\n fma.rn.f32.bf16 %0, ah, bh, %0;\n}"
+      : "+f"(c)
+      : "r"(a), "r"(b));
+  return c;
+}
+
+// Token rows t0 .. t0+kTT-1, columns [hb, hb + kXCols), into xs (zero past the
+// chunk's tokens or past H).  All loads are issued before the stores.
+template <int kTT>
+__device__ __forceinline__ void stage_tokens(const uint16_t* __restrict__ x, int t0, int nt, int H,
+                                             int hb, uint16_t* xs) {
+  constexpr int kRowVecs = kXCols / 8;
+  constexpr int kPer = kTT * kRowVecs / (kSmallWarps * 32);
+  static_assert(kTT * kRowVecs % (kSmallWarps * 32) == 0, "whole vectors per thread");
+  uint4 v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int q = threadIdx.x + i * kSmallWarps * 32;
+    const int tt = q / kRowVecs, h = hb + (q % kRowVecs) * 8;
+    v[i] = (tt < nt && h < H) ? *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + h)
+                              : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) reinterpret_cast<uint4*>(xs)[threadIdx.x + i * kSmallWarps * 32] = v[i];
+}
+
 template <int kTT, bool kGroup>
 __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
     int T, int H, int E, int k, int gamma_terms, float* __restrict__ logits,
     float* __restrict__ wnorm, float* __restrict__ xnorm, double* __restrict__ l64,
     int* __restrict__ cnt, int32_t* __restrict__ idx, float* __restrict__ w, void* ws, GroupOut go) {
+  using Cfg = SmallCfg<kTT>;
+  constexpr int kEPW = Cfg::kEPW;
   extern __shared__ __align__(16) int dsm[];
   __shared__ WarpScratch scr[kTT];
+  __shared__ double s_part[kSmallWarps];
   __shared__ int s_last, s_group;
   __shared__ int4 sw[grouping::kWarps];
   pdl_wait();      // the workspace counters are cleared
@@ -412,97 +491,112 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
   const int chunk = blockIdx.x;
   const int t0 = chunk * kTT;
   const int nt = min(kTT, T - t0);
-  const int e = blockIdx.y * kSmallWarps + warp;
+  const int e0 = blockIdx.y * Cfg::kExperts + warp * kEPW;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  if (e < E) {
-    float acc[kTT], sq = 0.f;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(
+      reinterpret_cast<unsigned char*>(dsm) +
+      ((router_small_select_bytes(E, T * k, kTT, kGroup) + 15) & ~size_t(15)));
+  const bool xn_warp = blockIdx.y == 0 && warp < nt;   // this warp writes ||x_{t0+warp}||
+  float acc[kEPW][kTT], sq[kEPW], sqx = 0.f;
 #pragma unroll
-    for (int tt = 0; tt < kTT; ++tt) acc[tt] = 0.f;
-    const uint16_t* wr = gw + (size_t)e * H;
-    for (int hb = 0; hb < H; hb += 2048) {
-      uint4 wv[8];
+  for (int ep = 0; ep < kEPW; ++ep) {
+    sq[ep] = 0.f;
+#pragma unroll
+    for (int tt = 0; tt < kTT; ++tt) acc[ep][tt] = 0.f;
+  }
+  for (int hb = 0; hb < H; hb += 2048) {
+    uint4 wv[kEPW][8];
+#pragma unroll
+    for (int ep = 0; ep < kEPW; ++ep)
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         const int h = hb + lane * 8 + 256 * v;
-        wv[v] = h < H ? ldg_nc_v4(wr + h) : make_uint4(0, 0, 0, 0);
+        wv[ep][v] = (e0 + ep < E && h < H) ? ldg_nc_v4(gw + (size_t)(e0 + ep) * H + h)
+                                           : make_uint4(0, 0, 0, 0);
       }
+    if constexpr (Cfg::kStaged) {
+      if (hb > 0) __syncthreads();   // every warp is done with the previous block
+      stage_tokens<kTT>(x, t0, nt, H, hb, xs);
+      __syncthreads();
+    }
+#pragma unroll
+    for (int ep = 0; ep < kEPW; ++ep)
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
-        const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
+        const uint32_t ww[4] = {wv[ep][v].x, wv[ep][v].y, wv[ep][v].z, wv[ep][v].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          sq = fmaf(bf16lo(ww[i]), bf16lo(ww[i]), sq);
-          sq = fmaf(bf16hi(ww[i]), bf16hi(ww[i]), sq);
+          sq[ep] = fmaf(bf16lo(ww[i]), bf16lo(ww[i]), sq[ep]);
+          sq[ep] = fmaf(bf16hi(ww[i]), bf16hi(ww[i]), sq[ep]);
         }
       }
-      // token rows two at a time, all loads of a pair issued before its
-      // products (rows past the chunk read as zero and are never stored)
-      constexpr int kPair = kTT < 2 ? kTT : 2;
+    if constexpr (Cfg::kStaged) {
+      const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
 #pragma unroll
-      for (int tp = 0; tp < kTT; tp += kPair) {
-        uint4 xv[kPair][8];
+      for (int tt = 0; tt < kTT; ++tt) {
 #pragma unroll
-        for (int u = 0; u < kPair; ++u) {
-          const uint16_t* xr = x + (size_t)(t0 + tp + u) * H;
+        for (int v = 0; v < 8; ++v) {
+          const uint4 xv = xs4[tt * (kXCols / 8) + lane + 32 * v];
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const int h = hb + lane * 8 + 256 * v;
-            xv[u][v] = (tp + u < nt && h < H) ? *reinterpret_cast<const uint4*>(xr + h)
-                                              : make_uint4(0, 0, 0, 0);
-          }
-        }
+          for (int ep = 0; ep < kEPW; ++ep) {
+            const uint32_t ww[4] = {wv[ep][v].x, wv[ep][v].y, wv[ep][v].z, wv[ep][v].w};
 #pragma unroll
-        for (int u = 0; u < kPair; ++u) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint32_t xw[4] = {xv[u][v].x, xv[u][v].y, xv[u][v].z, xv[u][v].w};
-            const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              acc[tp + u] = fmaf(bf16lo(xw[i]), bf16lo(ww[i]), acc[tp + u]);
-              acc[tp + u] = fmaf(bf16hi(xw[i]), bf16hi(ww[i]), acc[tp + u]);
-            }
+            for (int i = 0; i < 4; ++i) acc[ep][tt] = fma_bf16x2(xw[i], ww[i], acc[ep][tt]);
           }
         }
       }
-    }
+      if (xn_warp) {   // ||x_t||^2 from the staged row, same order as the products
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        for (int v = 0; v < 8; ++v) {
+          const uint4 xv = xs4[warp * (kXCols / 8) + lane + 32 * v];
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-      for (int tt = 0; tt < kTT; ++tt) acc[tt] += __shfl_xor_sync(0xffffffffu, acc[tt], o);
-    }
-    float mine = acc[0];
-#pragma unroll
-    for (int tt = 1; tt < kTT; ++tt) if (lane == tt) mine = acc[tt];
-    if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = bias ? mine + bias[e] : mine;
-    if (lane == 31) wnorm[e] = sqrtf(sq);   // the same value from every chunk's CTA
-  }
-  if (blockIdx.y == 0 && warp < nt) {
-    // ||x_t|| of token t0 + warp (a row just read, mostly cache hits)
-    const uint16_t* xr = x + (size_t)(t0 + warp) * H;
-    float sqx = 0.f;
-    for (int hb = 0; hb < H; hb += 2048) {
+          for (int i = 0; i < 4; ++i) sqx = fma_bf16x2(xw[i], xw[i], sqx);
+        }
+      }
+    } else {
+      // one token: its row straight from global memory
       uint4 xv[8];
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         const int h = hb + lane * 8 + 256 * v;
-        xv[v] = h < H ? *reinterpret_cast<const uint4*>(xr + h) : make_uint4(0, 0, 0, 0);
+        xv[v] = (nt > 0 && h < H) ? *reinterpret_cast<const uint4*>(x + (size_t)t0 * H + h)
+                                  : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         const uint32_t xw[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
+        const uint32_t ww[4] = {wv[0][v].x, wv[0][v].y, wv[0][v].z, wv[0][v].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          sqx = fmaf(bf16lo(xw[i]), bf16lo(xw[i]), sqx);
-          sqx = fmaf(bf16hi(xw[i]), bf16hi(xw[i]), sqx);
+          acc[0][0] = fma_bf16x2(xw[i], ww[i], acc[0][0]);
+          if (xn_warp) sqx = fma_bf16x2(xw[i], xw[i], sqx);
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
-    if (lane == 0) xnorm[t0 + warp] = sqrtf(sqx);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
+#pragma unroll
+    for (int ep = 0; ep < kEPW; ++ep) {
+      sq[ep] += __shfl_xor_sync(0xffffffffu, sq[ep], o);
+#pragma unroll
+      for (int tt = 0; tt < kTT; ++tt) acc[ep][tt] += __shfl_xor_sync(0xffffffffu, acc[ep][tt], o);
+    }
+  }
+#pragma unroll
+  for (int ep = 0; ep < kEPW; ++ep) {
+    const int e = e0 + ep;
+    if (e >= E) continue;
+    float mine = acc[ep][0];
+#pragma unroll
+    for (int tt = 1; tt < kTT; ++tt) if (lane == tt) mine = acc[ep][tt];
+    if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = bias ? mine + bias[e] : mine;
+    if (lane == 31) wnorm[e] = sqrtf(sq[ep]);   // the same value from every chunk's CTA
+  }
+  if (xn_warp && lane == 0) xnorm[t0 + warp] = sqrtf(sqx);
   // Publish the CTA's results and count the CTA in; the last CTA of the
   // chunk sees every other CTA's results.
   __syncthreads();
@@ -512,6 +606,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
 
   // ---- last CTA of the chunk: stage logits, ||w_e||, ||x_t|| (one L2 trip)
   // (the grouping scratch is an even number of ints: the keys are 8-byte aligned)
+  const bool by_warp = kTT >= 4 && E <= 128;   // extraction in rank order, one warp per token
   uint64_t* skey = reinterpret_cast<uint64_t*>(dsm + router_small_group_ints(E, T * k, kGroup));
   float* sl = reinterpret_cast<float*>(skey + (size_t)kTT * E);
   float* swn = sl + (size_t)kTT * E;
@@ -522,34 +617,36 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     const float v = __ldcg(logits + (size_t)t0 * E + i);
     sl[i] = v;
     const uint32_t e = (uint32_t)(i % E);
-    skey[i] = ((uint64_t)order_bits(rank_key(v)) << 32) | (uint64_t)(0xffffffffu - e);
+    if (!by_warp) skey[i] = ((uint64_t)order_bits(rank_key(v)) << 32) | (uint64_t)(0xffffffffu - e);
   }
   for (int i = threadIdx.x; i < E; i += blockDim.x) swn[i] = __ldcg(wnorm + i);
   if (threadIdx.x < nt) sxn[threadIdx.x] = __ldcg(xnorm + t0 + threadIdx.x);
   __syncthreads();
-  // Rank of every (token, expert) by counting the experts ahead of it:
-  // larger logit first, lower index first on equal logits, NaN last.  Four
-  // threads share an expert, thread q counting over j = q (mod 4).
-  for (int tt = 0; tt < nt; ++tt) {
-    const uint64_t* krow = skey + (size_t)tt * E;
-    for (int base = 0; base < 4 * E; base += blockDim.x) {   // uniform trip count
-      const int it = base + threadIdx.x;
-      const int q = it & 3, ee = it >> 2;
-      int r = 0;
-      if (ee < E) {
-        const uint64_t key = krow[ee];
+  if (!by_warp) {
+    // Rank of every (token, expert) by counting the experts ahead of it:
+    // larger logit first, lower index first on equal logits, NaN last.  Four
+    // threads share an expert, thread q counting over j = q (mod 4).
+    for (int tt = 0; tt < nt; ++tt) {
+      const uint64_t* krow = skey + (size_t)tt * E;
+      for (int base = 0; base < 4 * E; base += blockDim.x) {   // uniform trip count
+        const int it = base + threadIdx.x;
+        const int q = it & 3, ee = it >> 2;
+        int r = 0;
+        if (ee < E) {
+          const uint64_t key = krow[ee];
 #pragma unroll 8
-        for (int j = q; j < E; j += 4) r += krow[j] > key ? 1 : 0;
-      }
-      r += __shfl_xor_sync(0xffffffffu, r, 1);
-      r += __shfl_xor_sync(0xffffffffu, r, 2);
-      if (ee < E && q == 0 && r < kCandCap) {
-        scr[tt].cand_e[r] = ee;
-        scr[tt].cand_v[r] = rank_key(sl[(size_t)tt * E + ee]);
+          for (int j = q; j < E; j += 4) r += krow[j] > key ? 1 : 0;
+        }
+        r += __shfl_xor_sync(0xffffffffu, r, 1);
+        r += __shfl_xor_sync(0xffffffffu, r, 2);
+        if (ee < E && q == 0 && r < kCandCap) {
+          scr[tt].cand_e[r] = ee;
+          scr[tt].cand_v[r] = rank_key(sl[(size_t)tt * E + ee]);
+        }
       }
     }
+    __syncthreads();
   }
-  __syncthreads();
 
   if (warp < nt) {
     const int t = t0 + warp;
@@ -567,15 +664,15 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     }
     const float delta = gamma_bound(gamma_terms) * sxn[warp] * wmax * (1.0f + 0x1p-10f) +
                         0x1p-22f * lmax + (float)H * 0x1p-149f;
-    const int end = certain_end_ranked(sc, E, k, cert_threshold(delta));
+    const float thr = cert_threshold(delta);
+    const int end = by_warp ? extract_small(row, E, k, thr, sc) : certain_end_ranked(sc, E, k, thr);
     select_begin(E, k, delta, end, sc, idx + (size_t)t * k, w + (size_t)t * k, hdr);
   }
   __syncthreads();
   int ndots = 0;
   for (int tt = 0; tt < nt; ++tt) ndots += scr[tt].nd;
   if (ndots > 0) {   // uniform over the block
-    select_dots(scr, nt, t0, x, gw, bias, H, E, l64);
-    __syncthreads();
+    select_dots(scr, nt, t0, x, gw, bias, H, E, l64, s_part);
     if (warp < nt && scr[warp].nd > 0)
       select_end(E, k, scr[warp], l64 + (size_t)(t0 + warp) * E, idx + (size_t)(t0 + warp) * k,
                  w + (size_t)(t0 + warp) * k);
@@ -767,6 +864,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     const float* __restrict__ xnorm, const float* __restrict__ wnorm, double* __restrict__ l64,
     int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ double s_part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem_raw);
   float* sl = reinterpret_cast<float*>(smem_raw + sizeof(WarpScratch) * 8) + (size_t)warp * E;
@@ -797,8 +895,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
   int ndots = 0;
   for (int tt = 0; tt < nt; ++tt) ndots += scr[tt].nd;
   if (ndots == 0) return;   // uniform over the block
-  select_dots(scr, nt, t0, x, gw, bias, H, E, l64);
-  __syncthreads();
+  select_dots(scr, nt, t0, x, gw, bias, H, E, l64, s_part);
   if (warp < nt && scr[warp].nd > 0)
     select_end(E, k, scr[warp], l64 + (size_t)t * E, idx + (size_t)t * k, w + (size_t)t * k);
 }
@@ -860,7 +957,8 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
   const int tt = T <= 16 ? 1 : T <= 128 ? 4 : 8;
   const size_t smem = router_small_smem(E, T * k, tt, grp);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)((T + tt - 1) / tt), (unsigned)((E + kSmallWarps - 1) / kSmallWarps));
+  const int per_cta = tt >= 4 ? SmallCfg<4>::kExperts : SmallCfg<1>::kExperts;
+  const dim3 grid((unsigned)((T + tt - 1) / tt), (unsigned)((E + per_cta - 1) / per_cta));
   int* cnt = ws_ptr<int>(ws, L.cnt);
   float* logits = ws_ptr<float>(ws, L.logits);
   float* xnorm = ws_ptr<float>(ws, L.xnorm);
