@@ -124,81 +124,88 @@ __device__ void finish_scan(const int* s_counts, int E, int S, int large_thresho
 constexpr int kSingleMaxChunks = 8;
 constexpr int kSingleMaxSlots = kSingleMaxChunks * kThreads;
 
-// Dynamic shared memory (ints) that group_single_block needs for S slots.
+// Dynamic shared memory (ints) that group_single_block needs (an even number).
 __host__ __device__ inline size_t single_block_smem_ints(int E, int S) {
-  return (size_t)E * (2 + kWarps) + 2 * (size_t)S;
+  (void)S;
+  return (size_t)E * (2 + kWarps);
 }
 
-// The whole grouping for S <= kSingleMaxSlots slots in one 512-thread block.
+// The whole grouping for S <= kSingleMaxSlots slots in one 512-thread block,
+// with few block barriers (this often runs alone on one SM at the end of the
+// router, where every barrier and every cold instruction line is latency).
+// Warp w owns the contiguous slice of slots [w*L, (w+1)*L), L a multiple of
+// 32, and walks it in rounds of 32 ascending slots: __match_any gives each
+// slot its rank among equal experts in the round, and the warp's own table
+// row tab[w][e] (read and advanced by each group's first lane) adds the
+// earlier rounds.  A scan down the warps per expert then gives each warp's
+// base, the expert offsets come from finish_scan, and position = offset[e] +
+// base[w][e] + rank in the slice: ascending slot order within every expert.
 // `dyn` holds single_block_smem_ints(E, S) ints, `sw` kWarps int4.
 // `zero`/`nzero`: an int region cleared on the way (counters used later in
-// the same call).  Every slot id is read once into shared memory; slot f of
-// chunk c (f = 512c + thread) gets its rank among equal experts from the
-// chunk's stable rank plus the running per-expert count of the earlier
-// chunks, and its position adds the expert's offset once all counts are
-// known.  The chunk loop is kept rolled: this code often runs once, on one
-// SM, where every extra instruction line is fetched cold.
+// the same call).
 __device__ void group_single_block(const int32_t* __restrict__ idx, int S, int E,
                                    int large_threshold, int tile_rows, int32_t* counts,
                                    int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                                    int32_t* active, int32_t* tiles, void* ws, int* dyn, int4* sw,
                                    int* zero, int nzero) {
-  int* s_cnt = dyn;              // [E] running counts, then totals
+  int* s_cnt = dyn;              // [E] totals
   int* s_off = s_cnt + E;        // [E] offsets
-  int* tab = s_off + E;          // [kWarps][E]
-  int* s_e = tab + kWarps * E;   // [S] expert of each slot
-  int* s_rel = s_e + S;          // [S] rank of each slot within its expert
+  int* tab = s_off + E;          // [kWarps][E] per-warp counts, then bases
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  const int warp = threadIdx.x >> 5;
-  {
-    int ev[kSingleMaxChunks];    // all loads in flight before the first store
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rounds = (S + kThreads - 1) / kThreads;   // <= kSingleMaxChunks
+  const int f0 = warp * rounds * 32 + lane;           // slot of round 0
+  int ev[kSingleMaxChunks];      // all loads in flight before any use
 #pragma unroll
-    for (int c = 0; c < kSingleMaxChunks; ++c) {
-      const int f = c * kThreads + threadIdx.x;
-      ev[c] = f < S ? __ldcg(&idx[f]) : -1;
-    }
-#pragma unroll
-    for (int c = 0; c < kSingleMaxChunks; ++c) {
-      const int f = c * kThreads + threadIdx.x;
-      if (f < S) s_e[f] = ev[c];
-    }
+  for (int r = 0; r < kSingleMaxChunks; ++r) {
+    const int f = f0 + 32 * r;
+    ev[r] = (r < rounds && f < S) ? __ldcg(&idx[f]) : -1;
   }
   for (int i = threadIdx.x; i < nzero; i += kThreads) zero[i] = 0;
-  for (int e = threadIdx.x; e < E; e += kThreads) s_cnt[e] = 0;
+  int* row = tab + warp * E;
+  for (int e = lane; e < E; e += 32) row[e] = 0;
+  __syncwarp();
   bool bad = false;
-#pragma unroll 1
-  for (int c0 = 0; c0 < S; c0 += kThreads) {
-    const int f = c0 + threadIdx.x;
-    const int e = f < S ? s_e[f] : -1;
+  int rel[kSingleMaxChunks];
+#pragma unroll
+  for (int r = 0; r < kSingleMaxChunks; ++r) {
+    rel[r] = -1;
+    if (r >= rounds) continue;   // uniform over the block
+    const int f = f0 + 32 * r;
+    const int e = ev[r];
     const bool valid = e >= 0 && e < E;
     if (f < S && !valid) bad = true;
-    if (c0 > 0) __syncthreads();   // every thread has read the previous chunk's ranks
-    for (int i = threadIdx.x; i < kWarps * E; i += kThreads) tab[i] = 0;
-    __syncthreads();
     const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
-    const int r = __popc(peers & lanemask_lt());
-    if (valid && r == 0) tab[warp * E + e] = __popc(peers);
-    __syncthreads();
-    for (int ee = threadIdx.x; ee < E; ee += kThreads) {
-      int s = s_cnt[ee];
-      for (int w = 0; w < kWarps; ++w) {
-        const int cw = tab[w * E + ee];
-        tab[w * E + ee] = s;
-        s += cw;
-      }
-      s_cnt[ee] = s;
+    const int first = __ffs(peers) - 1;
+    int before = 0;
+    if (valid && lane == first) {
+      before = row[e];
+      row[e] = before + __popc(peers);
     }
-    __syncthreads();
-    if (f < S) s_rel[f] = valid ? tab[warp * E + e] + r : -1;
+    before = __shfl_sync(0xffffffffu, before, first);
+    if (valid) rel[r] = before + __popc(peers & lanemask_lt());
+    __syncwarp();   // the table row is read again in the next round
   }
   if (bad) set_status(ws, kStatusBadExpert);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    int s = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = tab[w * E + e];
+      tab[w * E + e] = s;
+      s += c;
+    }
+    s_cnt[e] = s;
+  }
+  __syncthreads();
   finish_scan(s_cnt, E, S, large_threshold, tile_rows, counts, offsets, active, tiles, hdr, s_off,
               sw);
   __syncthreads();
-  for (int f = threadIdx.x; f < S; f += kThreads) {
-    const int rel = s_rel[f];
-    if (rel < 0) continue;
-    const int pos = s_off[s_e[f]] + rel;
+#pragma unroll
+  for (int r = 0; r < kSingleMaxChunks; ++r) {
+    if (rel[r] < 0) continue;
+    const int f = f0 + 32 * r;
+    const int pos = s_off[ev[r]] + row[ev[r]] + rel[r];
     perm[pos] = f;
     inv_perm[f] = pos;
   }

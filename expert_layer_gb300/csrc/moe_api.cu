@@ -199,8 +199,15 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   // Experts with at least `large` rows go to the tensor-core kernels (bf16
   // weights, H a multiple of their 256-wide output tiles); a group can never
   // exceed T rows, so small batches skip them.
-  const int large = (long long)T * top_k >= 8192 ? kLargeGroupPrefill : kLargeGroupDecode;
+  const bool prefill = (long long)T * top_k >= 8192;
+  const int large = prefill ? kLargeGroupPrefill : kLargeGroupDecode;
   const bool use_tc = !nvfp4 && T >= large && H % 256 == 0;
+  // At prefill sizes every group goes to the tensor-core kernels: a 128-row
+  // tile of a small group costs the whole GPU about 0.7 us of tensor time,
+  // less than streaming that expert's 9.4 MB of weights, and the streaming
+  // kernel is then not launched at all.
+  const bool tc_all = use_tc && prefill;
+  const int large_threshold = tc_all ? 1 : use_tc ? large : INT_MAX;
   // Small batches fuse the grouping into the router.
   const bool fuse = !use_tc && route_can_group(T, E, top_k);
 
@@ -209,7 +216,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   if (launches) *launches += 1;
   if (fuse) {
     GroupOut go{counts, offsets, perm, inv_perm, ws_ptr<int32_t>(workspace, L.active),
-                ws_ptr<int32_t>(workspace, L.tiles), INT_MAX, kTcRows, nullptr, 0};
+                ws_ptr<int32_t>(workspace, L.tiles), large_threshold, kTcRows, nullptr, 0};
     MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches, &go));
     MOE_TRY_CUDA(mark(1));
     MOE_TRY_CUDA(mark(2));
@@ -218,7 +225,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
                               nullptr));
     MOE_TRY_CUDA(mark(1));
     MOE_TRY_CUDA(launch_permute(idx, T, E, top_k, counts, offsets, perm, inv_perm, workspace, L,
-                                use_tc ? large : INT_MAX, kTcRows, s, launches));
+                                large_threshold, kTcRows, s, launches));
     MOE_TRY_CUDA(mark(2));
   }
 
@@ -252,7 +259,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   tc.h = a.h; tc.partial = a.partial; tc.partial_f32 = L.partial_f32;
   tc.status = &hdr->status; tc.num_sms = num_sms;
 
-  MOE_TRY_CUDA(launch_stream_gemm(a, s, launches));
+  if (!tc_all) MOE_TRY_CUDA(launch_stream_gemm(a, s, launches));
   MOE_TRY_CUDA(mark(3));
   if (use_tc) {
     MOE_TRY_CUDA(launch_tc_gemm(tc, false, s, launches));

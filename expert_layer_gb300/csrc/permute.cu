@@ -35,6 +35,9 @@ __global__ void __launch_bounds__(kThreads) permute_single_kernel(
 }
 
 // ---------------------------------------------------------------- many blocks
+// Largest dynamic shared memory of the scan kernel's staged path.
+constexpr size_t kScanSmemMax = 160 * 1024;
+
 __global__ void __launch_bounds__(kThreads) permute_block_rank_kernel(
     const int32_t* __restrict__ idx, int S, int E, int32_t* __restrict__ blk_cnt,
     int32_t* __restrict__ lrank, void* ws) {
@@ -48,29 +51,51 @@ __global__ void __launch_bounds__(kThreads) permute_block_rank_kernel(
   if (f < S) lrank[f] = r;
 }
 
+// One block.  When the per-block counts fit in shared memory (`staged`) they
+// are read there with coalesced loads first, so the per-expert walks over the
+// blocks run on shared memory instead of one global load after another.
 __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
     const int32_t* __restrict__ blk_cnt, int nblk, int S, int E, int large_threshold,
     int tile_rows, int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ active, int32_t* __restrict__ tiles,
-    void* ws) {
+    void* ws, int staged) {
   extern __shared__ int smem[];
   int* s_cnt = smem;       // [E]
   int* s_off = s_cnt + E;  // [E]
+  int* s_blk = s_off + E;  // [nblk][E] when staged
   __shared__ int4 sw[kWarps];
+  const size_t n = (size_t)nblk * E;
+  if (staged)
+    for (size_t i = threadIdx.x; i < n; i += kThreads) s_blk[i] = __ldcg(&blk_cnt[i]);
+  __syncthreads();
+  const int32_t* src = staged ? s_blk : blk_cnt;
   for (int e = threadIdx.x; e < E; e += kThreads) {
     int s = 0;
-    for (int b = 0; b < nblk; ++b) s += blk_cnt[(size_t)b * E + e];
+    for (int b = 0; b < nblk; ++b) s += src[(size_t)b * E + e];
     s_cnt[e] = s;
   }
   __syncthreads();
   finish_scan(s_cnt, E, S, large_threshold, tile_rows, counts, offsets, active, tiles,
               reinterpret_cast<WsHeader*>(ws), s_off, sw);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kThreads) {
-    int s = s_off[e];
-    for (int b = 0; b < nblk; ++b) {
-      blk_base[(size_t)b * E + e] = s;
-      s += blk_cnt[(size_t)b * E + e];
+  if (staged) {
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+      int s = s_off[e];
+      for (int b = 0; b < nblk; ++b) {
+        const int c = s_blk[(size_t)b * E + e];
+        s_blk[(size_t)b * E + e] = s;
+        s += c;
+      }
+    }
+    __syncthreads();
+    for (size_t i = threadIdx.x; i < n; i += kThreads) blk_base[i] = s_blk[i];
+  } else {
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+      int s = s_off[e];
+      for (int b = 0; b < nblk; ++b) {
+        blk_base[(size_t)b * E + e] = s;
+        s += blk_cnt[(size_t)b * E + e];
+      }
     }
   }
 }
@@ -116,9 +141,15 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* cou
   if (err != cudaSuccess) return err;
   if (launches) *launches += 3;
   permute_block_rank_kernel<<<L.nblk, kThreads, smem_tab, stream>>>(idx, S, E, blk_cnt, lrank, ws);
-  permute_scan_kernel<<<1, kThreads, sizeof(int) * 2 * E, stream>>>(
+  const size_t scan_smem_staged = sizeof(int) * (2 * (size_t)E + (size_t)L.nblk * E);
+  const int staged = scan_smem_staged <= kScanSmemMax ? 1 : 0;
+  const size_t scan_smem = staged ? scan_smem_staged : sizeof(int) * 2 * (size_t)E;
+  err = cudaFuncSetAttribute(permute_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)scan_smem);
+  if (err != cudaSuccess) return err;
+  permute_scan_kernel<<<1, kThreads, scan_smem, stream>>>(
       blk_cnt, L.nblk, S, E, large_threshold, tile_rows, blk_base, counts, offsets, active, tiles,
-      ws);
+      ws, staged);
   permute_scatter_kernel<<<L.nblk, kThreads, 0, stream>>>(idx, S, E, blk_base, lrank, perm,
                                                           inv_perm);
   return cudaGetLastError();

@@ -51,6 +51,9 @@ SMALL_CASES = {
     "tc_all": dict(T=512, H=256, E=8, k=2, I=128),
     "tc_mixed": dict(T=300, H=512, E=16, k=2, I=256, bias="zipf"),
     "tc_ragged": dict(T=200, H=256, E=2, k=1, I=384),
+    # prefill-sized batch (T*k >= 8192): every group, down to a few rows, on
+    # the tensor-core kernels, with the multi-block grouping
+    "tc_prefill_small_groups": dict(T=1024, H=256, E=512, k=8, I=128, bias="zipf"),
 }
 
 
