@@ -51,9 +51,16 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--weight-sets", type=int, default=WEIGHT_SETS,
                    help="copies of the expert weights cycled across steps")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="batch size T in place of the workload's own (e.g. a T = 1..16 verify sweep "
+                        "at decode shapes); the workload is then named <workload>_T<T>")
     p.add_argument("--target-seconds", type=float, default=2.0,
                    help="timed-region length used to pick K when --steps is not given")
     return p.parse_args()
+
+
+def workload_name(args) -> str:
+    return args.workload if args.tokens is None else f"{args.workload}_T{args.tokens}"
 
 
 STAGE_SOURCES = {
@@ -287,7 +294,8 @@ def run_ours(args):
     if not os.path.exists(moe.LIB_PATH):
         _build.build()
     lib = moe.lib()
-    inp = moe_inputs.make_inputs(args.workload, seed=args.seed + rank, device=dev)
+    over = {} if args.tokens is None else {"T": args.tokens}
+    inp = moe_inputs.make_inputs(args.workload, seed=args.seed + rank, device=dev, **over)
     T, H, E, k, I = inp.T, inp.H, inp.E, inp.top_k, inp.I
     nv = inp.nvfp4_gate_up is not None
 
@@ -434,7 +442,7 @@ def run_ours(args):
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         achieved = byt[dom] / dom_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": measured_traffic(args.workload, dom)}
+                "frac": achieved / peak, "traffic": measured_traffic(workload_name(args), dom)}
     roof.update({"kernel": dom, "peak_source": f"{peak_src} MEASURED_PEAKS.json" if peak_src == "measured"
                  else "fallback", "algorithmic_bytes": byt[dom],
                  "algorithmic_flops": flops.get(dom), "launch_us": stage_ms[dom] * 1e3})
@@ -446,7 +454,7 @@ def run_ours(args):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, args.workload)
+        cpu = cpu_baseline(inp, workload_name(args))
 
     h2d = T * H * 2
     d2h = T * H * 2
@@ -463,7 +471,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "nvfp4-w4a16/bf16/f32acc" if nv else "bf16/f32acc",
         "data": "synthetic",
-        "config": {"workload": args.workload, "T": T, "H": H, "E": E, "top_k": k, "I": I,
+        "config": {"workload": workload_name(args), "T": T, "H": H, "E": E, "top_k": k, "I": I,
                    "weights": "nvfp4" if nv else "bf16",
                    "router_bias": "0.5*log-Zipf(1.1)" if inp.bias is not None else None,
                    "seed": args.seed, "parallelism": f"replicas x{world}",
@@ -494,7 +502,8 @@ def run_reference(args):
     import oracle
 
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = moe_inputs.make_inputs(args.workload, seed=args.seed, device=dev)
+    over = {} if args.tokens is None else {"T": args.tokens}
+    inp = moe_inputs.make_inputs(args.workload, seed=args.seed, device=dev, **over)
     x = moe_inputs.bf16_bits(inp.x)
     gw = moe_inputs.bf16_bits(inp.gate_w)
     bias = inp.bias.cpu().numpy() if inp.bias is not None else None
@@ -523,12 +532,12 @@ def run_reference(args):
         oracle.forward(x, gw, bias, top_k, W, tokens=tokens)
     el = time.perf_counter() - t0
     value = K * len(tokens) / el
-    sample = (f"{args.workload}: oracle forward of {len(tokens)} of the batch's {T} tokens per step "
+    sample = (f"{workload_name(args)}: oracle forward of {len(tokens)} of the batch's {T} tokens per step "
               f"(routing and grouping of the whole batch each step), fp64 numpy, 1 thread")
     line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s",
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": K, "warmup": Wm,
             "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic", "config": {"workload": args.workload},
+            "dtype": "f64", "data": "synthetic", "config": {"workload": workload_name(args)},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

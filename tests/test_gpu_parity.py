@@ -4,6 +4,7 @@ Routing (expert ids), counts, offsets and the permutation must match bit for
 bit; routing weights within the derived fp32 bound; outputs within
 max|out - ref| <= 1e-2 * max|ref| (bf16 weights) or 3e-2 (NVFP4 weights).
 """
+import dataclasses
 import os
 import sys
 
@@ -166,9 +167,12 @@ def test_all_tokens_one_expert():
     gh.check_output(inp, out, orc)
 
 
-def test_large_router_path():
-    """T >= 2048 uses the token-tiled router and the multi-block grouping."""
-    inp = _small(2304, 256, 64, 4, 128, bias="zipf")
+@pytest.mark.parametrize("T", [2304, 5000])
+def test_large_router_path(T):
+    """T >= 2048 uses the token-tiled router and the multi-block grouping
+    (T = 5000 spreads the tokens over CTAs of fewer than 32, with a ragged
+    last CTA)."""
+    inp = _small(T, 256, 64, 4, 128, bias="zipf")
     idx, w = moe.route(inp.x, inp.gate_w, inp.bias, inp.top_k)
     counts, offsets, perm, inv = moe.permute(idx, inp.E)
     torch.cuda.synchronize()
@@ -221,3 +225,27 @@ def test_prefill_workload_sampled():
     orc = oracle.forward_from_inputs(inp, tokens=rows)
     gh.check_routing(inp, idx, w, orc)
     gh.check_output(inp, out, orc, rows=rows)
+
+
+# ------------------------------------------------------------ verify sweep T = 1..16
+@pytest.fixture(scope="module")
+def verify_batch():
+    """Decode-shaped layer (H=2048, E=128, top_k=8, I=768) with 16 token rows;
+    each sweep case takes the first T rows (a token's routing and output do
+    not depend on the other tokens of the batch)."""
+    inp = moe_inputs.make_inputs("decode8", T=16, device="cuda")
+    W = oracle.ExpertWeights(moe_inputs.bf16_bits(inp.w_gate_up), moe_inputs.bf16_bits(inp.w_down))
+    return inp, W, moe_inputs.bf16_bits(inp.x), moe_inputs.bf16_bits(inp.gate_w)
+
+
+@pytest.mark.parametrize("T", list(range(1, 17)))
+def test_verify_sweep(verify_batch, T):
+    """Speculative-verify batch sizes T = 1..16 at decode shapes, no per-group
+    row ceiling: routing bit-exact and output within tolerance for every T."""
+    full, W, xb, gb = verify_batch
+    inp = dataclasses.replace(full, T=T, x=full.x[:T].contiguous())
+    out, idx, w, ws = gh.run_forward(inp)
+    assert moe.read_status(ws) == 0
+    orc = oracle.forward(xb[:T], gb, None, inp.top_k, W)
+    gh.check_routing(inp, idx, w, orc)
+    gh.check_output(inp, out, orc)
