@@ -66,6 +66,9 @@ def workload_name(args) -> str:
 STAGE_SOURCES = {
     "stream": ["expert_layer_gb300/csrc/stream_gemm.cu", "expert_layer_gb300/csrc/common.cuh",
                "expert_layer_gb300/csrc/kernels.h"],
+    # the tensor-core stage: token-row gather + gate/up + down kernels
+    "tc": ["expert_layer_gb300/csrc/tc_gemm.cu", "expert_layer_gb300/csrc/tc_ptx.cuh",
+           "expert_layer_gb300/csrc/common.cuh", "expert_layer_gb300/csrc/kernels.h"],
 }
 
 
@@ -437,7 +440,7 @@ def run_ours(args):
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         achieved = flops[dom] / dom_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None}
+                "frac": achieved / peak, "traffic": measured_traffic(workload_name(args), dom)}
     else:
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         achieved = byt[dom] / dom_s / 1e9

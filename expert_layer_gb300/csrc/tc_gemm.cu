@@ -234,11 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       const uint32_t b = lt & 1;
       const uint32_t tph = (lt >> 1) & 1;
-      if (!warp_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
-      tc_fence_after();
+      // the tile's rows, and for down their slots and routing weights, are
+      // fetched before waiting for the accumulator (two dependent global
+      // loads off the critical path)
       const TileInfo ti = decode_tile(md, nlarge, NTN, t);
       const int r = ti.mtile * BM + row;   // row within the expert's group
       const bool live = r < ti.m;
+      int f = 0;
+      float wt = 0.f;
+      if (kDown && live) { f = __ldg(&a.perm[ti.off + r]); wt = __ldg(&a.topk_w[f]); }
+      if (!warp_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
+      tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
       if (!kDown) {
         uint16_t* dst = a.h + (size_t)(ti.off + r) * a.I + ti.ntile * (BN / 2);
@@ -262,9 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        int f = 0;
-        float wt = 0.f;
-        if (live) { f = a.perm[ti.off + r]; wt = a.topk_w[f]; }
         const size_t obase = (size_t)f * a.H + ti.ntile * BN;
 #pragma unroll 1
         for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
