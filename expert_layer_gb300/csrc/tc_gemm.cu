@@ -93,21 +93,79 @@ struct TileInfo {
   int e, m, off, mtile, ntile;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const TileMeta& md, int nlarge, int NTN, int t) {
-  int lo = 0, hi = nlarge;  // find i with tiles[i]*NTN <= t < tiles[i+1]*NTN
+// `prefix` is the per-expert prefix of row tiles (md.tiles: 128-row m-tiles;
+// the pair kernel's prefix of 256-row m-tile pairs).
+__device__ __forceinline__ TileInfo decode_tile(const TileMeta& md, const int* prefix, int nlarge,
+                                                int NTN, int t) {
+  int lo = 0, hi = nlarge;  // find i with prefix[i]*NTN <= t < prefix[i+1]*NTN
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (md.tiles[mid] * NTN <= t) lo = mid; else hi = mid;
+    if (prefix[mid] * NTN <= t) lo = mid; else hi = mid;
   }
   TileInfo ti;
-  const int mt = md.tiles[lo + 1] - md.tiles[lo];
-  const int local = t - md.tiles[lo] * NTN;
+  const int mt = prefix[lo + 1] - prefix[lo];
+  const int local = t - prefix[lo] * NTN;
   ti.e = md.e[lo];
   ti.m = md.m[lo];
   ti.off = md.off[lo];
   ti.ntile = local / mt;
   ti.mtile = local % mt;
   return ti;
+}
+
+// Epilogue of one 128-row accumulator slice (this thread: TMEM lane = tile
+// row; tb = its TMEM address): SwiGLU into h (gate/up) or routing weight into
+// the slot's partial row (down).  r = row within the expert's group.
+template <bool kDown>
+__device__ __forceinline__ void store_tile(const TcArgs& a, uint32_t tb, int off, int r, bool live,
+                                           int ntile, int f, float wt) {
+  if (!kDown) {
+    uint16_t* dst = a.h + (size_t)(off + r) * a.I + ntile * (BN / 2);
+#pragma unroll 1
+    for (int cchunk = 0; cchunk < 4; ++cchunk) {
+      uint32_t gv[32], uv[32];
+      tmem_ld32(tb + cchunk * 32, gv);
+      tmem_ld32(tb + BN / 2 + cchunk * 32, uv);
+      tmem_wait_ld();
+      if (live) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
+          const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
+          pk[j] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(dst + cchunk * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
+    }
+  } else {
+    const size_t obase = (size_t)f * a.H + ntile * BN;
+#pragma unroll 1
+    for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
+      uint32_t yv[32];
+      tmem_ld32(tb + cchunk * 32, yv);
+      tmem_wait_ld();
+      if (live) {
+        if (a.partial_f32) {
+          float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.partial) + obase + cchunk * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            d4[v] = make_float4(wt * __uint_as_float(yv[4 * v]), wt * __uint_as_float(yv[4 * v + 1]),
+                                wt * __uint_as_float(yv[4 * v + 2]), wt * __uint_as_float(yv[4 * v + 3]));
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(wt * __uint_as_float(yv[2 * j]), wt * __uint_as_float(yv[2 * j + 1]));
+          uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.partial) + obase + cchunk * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+    }
+  }
 }
 
 template <bool kDown>
@@ -171,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(md, nlarge, NTN, t);
+        const TileInfo ti = decode_tile(md, md.tiles, nlarge, NTN, t);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % NS;
           const uint32_t ph = (it / NS) & 1;
@@ -237,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the tile's rows, and for down their slots and routing weights, are
       // fetched before waiting for the accumulator (two dependent global
       // loads off the critical path)
-      const TileInfo ti = decode_tile(md, nlarge, NTN, t);
+      const TileInfo ti = decode_tile(md, md.tiles, nlarge, NTN, t);
       const int r = ti.mtile * BM + row;   // row within the expert's group
       const bool live = r < ti.m;
       int f = 0;
@@ -246,53 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
-      if (!kDown) {
-        uint16_t* dst = a.h + (size_t)(ti.off + r) * a.I + ti.ntile * (BN / 2);
-#pragma unroll 1
-        for (int cchunk = 0; cchunk < 4; ++cchunk) {
-          uint32_t gv[32], uv[32];
-          tmem_ld32(tb + cchunk * 32, gv);
-          tmem_ld32(tb + BN / 2 + cchunk * 32, uv);
-          tmem_wait_ld();
-          if (live) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
-              const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
-              pk[j] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cchunk * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
-        }
-      } else {
-        const size_t obase = (size_t)f * a.H + ti.ntile * BN;
-#pragma unroll 1
-        for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
-          uint32_t yv[32];
-          tmem_ld32(tb + cchunk * 32, yv);
-          tmem_wait_ld();
-          if (live) {
-            if (a.partial_f32) {
-              float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.partial) + obase + cchunk * 32);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                d4[v] = make_float4(wt * __uint_as_float(yv[4 * v]), wt * __uint_as_float(yv[4 * v + 1]),
-                                    wt * __uint_as_float(yv[4 * v + 2]), wt * __uint_as_float(yv[4 * v + 3]));
-            } else {
-              uint32_t pk[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                pk[j] = pack_bf16x2(wt * __uint_as_float(yv[2 * j]), wt * __uint_as_float(yv[2 * j + 1]));
-              uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.partial) + obase + cchunk * 32);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            }
-          }
-        }
-      }
+      store_tile<kDown>(a, tb, ti.off, r, live, ti.ntile, f, wt);
       tc_fence_before();
       mbar_arrive(&tempty[b]);
       if (*(volatile int*)abort_flag) break;
@@ -305,6 +317,257 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols));
+  }
+}
+
+// ------------------------------------------------------------------ CTA pairs
+// The same GEMMs on 2-CTA clusters (launched with cluster dimension 2) with
+// the weights as the MMA's M side: one tcgen05.mma.cta_group::2 per 16-wide
+// K step computes 256 weight rows (128 in each CTA's shared and tensor
+// memory) x N token rows (N <= 256, split N/2 + N/2 between the CTAs' shared
+// memory; every CTA's accumulator holds all N columns for its own 128 weight
+// rows).  A pair tile is (expert, block of 256 weight rows, block of up to
+// 256 of the expert's token rows); the last token block of an expert uses the
+// smallest N (a multiple of 16) that covers it, so groups are padded by at
+// most 15 rows instead of to a whole 128- or 256-row tile.
+//   gate/up   CTA r holds gate and up rows of j = j0 + 64r .. +63
+//             interleaved (row 2jj = gate, 2jj+1 = up, one 4-D TMA box), so
+//             a lane pair of the epilogue holds g and u of one (j, token)
+//   down      CTA r holds output features d0 + 128r .. +127
+// Each CTA stages 32 KB per 64-wide K stage (16 KB of weights, 16 KB of
+// token rows), six stages.
+//   producers   one thread per CTA; both CTAs' TMA loads count on CTA 0's
+//               full barrier (tx bytes of the pair), each CTA waits on its
+//               own empty barrier
+//   MMA issuer  CTA 0 only; tcgen05.commit multicast to both CTAs' empty /
+//               accumulator-full barriers
+//   epilogue    both CTAs, eight warps (two per TMEM lane quadrant, taking
+//               alternate 32-column chunks), lane = weight row, column =
+//               token: stores of consecutive j (h) or d (partials) across a
+//               warp; one arrive per warp on CTA 0's accumulator-empty
+//               barrier (16 per tile)
+constexpr int NS2 = 6;
+constexpr int kEpiWarps = 8;                             // epilogue warps 2 .. 9
+constexpr int kThreadsPair = (2 + kEpiWarps) * 32;
+constexpr int kPairRows = 128;                          // weight rows, token rows per CTA
+constexpr int kStageBytes2 = 2 * kPairRows * BK * 2;    // 32 KB
+constexpr size_t kSmemBytes2 = (size_t)NS2 * kStageBytes2 + 1024 + 256 + 5 * 4 * (kMaxLarge + 1);
+
+__device__ __forceinline__ uint32_t idesc_pair(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)((2 * kPairRows) >> 4) << 24);
+}
+// token rows of a pair tile: 256, or the rest of the group rounded up to 16
+__device__ __forceinline__ int pair_n(int rem) { return rem >= 256 ? 256 : (rem + 15) & ~15; }
+
+template <bool kDown>
+__global__ void __launch_bounds__(kThreadsPair, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS2 * kStageBytes2);
+  uint64_t* empty = full + NS2;
+  uint64_t* tfull = empty + NS2;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  TileMeta md;
+  md.tiles = reinterpret_cast<int*>(smem + NS2 * kStageBytes2 + 256);   // [nlarge+1] token-block prefix
+  md.e = md.tiles + (kMaxLarge + 1);
+  md.m = md.e + (kMaxLarge + 1);
+  md.off = md.m + (kMaxLarge + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int cid = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
+  const int nlarge = *a.num_large;
+  const int nsmall = *a.num_active - nlarge;
+  const int NW = kDown ? a.H / (2 * kPairRows) : a.I / kPairRows;   // weight blocks per expert
+  const int K = kDown ? a.I : a.H;
+  const int nkb = K / BK;
+
+  for (int i = threadIdx.x; i < nlarge; i += kThreadsPair) {
+    const int e = a.active[nsmall + i];
+    md.e[i] = e;
+    md.m[i] = a.counts[e];
+    md.off[i] = a.offsets[e];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int i = 0; i < nlarge; ++i) {
+      md.tiles[i] = acc;
+      acc += (md.m[i] + 2 * kPairRows - 1) / (2 * kPairRows);
+    }
+    md.tiles[nlarge] = acc;
+  }
+  __syncthreads();
+  const int total = md.tiles[nlarge] * NW;
+  if (cid >= total) return;   // uniform for the pair (both read the same counts)
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS2; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 2 * kEpiWarps); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  tc_fence_before();
+  cluster_sync();   // both CTAs' barriers and tensor memory exist before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (each CTA)
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int p = cid; p < total && ok; p += ncl) {
+        const TileInfo ti = decode_tile(md, md.tiles, nlarge, NW, p);   // ntile = weight block
+        const int n = pair_n(ti.m - ti.mtile * 2 * kPairRows);
+        const int brow = ti.off + ti.mtile * 2 * kPairRows + (int)rank * (n / 2);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % NS2;
+          const uint32_t ph = (it / NS2) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
+          if (rank == 0) mbar_expect_tx(&full[s], 2 * kStageBytes2);
+          const uint32_t fb = map_to_rank(&full[s], 0);
+          unsigned char* sA = smem + s * kStageBytes2;
+          if (kDown)
+            tma_load_2d_pair(sA, &tmA, kb * BK, ti.e * a.H + ti.ntile * 2 * kPairRows + (int)rank * kPairRows, fb);
+          else
+            tma_load_4d_pair(sA, &tmA, kb * BK, 0, ti.ntile * kPairRows + (int)rank * (kPairRows / 2), ti.e, fb);
+          tma_load_2d_pair(sA + kPairRows * BK * 2, &tmB, kb * BK, brow, fb);
+        }
+        if (*(volatile int*)abort_flag) ok = false;
+      }
+      if (!ok) atomicOr(abort_flag, 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (CTA 0)
+    if (lane == 0 && rank == 0) {
+      uint32_t it = 0, lt = 0;
+      bool ok = true;
+      for (int p = cid; p < total && ok; p += ncl, ++lt) {
+        const TileInfo ti = decode_tile(md, md.tiles, nlarge, NW, p);
+        const uint32_t idesc = idesc_pair(pair_n(ti.m - ti.mtile * 2 * kPairRows));
+        const uint32_t b = lt & 1;
+        const uint32_t tph = (lt >> 1) & 1;
+        if (!mbar_wait(&tempty[b], tph ^ 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + b * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % NS2;
+          const uint32_t ph = (it / NS2) & 1;
+          if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + s * kStageBytes2);
+          const uint32_t sB = sA + kPairRows * BK * 2;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16_pair(tmem_d, umma_desc(sA + kk * 32), umma_desc(sB + kk * 32), idesc,
+                           (kb | kk) != 0 ? 1u : 0u);
+          umma_commit_pair(&empty[s]);   // both CTAs' stage s free once these MMAs are done
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[b]);     // both CTAs' accumulators ready
+        if (*(volatile int*)abort_flag) ok = false;
+      }
+      if (!ok) atomicOr(abort_flag, 1);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (each CTA)
+    // warp w reads TMEM lanes 32(w % 4) .. +31 and the 32-column chunks
+    // v = 2i + hc of the tile (hc = 0 for warps 2-5, 1 for warps 6-9)
+    const int q = warp & 3;
+    const int hc = (warp - 2) >> 2;
+    const uint32_t tempty0[2] = {map_to_rank(&tempty[0], 0), map_to_rank(&tempty[1], 0)};
+    uint32_t lt = 0;
+    for (int p = cid; p < total; p += ncl, ++lt) {
+      const uint32_t b = lt & 1;
+      const uint32_t tph = (lt >> 1) & 1;
+      const TileInfo ti = decode_tile(md, md.tiles, nlarge, NW, p);
+      const int tok0 = ti.mtile * 2 * kPairRows;     // first token row of the tile (within the group)
+      const int rem = ti.m - tok0;                   // token rows left in the group (> 0)
+      const int n = pair_n(rem);
+      const int ncols = rem < n ? rem : n;           // token columns to store
+      // down: slots and routing weights of this warp's columns (lane c of
+      // chunk i: token 32(2i + hc) + c), fetched before the accumulator wait
+      int fl[4];
+      float wl[4];
+      if (kDown) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = 32 * (2 * i + hc) + lane;
+          fl[i] = c < ncols ? __ldg(&a.perm[ti.off + tok0 + c]) : 0;
+          wl[i] = c < ncols ? __ldg(&a.topk_w[fl[i]]) : 0.f;
+        }
+      }
+      if (!warp_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+      // rolled: inlined copies of the 32-column body would crowd the
+      // instruction cache that the producer and MMA threads share
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        const int c0 = 32 * (2 * i + hc);
+        if (c0 >= ncols) break;   // uniform over the warp
+        uint32_t y[32];
+        tmem_ld32(tb + c0, y);
+        tmem_wait_ld();
+        if (!kDown) {
+          // lane pair (2jj, 2jj+1) holds gate and up of one j for 32 tokens;
+          // the even lane forms h for tokens 0-15 of the chunk, the odd lane
+          // for tokens 16-31, each with one exchange per token
+          const bool odd = lane & 1;
+          const int j = ti.ntile * kPairRows + (int)rank * (kPairRows / 2) + 16 * q + (lane >> 1);
+          uint16_t* hcol = a.h + (size_t)(ti.off + tok0 + c0 + (odd ? 16 : 0)) * a.I + j;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float send = __uint_as_float(odd ? y[c] : y[c + 16]);
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float g = odd ? recv : __uint_as_float(y[c]);
+            const float u = odd ? __uint_as_float(y[c + 16]) : recv;
+            if (c0 + c + (odd ? 16 : 0) < ncols) hcol[(size_t)c * a.I] = f2bf(silu(g) * u);
+          }
+        } else {
+          const int d = ti.ntile * 2 * kPairRows + (int)rank * kPairRows + 32 * q + lane;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int f = __shfl_sync(0xffffffffu, fl[i], c);
+            const float w = __shfl_sync(0xffffffffu, wl[i], c);
+            if (c0 + c < ncols) {
+              const float val = w * __uint_as_float(y[c]);
+              const size_t o = (size_t)f * a.H + d;
+              if (a.partial_f32) reinterpret_cast<float*>(a.partial)[o] = val;
+              else reinterpret_cast<uint16_t*>(a.partial)[o] = f2bf(val);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0[b]);
+      if (*(volatile int*)abort_flag) break;
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();   // no remote arrive or multicast commit is still aimed at either CTA
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.status, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kTmemCols));
   }
 }
@@ -350,7 +613,59 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
     const cudaError_t gerr = launch_gather_rows(p.x, p.perm, (int)S, p.H, p.k, p.xp, stream, launches);
     if (gerr != cudaSuccess) return gerr;
   }
+  // CTA pairs need an even number of co-resident CTAs; the single-CTA
+  // kernel serves the rest
+  const bool pair = p.num_sms >= 2;
   CUtensorMap tmA, tmB;
+  cudaError_t err;
+  if (pair) {
+    // A = weights (M), B = token rows (N)
+    if (!down) {
+      if (!make_map_gate_up_interleaved(&tmA, p.w_gate_up, p.E, p.I, p.H)) return cudaErrorInvalidValue;
+      if (!make_map(&tmB, p.xp, S, p.H, kPairRows)) return cudaErrorInvalidValue;
+    } else {
+      if (!make_map(&tmA, p.w_down, (uint64_t)p.E * p.H, p.I, kPairRows)) return cudaErrorInvalidValue;
+      if (!make_map(&tmB, p.h, S, p.I, kPairRows)) return cudaErrorInvalidValue;
+    }
+    const size_t smem = kSmemBytes2;
+    auto kern = down ? tc_gemm_pair_kernel<true> : tc_gemm_pair_kernel<false>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    // as many pairs as can be resident at once (persistent kernel)
+    int clusters = 0;
+    {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(p.num_sms & ~1));
+      cfg.blockDim = dim3(kThreadsPair);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      if (err != cudaSuccess) return err;
+    }
+    if (clusters > p.num_sms / 2) clusters = p.num_sms / 2;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    if (launches) *launches += 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.blockDim = dim3(kThreadsPair);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
+  }
   if (!down) {
     if (!make_map(&tmA, p.xp, S, p.H, BM)) return cudaErrorInvalidValue;
     if (!make_map(&tmB, p.w_gate_up, (uint64_t)p.E * 2 * p.I, p.H, BN / 2)) return cudaErrorInvalidValue;
@@ -359,7 +674,6 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
     if (!make_map(&tmB, p.w_down, (uint64_t)p.E * p.H, p.I, BN)) return cudaErrorInvalidValue;
   }
   const size_t smem = kSmemBytes;
-  cudaError_t err;
   if (down) err = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   else err = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
