@@ -335,8 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 //             interleaved (row 2jj = gate, 2jj+1 = up, one 4-D TMA box), so
 //             a lane pair of the epilogue holds g and u of one (j, token)
 //   down      CTA r holds output features d0 + 128r .. +127
-// Each CTA stages 32 KB per 64-wide K stage (16 KB of weights, 16 KB of
-// token rows), six stages.
+// Each CTA stages 64 KB per 128-wide K stage (32 KB of weights, 32 KB of
+// token rows, each as two 64-wide halves in the 128-byte swizzle layout),
+// three stages: the MMA thread polls one barrier and commits once per eight
+// MMAs, which keeps its issue loop ahead of the tensor pipe.
 //   producers   one thread per CTA; both CTAs' TMA loads count on CTA 0's
 //               full barrier (tx bytes of the pair), each CTA waits on its
 //               own empty barrier
@@ -347,11 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 //               token: stores of consecutive j (h) or d (partials) across a
 //               warp; one arrive per warp on CTA 0's accumulator-empty
 //               barrier (16 per tile)
-constexpr int NS2 = 6;
+constexpr int NS2 = 3;
 constexpr int kEpiWarps = 8;                             // epilogue warps 2 .. 9
 constexpr int kThreadsPair = (2 + kEpiWarps) * 32;
 constexpr int kPairRows = 128;                          // weight rows, token rows per CTA
-constexpr int kStageBytes2 = 2 * kPairRows * BK * 2;    // 32 KB
+// A stage is 128 K wide, two 64-wide halves of each operand: one barrier
+// poll and one commit per eight MMAs
+constexpr int kHalves = 2;
+constexpr int kHalfBytes = kPairRows * BK * 2;            // 16 KB: one operand, one half
+constexpr int kStageBytes2 = 2 * kHalves * kHalfBytes;    // 64 KB
 constexpr size_t kSmemBytes2 = (size_t)NS2 * kStageBytes2 + 1024 + 256 + 5 * 4 * (kMaxLarge + 1);
 
 __device__ __forceinline__ uint32_t idesc_pair(int n) {
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const int nsmall = *a.num_active - nlarge;
   const int NW = kDown ? a.H / (2 * kPairRows) : a.I / kPairRows;   // weight blocks per expert
   const int K = kDown ? a.I : a.H;
-  const int nkb = K / BK;
+  const int nkb = K / (kHalves * BK);
 
   for (int i = threadIdx.x; i < nlarge; i += kThreadsPair) {
     const int e = a.active[nsmall + i];
@@ -440,12 +446,19 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
           if (rank == 0) mbar_expect_tx(&full[s], 2 * kStageBytes2);
           const uint32_t fb = map_to_rank(&full[s], 0);
+          // [A half 0][A half 1][B half 0][B half 1]
           unsigned char* sA = smem + s * kStageBytes2;
-          if (kDown)
-            tma_load_2d_pair(sA, &tmA, kb * BK, ti.e * a.H + ti.ntile * 2 * kPairRows + (int)rank * kPairRows, fb);
-          else
-            tma_load_4d_pair(sA, &tmA, kb * BK, 0, ti.ntile * kPairRows + (int)rank * (kPairRows / 2), ti.e, fb);
-          tma_load_2d_pair(sA + kPairRows * BK * 2, &tmB, kb * BK, brow, fb);
+#pragma unroll
+          for (int hh = 0; hh < kHalves; ++hh) {
+            const int x = (kb * kHalves + hh) * BK;
+            if (kDown)
+              tma_load_2d_pair(sA + hh * kHalfBytes, &tmA, x,
+                               ti.e * a.H + ti.ntile * 2 * kPairRows + (int)rank * kPairRows, fb);
+            else
+              tma_load_4d_pair(sA + hh * kHalfBytes, &tmA, x, 0,
+                               ti.ntile * kPairRows + (int)rank * (kPairRows / 2), ti.e, fb);
+            tma_load_2d_pair(sA + (kHalves + hh) * kHalfBytes, &tmB, x, brow, fb);
+          }
         }
         if (*(volatile int*)abort_flag) ok = false;
       }
@@ -471,11 +484,14 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           if (!mbar_wait(&full[s], ph)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + s * kStageBytes2);
-          const uint32_t sB = sA + kPairRows * BK * 2;
+          const uint32_t sB = sA + kHalves * kHalfBytes;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16_pair(tmem_d, umma_desc(sA + kk * 32), umma_desc(sB + kk * 32), idesc,
-                           (kb | kk) != 0 ? 1u : 0u);
+          for (int hh = 0; hh < kHalves; ++hh)
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16_pair(tmem_d, umma_desc(sA + hh * kHalfBytes + kk * 32),
+                             umma_desc(sB + hh * kHalfBytes + kk * 32), idesc,
+                             (kb | hh | kk) != 0 ? 1u : 0u);
           umma_commit_pair(&empty[s]);   // both CTAs' stage s free once these MMAs are done
         }
         if (!ok) break;
