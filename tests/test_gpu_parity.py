@@ -55,6 +55,8 @@ SMALL_CASES = {
     # prefill-sized batch (T*k >= 8192): every group, down to a few rows, on
     # the tensor-core kernels, with the multi-block grouping
     "tc_prefill_small_groups": dict(T=1024, H=256, E=512, k=8, I=128, bias="zipf"),
+    # groups of several 256-row token blocks plus a ragged last block
+    "tc_multi_block": dict(T=1100, H=256, E=4, k=1, I=256, bias="zipf"),
 }
 
 
