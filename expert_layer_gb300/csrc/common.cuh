@@ -13,6 +13,7 @@ namespace moe {
 enum : int {
   kStatusBadExpert = 1,   // moe_permute saw an expert id outside [0, E)
   kStatusTimeout = 2,     // a bounded device-side wait gave up
+  kStatusRange = 4,       // NVFP4 path: an activation (x or h) beyond the f16 range
 };
 
 // Workspace header (first 256 bytes of every workspace).
@@ -30,7 +31,7 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte slot");
 // Offsets (bytes) of every workspace region for one shape.
 struct WsLayout {
   size_t hdr, sched, cnt, xnorm, wnorm, logits, logits64, idx, w, counts, offsets, active, tiles, blk_cnt,
-      blk_base, lrank, perm, inv_perm, h, partial, xp, total;
+      blk_base, lrank, perm, inv_perm, h, partial, xp, x16, total;
   int nblk;               // 512-slot blocks of the grouping kernels
   bool partial_f32;       // fp32 partials (else bf16)
 };
@@ -68,6 +69,7 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
   L.h = take(sizeof(uint16_t) * S * I);
   L.partial = take((L.partial_f32 ? 4 : 2) * (size_t)S * H);
   L.xp = take(sizeof(uint16_t) * (size_t)S * H);   // token rows in grouped order (tensor-core path)
+  L.x16 = take(sizeof(uint16_t) * (size_t)T * H);  // x in f16 (NVFP4 path)
   L.total = o;
   return L;
 }
@@ -104,6 +106,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same MMA with f16 operands (NVFP4 path).
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// f16 bits of a float, round to nearest even (|f| >= 65520 gives infinity)
+__device__ __forceinline__ uint16_t f2h(float f) {
+  uint16_t h;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
 }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {

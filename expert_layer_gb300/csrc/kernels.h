@@ -48,11 +48,12 @@ struct StreamGemmArgs {
   const int* num_large;      // device scalar: leading active experts served elsewhere (may be null)
   // gate/up
   const uint16_t* x;         // [T, H]
+  const uint16_t* x16;       // [T, H] x in f16 (NVFP4 path)
   const uint16_t* w_gate_up; // [E, 2I, H] bf16 (or null)
   const uint8_t* gu_codes;   // NVFP4 (or null)
   const uint8_t* gu_scales;
   const float* gu_global;
-  uint16_t* h;               // [S, I] bf16, grouped order
+  uint16_t* h;               // [S, I] grouped order: bf16, or f16 on the NVFP4 path
   // down
   const uint16_t* w_down;    // [E, H, I]
   const uint8_t* dn_codes;
@@ -70,6 +71,10 @@ struct StreamGemmArgs {
 };
 // gate/up then down of the small groups, one persistent launch
 cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
+// y = f16(x) for n bf16 values (n % 8 == 0); sets kStatusRange in *status
+// when a value rounds beyond the f16 range
+cudaError_t launch_to_f16(const uint16_t* x, size_t n, uint16_t* y, int* status, cudaStream_t stream,
+                          int* launches);
 
 // tc_gemm.cu -- tcgen05/TMEM grouped GEMMs for experts with many rows (bf16 weights)
 struct TcLaunch {

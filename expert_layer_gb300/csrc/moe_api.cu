@@ -259,6 +259,12 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   tc.h = a.h; tc.partial = a.partial; tc.partial_f32 = L.partial_f32;
   tc.status = &hdr->status; tc.num_sms = num_sms;
 
+  if (nvfp4) {
+    // the NVFP4 expert kernels multiply in f16: x converted once per call
+    a.x16 = ws_ptr<uint16_t>(workspace, L.x16);
+    MOE_TRY_CUDA(launch_to_f16(x, (size_t)T * H, ws_ptr<uint16_t>(workspace, L.x16), &hdr->status, s,
+                               launches));
+  }
   if (!tc_all) MOE_TRY_CUDA(launch_stream_gemm(a, s, launches));
   MOE_TRY_CUDA(mark(3));
   if (use_tc) {
@@ -303,7 +309,7 @@ int moe_read_status(const void* workspace, void* stream) {
   if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (st & kStatusTimeout) return MOE_ERR_DEVICE_TIMEOUT;
-  if (st & kStatusBadExpert) return MOE_ERR_DEVICE;
+  if (st & (kStatusBadExpert | kStatusRange)) return MOE_ERR_DEVICE;
   return MOE_OK;
 }
 

@@ -29,13 +29,19 @@
 // operand uses the same assignment, so every k meets its own partner exactly
 // once: a permutation of the summation inside each 16-wide step, nothing else.
 //
-// NVFP4 weights (W4A16): the A fragments are decoded in registers.  Thread
-// (g, c) loads 16 bytes of codes (32 elements, k = 32c..32c+31 of a 128-wide
-// block) and the two e4m3 scales of those 32 elements; a 256-entry table maps
-// a code byte to two bf16 values, multiplied by the bf16 form of the scale.
-// Both steps are exact (an e2m1 value times an e4m3 value has at most 6
-// significant bits); the per-expert fp32 global scale multiplies the fp32
-// accumulator in the epilogue.
+// NVFP4 weights (W4A16): the A fragments are decoded in registers and the
+// MMA runs on f16 operands.  Thread (g, c) loads 16 bytes of codes (32
+// elements, k = 32c..32c+31 of a 128-wide block) and the two e4m3 scales of
+// those 32 elements; the hardware conversions cvt.rn.f16x2.e2m1x2 (a code
+// byte to two f16, low nibble to the low half) and cvt.rn.f16x2.e4m3x2 (the
+// scale) are exact, and so is their f16 product (an e2m1 value times an e4m3
+// value has at most 6 significant bits and lies in [2^-10, 2688]); the
+// per-expert fp32 global scale multiplies the fp32 accumulator in the
+// epilogue.  The token rows are x converted to f16 beforehand
+// (launch_to_f16) and h, which the gate/up epilogue writes in f16 on this
+// path: exact for activations of magnitude 2^-14 .. 65504, below that
+// rounded to the f16 subnormal grid (absolute error <= 2^-25), above it
+// flagged (kStatusRange).
 #include <type_traits>
 
 #include "common.cuh"
@@ -78,8 +84,7 @@ struct StreamCfg {
   static constexpr int kWBytes = NS * KG * FR * 2 * 32 * 16;
   static constexpr int kSBytes = kFp4 ? NS * KG * FR * 2 * 32 * 8 : 0;
   static constexpr int kWarpBytes = kWBytes + kSBytes;
-  // NVFP4: the byte -> two-bf16 table replicated per lane (conflict-free lookups)
-  static constexpr int kLutBytes = kFp4 ? 256 * 32 * 4 : 0;
+  static constexpr int kLutBytes = 0;
 };
 
 // Bounded waits: polls before a wait gives up (and the kernel records
@@ -172,9 +177,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
   constexpr int KB = C::KB, KG = C::KG, NS = C::NS, NW = C::kWarps;
   constexpr int kFifo = 8;   // > NS: unit ids the producer may hold ahead of the consumer
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ uint16_t lut8[kFp4 ? 256 : 1];
   __shared__ int fifo[NW][kFifo];
-  uint32_t* lut2 = reinterpret_cast<uint32_t*>(smem + NW * C::kWarpBytes);   // [256][32]
   int4* smeta = reinterpret_cast<int4*>(smem + NW * C::kWarpBytes + C::kLutBytes);   // [E]
   int* sperm = reinterpret_cast<int*>(smeta + a.E);                                 // [S]
 
@@ -182,11 +185,6 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
   const int g = lane >> 2, c = lane & 3;
   uint4* ring = reinterpret_cast<uint4*>(smem + warp * C::kWarpBytes);
   uint2* sring = reinterpret_cast<uint2*>(smem + warp * C::kWarpBytes + C::kWBytes);
-
-  if constexpr (kFp4) {
-    nvfp4::fill_tables(lut2, lut8, threadIdx.x, NW * 32);
-    __syncthreads();
-  }
 
   // the grouping is complete once the kernel before this one is; the
   // combine may start launching
@@ -322,7 +320,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
         bsrc[nt] = nullptr;
         if (n < ct.m) {
           if (ct.down) bsrc[nt] = a.h + (size_t)(ct.off + n) * a.I;
-          else bsrc[nt] = a.x + (size_t)(permp[ct.off + n] / a.k) * a.H;
+          else bsrc[nt] = (kFp4 ? a.x16 : a.x) + (size_t)(permp[ct.off + n] / a.k) * a.H;
         }
       }
       // down: the epilogue's slots and routing weights, fetched now
@@ -380,25 +378,28 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
               const uint4 ahi = ring[rs + 32];
               const uint2 slo8 = sring[rs];
               const uint2 shi8 = sring[rs + 32];
-              // this thread's scale for this half: byte 2c + hf of the row's 8, as a
-              // bf16 pair {s, s}
+              // this thread's scale for this half: byte 2c + hf of the row's 8;
+              // rows g and g+8 converted together, then each as an f16 pair {s, s}
               const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1) + 8 * hf);
               const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1) + 8 * hf);
-              const uint32_t a8 = lut8[slo & 0xff], b8 = lut8[shi & 0xff];
-              const uint32_t sl2 = a8 | (a8 << 16), sh2 = b8 | (b8 << 16);
+              const uint32_t s2 = nvfp4::e4m3x2_f16x2((slo & 0xffu) | ((shi & 0xffu) << 8));
+              const uint32_t sl2 = __byte_perm(s2, 0, 0x1010), sh2 = __byte_perm(s2, 0, 0x3232);
               const uint32_t clo[2] = {hf ? alo.z : alo.x, hf ? alo.w : alo.y};
               const uint32_t chi[2] = {hf ? ahi.z : ahi.x, hf ? ahi.w : ahi.y};
   #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
                 const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
-                const uint32_t a0 = nvfp4::bf16x2_mul(lut2[((wl & 0xff) << 5) + lane], sl2);
-                const uint32_t a2 = nvfp4::bf16x2_mul(lut2[(((wl >> 8) & 0xff) << 5) + lane], sl2);
-                const uint32_t a1 = nvfp4::bf16x2_mul(lut2[((wh & 0xff) << 5) + lane], sh2);
-                const uint32_t a3 = nvfp4::bf16x2_mul(lut2[(((wh >> 8) & 0xff) << 5) + lane], sh2);
+                uint32_t l0, l1, h0, h1;
+                nvfp4::e2m1x4_f16x2(wl, l0, l1);
+                nvfp4::e2m1x4_f16x2(wh, h0, h1);
+                const uint32_t a0 = nvfp4::f16x2_mul(l0, sl2);
+                const uint32_t a2 = nvfp4::f16x2_mul(l1, sl2);
+                const uint32_t a1 = nvfp4::f16x2_mul(h0, sh2);
+                const uint32_t a3 = nvfp4::f16x2_mul(h1, sh2);
   #pragma unroll
                 for (int nt = 0; nt < NP; ++nt)
-                  if (nt < ntiles) mma_bf16_16816(acc[f][nt], a0, a1, a2, a3, bh[hf][nt][2 * q], bh[hf][nt][2 * q + 1]);
+                  if (nt < ntiles) mma_f16_16816(acc[f][nt], a0, a1, a2, a3, bh[hf][nt][2 * q], bh[hf][nt][2 * q + 1]);
               }
             }
           }
@@ -464,7 +465,15 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
           if (n < ct.m) {
             if (!ct.down) {
               const float gv = acc[fr][nt][h2] * gscale, uv = acc[fr][nt][2 + h2] * gscale;
-              a.h[(size_t)(ct.off + n) * a.I + (ct.blk * FR + fr) * 8 + g] = f2bf(silu(gv) * uv);
+              const float hv = silu(gv) * uv;
+              uint16_t hb;
+              if constexpr (kFp4) {
+                hb = f2h(hv);   // the down units' f16 operand
+                if ((hb & 0x7c00u) == 0x7c00u) atomicOr(a.status, kStatusRange);
+              } else {
+                hb = f2bf(hv);
+              }
+              a.h[(size_t)(ct.off + n) * a.I + (ct.blk * FR + fr) * 8 + g] = hb;
             } else {
               const int f = ef[nt][h2];
               const float wt = ew[nt][h2];
@@ -528,7 +537,37 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<kFp4, NT>, a);
 }
 
+// y = f16(x), eight values per thread; a value that rounds beyond the f16
+// range (or is not finite) sets kStatusRange, once per warp.
+__global__ void __launch_bounds__(256) to_f16_kernel(const uint16_t* __restrict__ x, size_t n8,
+                                                     uint16_t* __restrict__ y, int* status) {
+  bool bad = false;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint16_t lo = f2h(bf16lo(w[j])), hi = f2h(bf16hi(w[j]));
+      bad |= ((lo & 0x7c00u) == 0x7c00u) | ((hi & 0x7c00u) == 0x7c00u);
+      o[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    reinterpret_cast<uint4*>(y)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusRange);
+}
+
 }  // namespace
+
+cudaError_t launch_to_f16(const uint16_t* x, size_t n, uint16_t* y, int* status, cudaStream_t stream,
+                          int* launches) {
+  if (launches) *launches += 1;
+  const size_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  const size_t blocks = (n8 + 255) / 256;
+  to_f16_kernel<<<(unsigned)(blocks < 1024 ? blocks : 1024), 256, 0, stream>>>(x, n8, y, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;

@@ -52,7 +52,8 @@ typedef enum {
                                   pointer, device is not sm_103                      */
   MOE_ERR_WORKSPACE = -3,      /* workspace_bytes < moe_workspace_size(...)          */
   MOE_ERR_CUDA = -4,           /* a CUDA runtime call or kernel launch failed        */
-  MOE_ERR_DEVICE = -5,         /* a kernel found invalid data (moe_read_status)     */
+  MOE_ERR_DEVICE = -5,         /* a kernel found invalid data, e.g. an NVFP4-path
+                                  activation beyond the f16 range (moe_read_status) */
   MOE_ERR_DEVICE_TIMEOUT = -6  /* a bounded device-side wait gave up (moe_read_status) */
 } moe_status;
 
@@ -70,6 +71,11 @@ typedef enum {
  *   dn_codes  [E, H, I/2], dn_scales [E, H, I/16], dn_global [E]: same for w_down
  * Rows [0, I) of the gate/up tensor are the gate projection, rows [I, 2I) the
  * up projection.  All pointers are device pointers.
+ * The expert products run on f16 operands: the decoded weights are exact in
+ * f16, and the activations (x, and the SwiGLU output h) are converted to f16,
+ * which is exact for magnitudes 2^-14 .. 65504; smaller ones round to the
+ * f16 subnormal grid (absolute error <= 2^-25), larger ones are recorded as
+ * MOE_ERR_DEVICE for moe_read_status (the output is then unspecified).
  */
 typedef struct {
   const uint8_t *gu_codes;

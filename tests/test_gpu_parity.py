@@ -251,3 +251,17 @@ def test_verify_sweep(verify_batch, T):
     orc = oracle.forward(xb[:T], gb, None, inp.top_k, W)
     gh.check_routing(inp, idx, w, orc)
     gh.check_output(inp, out, orc)
+
+
+def test_nvfp4_activation_beyond_f16_is_flagged():
+    """The NVFP4 expert path multiplies in f16: an activation beyond the f16
+    range is reported as MOE_ERR_DEVICE instead of silently overflowing."""
+    inp = _small(24, 256, 8, 2, 128, nvfp4=True)
+    x = inp.x.clone()
+    x[3, 5] = 1.0e5
+    inp.x = x
+    _, _, _, ws = gh.run_forward(inp)
+    assert moe.read_status(ws) == -5   # MOE_ERR_DEVICE
+    # in range: clean status
+    _, _, _, ws2 = gh.run_forward(_small(24, 256, 8, 2, 128, nvfp4=True))
+    assert moe.read_status(ws2) == 0
