@@ -371,6 +371,10 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
   #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             if (hf == 1) load_half(bh[0], gi + 1, 0);
+            // codes and scales of all FR fragments first, then the four k
+            // steps with the fragments innermost: consecutive MMAs go to
+            // different accumulators, so their latencies overlap
+            uint32_t sl2[FR], sh2[FR], clo[FR][2], chi[FR][2];
   #pragma unroll
             for (int f = 0; f < FR; ++f) {
               const int rs = ((slot_r * FR + f) * 2) * 32 + lane;
@@ -383,20 +387,26 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
               const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1) + 8 * hf);
               const uint32_t shi = (c < 2 ? shi8.x : shi8.y) >> (16 * (c & 1) + 8 * hf);
               const uint32_t s2 = nvfp4::e4m3x2_f16x2((slo & 0xffu) | ((shi & 0xffu) << 8));
-              const uint32_t sl2 = __byte_perm(s2, 0, 0x1010), sh2 = __byte_perm(s2, 0, 0x3232);
-              const uint32_t clo[2] = {hf ? alo.z : alo.x, hf ? alo.w : alo.y};
-              const uint32_t chi[2] = {hf ? ahi.z : ahi.x, hf ? ahi.w : ahi.y};
+              sl2[f] = __byte_perm(s2, 0, 0x1010);
+              sh2[f] = __byte_perm(s2, 0, 0x3232);
+              clo[f][0] = hf ? alo.z : alo.x;
+              clo[f][1] = hf ? alo.w : alo.y;
+              chi[f][0] = hf ? ahi.z : ahi.x;
+              chi[f][1] = hf ? ahi.w : ahi.y;
+            }
   #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint32_t wl = clo[q >> 1] >> (16 * (q & 1));
-                const uint32_t wh = chi[q >> 1] >> (16 * (q & 1));
+            for (int q = 0; q < 4; ++q) {
+  #pragma unroll
+              for (int f = 0; f < FR; ++f) {
+                const uint32_t wl = clo[f][q >> 1] >> (16 * (q & 1));
+                const uint32_t wh = chi[f][q >> 1] >> (16 * (q & 1));
                 uint32_t l0, l1, h0, h1;
                 nvfp4::e2m1x4_f16x2(wl, l0, l1);
                 nvfp4::e2m1x4_f16x2(wh, h0, h1);
-                const uint32_t a0 = nvfp4::f16x2_mul(l0, sl2);
-                const uint32_t a2 = nvfp4::f16x2_mul(l1, sl2);
-                const uint32_t a1 = nvfp4::f16x2_mul(h0, sh2);
-                const uint32_t a3 = nvfp4::f16x2_mul(h1, sh2);
+                const uint32_t a0 = nvfp4::f16x2_mul(l0, sl2[f]);
+                const uint32_t a2 = nvfp4::f16x2_mul(l1, sl2[f]);
+                const uint32_t a1 = nvfp4::f16x2_mul(h0, sh2[f]);
+                const uint32_t a3 = nvfp4::f16x2_mul(h1, sh2[f]);
   #pragma unroll
                 for (int nt = 0; nt < NP; ++nt)
                   if (nt < ntiles) mma_f16_16816(acc[f][nt], a0, a1, a2, a3, bh[hf][nt][2 * q], bh[hf][nt][2 * q + 1]);
