@@ -68,10 +68,11 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // Pipeline shape per variant (NT = 8-row token tiles per pass).  A unit is
 // FR fragments of 16 weight rows.  NVFP4 units are two or four fragments
 // tall: each token-row fragment a thread loads then feeds FR mma instead of
-// one, which matters because 4-bit weights make the token rows (bf16) the
+// one, which matters because 4-bit weights make the token rows (16-bit) the
 // larger stream whenever an expert holds more than a few rows.  With four
-// token tiles (32 rows per pass, for batches above 16 tokens) the unit is two
-// fragments tall, so that an expert of up to 32 rows decodes its weights once.
+// token tiles (32 rows per pass, for experts averaging 24 rows or more) the
+// unit is two fragments tall, so that an expert of up to 32 rows decodes its
+// weights once.
 template <bool kFp4, int NT = 1>
 struct StreamCfg {
   static constexpr int KB = kFp4 ? 128 : 32;      // K elements per block
@@ -582,10 +583,14 @@ cudaError_t launch_to_f16(const uint16_t* x, size_t n, uint16_t* y, int* status,
 cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
   // a group never holds more rows than the batch has tokens: one 8-row tile
-  // per pass for T <= 8, two above (and four for NVFP4 above 16 tokens)
+  // per pass for T <= 8, two above; NVFP4 takes four (32-row passes) once
+  // the experts average 24 rows or more (measured: 16-row passes faster at
+  // 16 rows per expert, 32-row passes at 32 and 64)
   const bool two = a.T > 8;
   if (a.gu_codes != nullptr) {
-    if (a.T > 16) return launch_variant<true, 4>(a, stream);
+    const long long S = (long long)a.T * a.k;
+    const long long avg = S / (S < a.E ? S : a.E);
+    if (a.T > 16 && avg >= 24) return launch_variant<true, 4>(a, stream);
     return two ? launch_variant<true, 2>(a, stream) : launch_variant<true, 1>(a, stream);
   }
   return two ? launch_variant<false, 2>(a, stream) : launch_variant<false, 1>(a, stream);
