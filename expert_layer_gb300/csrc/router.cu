@@ -33,27 +33,33 @@ __host__ __device__ inline float gamma_bound(int n) {
   return (float)(n * u / (1.0 - n * u));
 }
 
-// fp64 value of a finite nonzero-exponent fp32 number, or of a signed zero,
-// assembled with integer operations (exact: fp64 holds every fp32 value).
-__device__ __forceinline__ double f32_as_f64(uint32_t u) {
-  const uint32_t e = (u >> 23) & 0xffu;
-  const uint32_t hi = e ? (u & 0x80000000u) | ((e + 896u) << 20) | ((u >> 3) & 0xfffffu)
-                        : (u & 0x80000000u);
-  return __hiloint2double((int)hi, e ? (int)(u << 29) : 0);
+// Exact sum of bf16 x bf16 products over columns [h0, h1) (h0 % 256 == 0,
+// h1 % 8 == 0) for one warp, returned as an fp64 value; every lane returns the
+// same value (xor butterfly).  A bf16 x bf16 product has at most 16
+// significant bits, so its fp32 value is exact unless it under- or overflows
+// fp32.  Exact products of magnitude 2^-33 .. < 1 are added as integers in a
+// 64-bit fixed-point accumulator with its unit in the last place at 2^-48
+// (16 significant bits shifted by exponent - 94, at most 32; a sum of up to
+// 2^15 terms below 2^48 each stays below 2^63, so a warp takes at most 32768
+// columns this way): those sums are exact, and the total is rounded to fp64
+// once per warp.  A batch of 8 elements in which any
+// lane meets a product outside that range (or an inexact fp32 product) is
+// added in fp64 instead, for the whole warp.  The integer work runs on the
+// full-rate integer pipes; GB300's fp64 pipe is slow.
+__device__ __forceinline__ long long fixed_of_product(uint32_t u) {
+  const int e = (int)((u >> 23) & 0xffu);
+  if (e == 0) return 0;   // exact zero (an underflow was sent the fp64 way)
+  const long long m16 = (long long)(((u & 0x7fffffu) | 0x800000u) >> 8);   // 16 significant bits
+  const long long q = m16 << (e - 94);
+  return (u & 0x80000000u) ? -q : q;
 }
 
-// fp64 dot of two bf16 rows over columns [h0, h1) (h0 % 256 == 0, h1 % 8 ==
-// 0), whole warp; every lane returns the same value (xor butterfly).  A bf16 x bf16 product has at most
-// 16 significant bits, so its fp32 value is exact unless it under- or
-// overflows fp32; then each exact product is added in fp64.  That is the
-// same arithmetic as an fp64 fma of the two factors, with one operation on
-// the (slow) fp64 pipe per element instead of three.  A batch of 8 elements
-// in which any lane meets an fp32 product that is not exact goes the fp64 way
-// for the whole warp.  Four independent chains per lane.
 __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
                                int h0, int h1) {
   const int lane = threadIdx.x & 31;
   double s[4] = {0.0, 0.0, 0.0, 0.0};
+  long long acc = 0;
+  const bool fixed_ok = h1 - h0 <= 32768;   // the accumulator's headroom
   constexpr int kB = 4;   // iterations whose loads are issued together
   for (int hb = h0; hb < h1; hb += 256 * kB) {
    uint4 va4[kB], vb4[kB];
@@ -70,7 +76,7 @@ __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* _
     const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
     uint32_t pu[8];
-    bool inexact = false;
+    bool outside = false;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -79,13 +85,13 @@ __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* _
         const float fb = j ? bf16hi(wb[i]) : bf16lo(wb[i]);
         const uint32_t u = __float_as_uint(__fmul_rn(fa, fb));
         const uint32_t e = (u >> 23) & 0xffu;
-        // exponent 255: overflow (or inf / nan); exponent 0 with two nonzero
-        // factors: underflow
-        inexact |= e == 0xffu || (e == 0 && fa != 0.0f && fb != 0.0f);
+        // inexact fp32 product (overflow, inf / nan, or underflow of two
+        // nonzero factors), or an exact one outside the fixed-point range
+        outside |= e == 0xffu || (e == 0 && fa != 0.0f && fb != 0.0f) || (e != 0 && (e < 94u || e > 126u));
         pu[2 * i + j] = u;
       }
     }
-    if (__any_sync(0xffffffffu, inexact)) {
+    if (__any_sync(0xffffffffu, outside || !fixed_ok)) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         s[i] = fma((double)bf16lo(wa[i]), (double)bf16lo(wb[i]), s[i]);
@@ -93,17 +99,16 @@ __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* _
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s[i] += f32_as_f64(pu[2 * i]);
-        s[i] += f32_as_f64(pu[2 * i + 1]);
-      }
+      for (int i = 0; i < 8; ++i) acc += fixed_of_product(pu[i]);
     }
    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   double r = (s[0] + s[1]) + (s[2] + s[3]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-  return r;
+  return ldexp((double)acc, -48) + r;
 }
 
 struct WarpScratch {
