@@ -83,7 +83,9 @@ struct StreamCfg {
   // per-warp ring: [NS][KG][FR][2 rows][32 lanes] x 16 B of weights (codes),
   // plus [NS][KG][FR][2][32] x 8 B of scales for NVFP4
   static constexpr int kWBytes = NS * KG * FR * 2 * 32 * 16;
-  static constexpr int kSBytes = kFp4 ? NS * KG * FR * 2 * 32 * 8 : 0;
+  // NVFP4 scales: per fragment and block the 8 scale bytes of each of its 16
+  // weight rows (one copy per row, read by the four lanes that use it)
+  static constexpr int kSBytes = kFp4 ? NS * KG * FR * 16 * 8 : 0;
   static constexpr int kWarpBytes = kWBytes + kSBytes;
   static constexpr int kLutBytes = 0;
 };
@@ -260,9 +262,14 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
             const size_t kc = (size_t)kb * 64 + 16 * c;
             cp_async16(d, cb + Rlo * (K / 2) + kc);
             cp_async16(d + 32, cb + Rhi * (K / 2) + kc);
-            uint2* ds = sring + (((slot_w * KG + i) * FR + f) * 2) * 32 + lane;
-            cp_async8(ds, sb + Rlo * (K / 16) + (size_t)kb * 8);
-            cp_async8(ds + 32, sb + Rhi * (K / 16) + (size_t)kb * 8);
+            // lanes 0-7: rows g = lane of the low half, lanes 8-15 the high half
+            if (lane < 16) {
+              const int r = lane & 7;
+              const int srow = it.down ? (it.blk * FR + f) * 16 + r + (lane & 8)
+                                       : (it.blk * FR + f) * 8 + r + ((lane & 8) ? a.I : 0);
+              cp_async8(sring + ((slot_w * KG + i) * FR + f) * 16 + lane,
+                        sb + ((size_t)it.e * NR + srow) * (K / 16) + (size_t)kb * 8);
+            }
           } else {
             const uint16_t* wb = it.down ? a.w_down : a.w_gate_up;
             const size_t kc = (size_t)kb * 32 + 8 * c;
@@ -369,6 +376,10 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
         for (int gi = 0; gi < ct.ngroups; ++gi) {   // KG = 1: group gi = block gi
           load_half(bh[1], gi, 1);
           cp_async_wait<NS - 2>();
+          // the scale rows were copied by other lanes: their copies of this
+          // block are complete and visible after the barrier, and every lane
+          // has finished reading the slot the next copies overwrite
+          __syncwarp();
   #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             if (hf == 1) load_half(bh[0], gi + 1, 0);
@@ -381,8 +392,8 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
               const int rs = ((slot_r * FR + f) * 2) * 32 + lane;
               const uint4 alo = ring[rs];
               const uint4 ahi = ring[rs + 32];
-              const uint2 slo8 = sring[rs];
-              const uint2 shi8 = sring[rs + 32];
+              const uint2 slo8 = sring[(slot_r * FR + f) * 16 + g];
+              const uint2 shi8 = sring[(slot_r * FR + f) * 16 + 8 + g];
               // this thread's scale for this half: byte 2c + hf of the row's 8;
               // rows g and g+8 converted together, then each as an f16 pair {s, s}
               const uint32_t slo = (c < 2 ? slo8.x : slo8.y) >> (16 * (c & 1) + 8 * hf);
