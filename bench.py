@@ -59,6 +59,24 @@ def parse_args():
     return p.parse_args()
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself with
+    one process or no process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, steps: int, tokens: int, max_ms: float) -> float:
+    """Whole-job throughput of `world` independent replicas, each running
+    `steps` steps of `tokens` tokens, timed by the slowest rank."""
+    return world * steps * tokens / (max_ms / 1e3)
+
+
 def workload_name(args) -> str:
     return args.workload if args.tokens is None else f"{args.workload}_T{args.tokens}"
 
@@ -374,12 +392,8 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * K * T / (ms / 1e3)
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    value = job_tokens_per_s(world, K, T, ms)
 
     # ---- per-stage times (same steps, events at stage boundaries)
     K2 = min(K, 2000)
@@ -419,12 +433,8 @@ def run_ours(args):
         out_h.copy_(out, non_blocking=True)
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * K3 * T / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
+    e2e_value = job_tokens_per_s(world, K3, T, e2e_ms)
 
     if rank != 0:
         dist.destroy_process_group()
