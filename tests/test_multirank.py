@@ -37,7 +37,7 @@ def _rank_main(rank, world, port, times, out):
 def test_slowest_rank_time_over_gloo():
     world = 2
     times = [3.25, 7.5]
-    out = mp.Manager().list([0.0] * world)
+    out = mp.get_context("spawn").Manager().list([0.0] * world)
     mp.spawn(_rank_main, args=(world, _free_port(), times, out), nprocs=world, join=True)
     assert list(out) == [7.5, 7.5]
 
