@@ -6,7 +6,12 @@
 // tensor cores.  Grouping stays on the device (page "第 9 章 prefill：最大的瓶颈",
 // sec. 9.9): tile lists come from the grouping kernels' counts, no host sync.
 //
-// One persistent CTA per SM, 6 warps:
+// Two kernels.  tc_gemm_pair_kernel (further down) is the one that runs on
+// GB300: 2-CTA clusters, one tcgen05.mma.cta_group::2 over both SMs with the
+// weights as M and the token rows as N.  tc_gemm_kernel, described here, is
+// the single-CTA form kept for devices with an odd SM count.
+//
+// Single-CTA form: one persistent CTA per SM, 6 warps:
 //   warp 0      producer (one thread): tiled TMA loads into a 4-stage
 //               shared-memory ring:
 //               token rows in grouped order (x gathered through the grouped
