@@ -52,8 +52,11 @@ __global__ void __launch_bounds__(kThreads) permute_block_rank_kernel(
 }
 
 // One block.  When the per-block counts fit in shared memory (`staged`) they
-// are read there with coalesced loads first, so the per-expert walks over the
-// blocks run on shared memory instead of one global load after another.
+// are copied there with coalesced 16-byte loads first, so the per-expert walks
+// over the blocks run on shared memory instead of one global load after
+// another; with E <= kThreads each expert's walk is also split into
+// P = kThreads / E contiguous ranges of blocks, one thread each (integer sums:
+// the split changes no result).
 __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
     const int32_t* __restrict__ blk_cnt, int nblk, int S, int E, int large_threshold,
     int tile_rows, int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
@@ -64,22 +67,58 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
   int* s_off = s_cnt + E;  // [E]
   int* s_blk = s_off + E;  // [nblk][E] when staged
   __shared__ int4 sw[kWarps];
+  __shared__ int s_part[kThreads];   // [P][E]: sums of each thread's range of blocks
   const size_t n = (size_t)nblk * E;
-  if (staged)
-    for (size_t i = threadIdx.x; i < n; i += kThreads) s_blk[i] = __ldcg(&blk_cnt[i]);
+  const bool vec = (n & 3) == 0 && (E & 3) == 0;   // s_blk starts 16-byte aligned when E % 4 == 0
+  if (staged) {
+    if (vec) {
+      for (size_t i = threadIdx.x; i < n / 4; i += kThreads)
+        reinterpret_cast<int4*>(s_blk)[i] = __ldcg(reinterpret_cast<const int4*>(blk_cnt) + i);
+    } else {
+      for (size_t i = threadIdx.x; i < n; i += kThreads) s_blk[i] = __ldcg(&blk_cnt[i]);
+    }
+  }
   __syncthreads();
-  const int32_t* src = staged ? s_blk : blk_cnt;
-  for (int e = threadIdx.x; e < E; e += kThreads) {
-    int s = 0;
-    for (int b = 0; b < nblk; ++b) s += src[(size_t)b * E + e];
-    s_cnt[e] = s;
+  const bool split = staged && E <= kThreads;
+  const int P = split ? kThreads / E : 1;
+  const int t = threadIdx.x, pe = t % E, pp = t / E;
+  const int b0 = pp * nblk / P, b1 = (pp + 1) * nblk / P;
+  if (split) {
+    if (t < P * E) {
+      int s = 0;
+      for (int b = b0; b < b1; ++b) s += s_blk[(size_t)b * E + pe];
+      s_part[t] = s;
+    }
+    __syncthreads();
+    for (int e = t; e < E; e += kThreads) {
+      int s = 0;
+      for (int q = 0; q < P; ++q) s += s_part[q * E + e];
+      s_cnt[e] = s;
+    }
+  } else {
+    const int32_t* src = staged ? s_blk : blk_cnt;
+    for (int e = t; e < E; e += kThreads) {
+      int s = 0;
+      for (int b = 0; b < nblk; ++b) s += src[(size_t)b * E + e];
+      s_cnt[e] = s;
+    }
   }
   __syncthreads();
   finish_scan(s_cnt, E, S, large_threshold, tile_rows, counts, offsets, active, tiles,
               reinterpret_cast<WsHeader*>(ws), s_off, sw);
   __syncthreads();
-  if (staged) {
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+  if (split) {
+    if (t < P * E) {
+      int s = s_off[pe];
+      for (int q = 0; q < pp; ++q) s += s_part[q * E + pe];
+      for (int b = b0; b < b1; ++b) {
+        const int c = s_blk[(size_t)b * E + pe];
+        s_blk[(size_t)b * E + pe] = s;
+        s += c;
+      }
+    }
+  } else if (staged) {
+    for (int e = t; e < E; e += kThreads) {
       int s = s_off[e];
       for (int b = 0; b < nblk; ++b) {
         const int c = s_blk[(size_t)b * E + e];
@@ -87,15 +126,22 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
         s += c;
       }
     }
-    __syncthreads();
-    for (size_t i = threadIdx.x; i < n; i += kThreads) blk_base[i] = s_blk[i];
   } else {
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+    for (int e = t; e < E; e += kThreads) {
       int s = s_off[e];
       for (int b = 0; b < nblk; ++b) {
         blk_base[(size_t)b * E + e] = s;
         s += blk_cnt[(size_t)b * E + e];
       }
+    }
+  }
+  if (staged) {
+    __syncthreads();
+    if (vec) {
+      for (size_t i = threadIdx.x; i < n / 4; i += kThreads)
+        reinterpret_cast<int4*>(blk_base)[i] = reinterpret_cast<const int4*>(s_blk)[i];
+    } else {
+      for (size_t i = threadIdx.x; i < n; i += kThreads) blk_base[i] = s_blk[i];
     }
   }
 }

@@ -28,24 +28,26 @@ namespace {
 
 constexpr int kCandCap = 64;  // candidates a warp can hold while certifying
 
-__host__ __device__ inline float gamma_bound(int n) {
+// gamma_n as fp32, evaluated on the host (fp64 division is slow on the device)
+// and passed to the kernels.
+inline float gamma_bound(int n) {
   const double u = 5.9604644775390625e-08;  // 2^-24
   return (float)(n * u / (1.0 - n * u));
 }
 
 // Exact sum of bf16 x bf16 products over columns [h0, h1) (h0 % 256 == 0,
-// h1 % 8 == 0) for one warp, returned as an fp64 value; every lane returns the
-// same value (xor butterfly).  A bf16 x bf16 product has at most 16
+// h1 % 8 == 0) for one warp, returned as an integer part acc * 2^-48 plus an
+// fp64 part r; every lane returns the same pair (xor butterflies).  A bf16 x bf16 product has at most 16
 // significant bits, so its fp32 value is exact unless it under- or overflows
 // fp32.  Exact products of magnitude 2^-33 .. < 1 are added as integers in a
 // 64-bit fixed-point accumulator with its unit in the last place at 2^-48
 // (16 significant bits shifted by exponent - 94, at most 32; a sum of up to
 // 2^15 terms below 2^48 each stays below 2^63, so a warp takes at most 32768
-// columns this way): those sums are exact, and the total is rounded to fp64
-// once per warp.  A batch of 8 elements in which any
+// columns this way): those sums are exact.  A batch of 8 elements in which any
 // lane meets a product outside that range (or an inexact fp32 product) is
-// added in fp64 instead, for the whole warp.  The integer work runs on the
-// full-rate integer pipes; GB300's fp64 pipe is slow.
+// added in fp64 instead, for the whole warp; when no batch went that way r is
+// 0 and its reduction is skipped.  The integer work runs on the full-rate
+// integer pipes; GB300's fp64 pipe is slow.
 __device__ __forceinline__ long long fixed_of_product(uint32_t u) {
   const int e = (int)((u >> 23) & 0xffu);
   if (e == 0) return 0;   // exact zero (an underflow was sent the fp64 way)
@@ -54,11 +56,17 @@ __device__ __forceinline__ long long fixed_of_product(uint32_t u) {
   return (u & 0x80000000u) ? -q : q;
 }
 
-__device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
-                               int h0, int h1) {
+struct DotPart {
+  long long acc;   // exact, in units of 2^-48
+  double r;
+};
+
+__device__ DotPart warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
+                                int h0, int h1) {
   const int lane = threadIdx.x & 31;
   double s[4] = {0.0, 0.0, 0.0, 0.0};
   long long acc = 0;
+  bool used64 = false;                      // warp-uniform
   const bool fixed_ok = h1 - h0 <= 32768;   // the accumulator's headroom
   constexpr int kB = 4;   // iterations whose loads are issued together
   for (int hb = h0; hb < h1; hb += 256 * kB) {
@@ -92,6 +100,7 @@ __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* _
       }
     }
     if (__any_sync(0xffffffffu, outside || !fixed_ok)) {
+      used64 = true;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         s[i] = fma((double)bf16lo(wa[i]), (double)bf16lo(wb[i]), s[i]);
@@ -105,10 +114,13 @@ __device__ double warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* _
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  double r = (s[0] + s[1]) + (s[2] + s[3]);
+  double r = 0.0;
+  if (used64) {
+    r = (s[0] + s[1]) + (s[2] + s[3]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-  return ldexp((double)acc, -48) + r;
+    for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  }
+  return {acc, r};
 }
 
 struct WarpScratch {
@@ -292,11 +304,12 @@ __device__ void select_begin(int E, int k, float delta, int end, WarpScratch& sc
 
 // The fp64 logits listed by select_begin for the tokens t0 .. t0+nt-1
 // (scratch scr[0..nt)), shared by all warps of the block.  Each dot is split
-// into kDotParts slices of its 256-column blocks, one warp per slice, so that
-// one dot keeps the fp64 pipes of all four SM sub-partitions busy (warps w .. w+3 sit on different
-// sub-partitions); the slice sums are added in slice order.  s_part holds one
-// double per warp.  Called by every thread of the block.
-constexpr int kDotParts = 4;
+// into kDotParts slices of its 256-column blocks, one warp per slice (a slice
+// of up to 1024 columns is one batch of loads per lane, so a round costs one
+// memory latency).  The slices' integer parts are added exactly (H <= 32768)
+// and rounded to fp64 once; their fp64 parts follow in slice order.  s_part
+// holds one DotPart per warp.  Called by every thread of the block.
+constexpr int kDotParts = 2;
 
 __device__ void dot_target(const WarpScratch* scr, int j, int& tt, int& r, int& e) {
   tt = 0;
@@ -307,7 +320,7 @@ __device__ void dot_target(const WarpScratch* scr, int j, int& tt, int& r, int& 
 
 __device__ void select_dots(WarpScratch* scr, int nt, int t0, const uint16_t* x,
                             const uint16_t* gate_w, const float* bias, int H, int E, double* l64,
-                            double* s_part) {
+                            DotPart* s_part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int per = nw / kDotParts;   // dots per round
   const int nb = (H + 255) / 256;
@@ -315,7 +328,7 @@ __device__ void select_dots(WarpScratch* scr, int nt, int t0, const uint16_t* x,
   for (int tt = 0; tt < nt; ++tt) total += scr[tt].nd;
   for (int base = 0; base < total; base += per) {   // uniform trip count
     const int j = base + warp / kDotParts, q = warp % kDotParts;
-    double d = 0.0;
+    DotPart d = {0, 0.0};
     if (j < total) {
       int tt, r, e;
       dot_target(scr, j, tt, r, e);
@@ -327,8 +340,19 @@ __device__ void select_dots(WarpScratch* scr, int nt, int t0, const uint16_t* x,
     if (lane == 0 && warp < per && base + warp < total) {
       int tt, r, e;
       dot_target(scr, base + warp, tt, r, e);
-      const double* p = s_part + kDotParts * warp;
-      double v = (p[0] + p[1]) + (p[2] + p[3]);
+      const DotPart* p = s_part + kDotParts * warp;
+      double v = 0.0;
+      if (H <= 32768) {   // fewer than 2^15 terms below 2^48 each: no overflow
+        long long a = 0;
+#pragma unroll
+        for (int i = 0; i < kDotParts; ++i) a += p[i].acc;
+        v = (double)a * 0x1p-48;   // exact scaling by a power of two
+      } else {
+#pragma unroll
+        for (int i = 0; i < kDotParts; ++i) v += (double)p[i].acc * 0x1p-48;
+      }
+#pragma unroll
+      for (int i = 0; i < kDotParts; ++i) v += p[i].r;
       if (bias) v += (double)bias[e];
       WarpScratch& sc = scr[tt];
       if (sc.end < 0) l64[(size_t)(t0 + tt) * E + e] = v;
@@ -480,14 +504,14 @@ __device__ __forceinline__ void stage_tokens(const uint16_t* __restrict__ x, int
 template <int kTT, bool kGroup>
 __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
-    int T, int H, int E, int k, int gamma_terms, float* __restrict__ logits,
+    int T, int H, int E, int k, float gamma, float* __restrict__ logits,
     float* __restrict__ wnorm, float* __restrict__ xnorm, double* __restrict__ l64,
     int* __restrict__ cnt, int32_t* __restrict__ idx, float* __restrict__ w, void* ws, GroupOut go) {
   using Cfg = SmallCfg<kTT>;
   constexpr int kEPW = Cfg::kEPW;
   extern __shared__ __align__(16) int dsm[];
   __shared__ WarpScratch scr[kTT];
-  __shared__ double s_part[kSmallWarps];
+  __shared__ DotPart s_part[kSmallWarps];
   __shared__ int s_last, s_group;
   __shared__ int4 sw[grouping::kWarps];
   pdl_wait();      // the workspace counters are cleared
@@ -667,7 +691,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
       wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
       lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
     }
-    const float delta = gamma_bound(gamma_terms) * sxn[warp] * wmax * (1.0f + 0x1p-10f) +
+    const float delta = gamma * sxn[warp] * wmax * (1.0f + 0x1p-10f) +
                         0x1p-22f * lmax + (float)H * 0x1p-149f;
     const float thr = cert_threshold(delta);
     const int end = by_warp ? extract_small(row, E, k, thr, sc) : certain_end_ranked(sc, E, k, thr);
@@ -862,37 +886,44 @@ __global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
   }
 }
 
-// Selection for the tiled path: one warp per token.
-__global__ void __launch_bounds__(256) router_select_kernel(
+// Selection for the tiled path (E <= 128): one warp per token, whose logits,
+// expert norms and ||x_t|| are loaded in one batch (lane l: experts l + 32i)
+// and ranked from registers.
+__global__ void __launch_bounds__(256, 3) router_select_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
-    int T, int H, int E, int k, int gamma_terms, const float* __restrict__ logits,
+    int T, int H, int E, int k, float gamma, const float* __restrict__ logits,
     const float* __restrict__ xnorm, const float* __restrict__ wnorm, double* __restrict__ l64,
     int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ double s_part[8];
+  __shared__ DotPart s_part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem_raw);
-  float* sl = reinterpret_cast<float*>(smem_raw + sizeof(WarpScratch) * 8) + (size_t)warp * E;
   const int t0 = blockIdx.x * 8;
   const int nt = min(8, T - t0);
   const int t = t0 + warp;
   if (warp < nt) {
+    float v[4], wn[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? logits[(size_t)t * E + e] : 0.0f;
+      wn[i] = e < E ? wnorm[e] : 0.0f;
+    }
+    const float xn = xnorm[t];
     float wmax = 0.f, lmax = 0.f;
-    for (int e = lane; e < E; e += 32) {
-      const float v = logits[(size_t)t * E + e];
-      sl[e] = v;
-      wmax = fmaxf(wmax, wnorm[e]);
-      lmax = fmaxf(lmax, fabsf(v));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      wmax = fmaxf(wmax, wn[i]);
+      lmax = fmaxf(lmax, fabsf(v[i]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
       lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
     }
-    __syncwarp();
-    const float delta = gamma_bound(gamma_terms) * xnorm[t] * wmax * (1.0f + 0x1p-10f) +
+    const float delta = gamma * xn * wmax * (1.0f + 0x1p-10f) +
                         0x1p-22f * lmax + (float)H * 0x1p-149f;
-    const int end = extract_small(sl, E, k, cert_threshold(delta), scr[warp]);   // E <= 128 here
+    const int end = extract_regs(v, E, k, cert_threshold(delta), scr[warp]);
     select_begin(E, k, delta, end, scr[warp], idx + (size_t)t * k, w + (size_t)t * k,
                  reinterpret_cast<WsHeader*>(ws));
   }
@@ -948,16 +979,16 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
     if (err != cudaSuccess) return err;
     router_tile_kernel<<<(T + kTileT - 1) / kTileT, kTileThreads, smem, stream>>>(x, gate_w, bias, T, H, E,
                                                                          logits, xnorm);
-    const size_t smem2 = sizeof(WarpScratch) * 8 + sizeof(float) * 8 * E;
+    const size_t smem2 = sizeof(WarpScratch) * 8;
     err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem2);
     if (err != cudaSuccess) return err;
-    const int gterms = kTileK + H / kTileK + 1;
-    router_select_kernel<<<(T + 7) / 8, 256, smem2, stream>>>(x, gate_w, bias, T, H, E, k, gterms,
+    const float gamma = gamma_bound(kTileK + H / kTileK + 1);
+    router_select_kernel<<<(T + 7) / 8, 256, smem2, stream>>>(x, gate_w, bias, T, H, E, k, gamma,
                                                               logits, xnorm, wnorm, l64, idx, w, ws);
     return cudaGetLastError();
   }
-  const int gterms = H / 32 + 5;
+  const float gamma = gamma_bound(H / 32 + 5);
   const bool grp = group != nullptr;
   const int tt = T <= 16 ? 1 : T <= 128 ? 4 : 8;
   const size_t smem = router_small_smem(E, T * k, tt, grp);
@@ -983,7 +1014,7 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, x, gate_w, bias, T, H, E, k, gterms, logits, wnorm, xnorm,
+    return cudaLaunchKernelEx(&cfg, kern, x, gate_w, bias, T, H, E, k, gamma, logits, wnorm, xnorm,
                               l64, cnt, idx, w, ws, go);
   };
   if (grp) {
