@@ -95,9 +95,16 @@ def test_route_and_permute_entry_points():
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 8, 1), (100, 64, 8), (512, 128, 8), (2048, 128, 8),
-                                   (3000, 200, 6), (9000, 128, 8)])
+                                   (3000, 200, 6), (9000, 128, 8), (5000, 99, 3), (4000, 600, 4),
+                                   (16384, 512, 4)])
 def test_permute_matches_oracle(T, E, k):
-    """Grouping alone on random expert ids, single-block and multi-block paths."""
+    """Grouping alone on random expert ids, single-block and multi-block paths.
+
+    The multi-block scan has three forms, all covered: per-block counts staged
+    in shared memory with each expert's walk split over 512 // E threads (E = 128,
+    200; E = 99 also takes the 4-byte staging copies), staged without the split
+    (E = 600 > 512), and walked in global memory (16384 x 4 slots, E = 512: the
+    counts exceed the shared-memory budget)."""
     g = torch.Generator().manual_seed(T + E)
     idx = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
     ws = moe.alloc_workspace(T, 128, E, 128, k)
