@@ -21,10 +21,11 @@ template <bool kF32>
 __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ partial, int T, int H,
                                                       int k, uint16_t* __restrict__ out) {
   constexpr int V = kF32 ? 4 : 8;
-  {
-    // while the down projection finishes: bring this thread's first partial
-    // row segment's address translation and lines toward L2 (a prefetch
-    // returns no data; the partials are read only after the wait)
+  if ((long long)T * (H / V) <= (long long)gridDim.x * blockDim.x) {
+    // one vector per thread (small batches): while the down projection
+    // finishes, bring this thread's partial row segment's address translation
+    // and lines toward L2 (a prefetch returns no data; the partials are read
+    // only after the wait)
     const long long v0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     if (v0 < (long long)T * (H / V)) {
       const size_t row = (size_t)(v0 / (H / V)) * k * H + (size_t)(v0 % (H / V)) * V;
