@@ -8,7 +8,10 @@ over one batch of the workload.  Inputs are seeded synthetic tensors with the
 workload's shapes; they stay resident in HBM during the device-timed region.
 Consecutive steps cycle through several copies of the expert weights (more
 bytes than L2 between two uses of a copy), so no step reads another step's
-weights from L2.  Under torchrun each rank runs an independent replica
+weights from L2.  The e2e figure repeats the steps with each step's input
+copied in from pinned host memory and its result copied back, the copies of
+neighbouring steps overlapping the current step's kernels as in a serving
+loop.  Under torchrun each rank runs an independent replica
 (weak scaling, no collective on the data path); the reported time is the max
 over ranks.
 
