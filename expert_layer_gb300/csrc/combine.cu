@@ -87,11 +87,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ p
 }  // namespace
 
 cudaError_t launch_combine(const void* partial, bool partial_f32, int T, int H, int k,
-                           uint16_t* out, cudaStream_t stream, int* launches) {
+                           uint16_t* out, int num_sms, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
   const long long nvec = (long long)T * (H / (partial_f32 ? 4 : 8));
   long long grid = (nvec + 255) / 256;
-  if (grid > 152 * 8) grid = 152 * 8;
+  // grid-stride beyond eight 256-thread CTAs per SM
+  const long long cap = 8ll * (num_sms > 0 ? num_sms : 1);
+  if (grid > cap) grid = cap;
   // programmatic launch: the combine's CTAs may become resident while the down
   // projection finishes and start the moment it completes
   cudaLaunchConfig_t cfg = {};

@@ -106,6 +106,6 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int S, in
 
 // combine.cu -- out[t] = sum_s partial[t*k+s] in slot order
 cudaError_t launch_combine(const void* partial, bool partial_f32, int T, int H, int k,
-                           uint16_t* out, cudaStream_t stream, int* launches);
+                           uint16_t* out, int num_sms, cudaStream_t stream, int* launches);
 
 }  // namespace moe

@@ -201,7 +201,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   // exceed T rows, so small batches skip them.
   const bool prefill = (long long)T * top_k >= 8192;
   const int large = prefill ? kLargeGroupPrefill : kLargeGroupDecode;
-  const bool use_tc = !nvfp4 && T >= large && H % 256 == 0;
+  const bool use_tc = !nvfp4 && T >= large && H % 256 == 0 && num_sms >= 2;
   // At prefill sizes every group goes to the tensor-core kernels: a 128-row
   // tile of a small group costs the whole GPU about 0.7 us of tensor time,
   // less than streaming that expert's 9.4 MB of weights, and the streaming
@@ -272,7 +272,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
     MOE_TRY_CUDA(launch_tc_gemm(tc, true, s, launches));
   }
   MOE_TRY_CUDA(mark(4));
-  MOE_TRY_CUDA(launch_combine(a.partial, L.partial_f32, T, H, top_k, out, s, launches));
+  MOE_TRY_CUDA(launch_combine(a.partial, L.partial_f32, T, H, top_k, out, num_sms, s, launches));
   MOE_TRY_CUDA(mark(5));
   return MOE_OK;
 }

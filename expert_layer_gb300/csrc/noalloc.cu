@@ -16,7 +16,10 @@
 // device address, so on the first call on each device (with that device
 // current) the library looks up the array's device address with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
-// capture begins.  All calls on a device share the one array and it keeps
+// capture begins.  The cached address stays valid while the device's primary
+// context lives: after cudaDeviceReset the library image is loaded again at
+// another address, so the entry point must not be called on a device that was
+// reset.  All calls on a device share the one array and it keeps
 // the previous call's contents: the header words that must start at zero are
 // cleared on the stream at the start of each call.  Calls whose work overlaps
 // on the GPU (different streams without ordering between them) race on the

@@ -6,28 +6,9 @@
 // tensor cores.  Grouping stays on the device (page "第 9 章 prefill：最大的瓶颈",
 // sec. 9.9): tile lists come from the grouping kernels' counts, no host sync.
 //
-// Two kernels.  tc_gemm_pair_kernel (further down) is the one that runs on
-// GB300: 2-CTA clusters, one tcgen05.mma.cta_group::2 over both SMs with the
-// weights as M and the token rows as N.  tc_gemm_kernel, described here, is
-// the single-CTA form kept for devices with an odd SM count.
-//
-// Single-CTA form: one persistent CTA per SM, 6 warps:
-//   warp 0      producer (one thread): tiled TMA loads into a 4-stage
-//               shared-memory ring:
-//               token rows in grouped order (x gathered through the grouped
-//               permutation by gather_rows, or h) and weight rows
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16 x bf16 -> fp32
-//               in TMEM), M = 128 token rows, N = 256, K = 16 per instruction
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, SwiGLU (gate/up) or
-//               routing-weight scaling (down), stores to global memory
-// TMEM holds two 128 x 256 fp32 accumulators, so the epilogue of one tile
-// overlaps the mainloop of the next.
-//
-// gate/up tile: 128 rows x (128 gate columns j0.. + the matching 128 up
-//               columns I+j0..) over K = H; h[r, j] = bf16(silu(g) * u)
-// down tile:    128 rows x 256 output features over K = I;
-//               partial[f, d] = topk_w[f] * y  (stored at the slot's own row)
-//
+// One kernel, tc_gemm_pair_kernel, on 2-CTA clusters: one
+// tcgen05.mma.cta_group::2 spans both SMs of a pair with the weights as M and
+// the expert's token rows as N (the layout is described above the kernel).
 // Operands are K-major with the 128-byte swizzle: TMA writes them in that
 // layout and the UMMA shared-memory descriptors describe it (8-row groups
 // 1024 bytes apart; the K step inside a 128-byte row advances the start
@@ -47,15 +28,9 @@ namespace {
 
 using namespace tcx;
 
-constexpr int BM = 128, BN = 256, BK = 64, NS = 4;
-constexpr int kTileBytesA = BM * BK * 2;                // 16 KB
-constexpr int kTileBytesB = BN * BK * 2;                // 32 KB
-constexpr int kStageBytes = kTileBytesA + kTileBytesB;  // 48 KB
-constexpr int kThreads = 192;
+constexpr int BN = 256, BK = 64;                        // accumulator columns, K per swizzled half
 constexpr uint32_t kTmemCols = 512;                     // two 256-column accumulators
 constexpr int kMaxLarge = 1024;
-// stages + alignment slack + barriers + tile metadata (4 int arrays of kMaxLarge+1)
-constexpr size_t kSmemBytes = (size_t)NS * kStageBytes + 1024 + 256 + 4 * 4 * (kMaxLarge + 1);
 
 struct TcArgs {
   int T, H, E, I, k;
@@ -73,17 +48,6 @@ struct TcArgs {
   int* status;
 };
 
-// Instruction descriptor: kind::f16, bf16 A/B, fp32 D, K-major A and B.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum));
-}
 // Per-CTA copy of the large-expert tile metadata (shared memory).
 struct TileMeta {
   int* tiles;   // [nlarge+1] m-tile prefix
@@ -116,214 +80,6 @@ __device__ __forceinline__ TileInfo decode_tile(const TileMeta& md, const int* p
   ti.ntile = local / mt;
   ti.mtile = local % mt;
   return ti;
-}
-
-// Epilogue of one 128-row accumulator slice (this thread: TMEM lane = tile
-// row; tb = its TMEM address): SwiGLU into h (gate/up) or routing weight into
-// the slot's partial row (down).  r = row within the expert's group.
-template <bool kDown>
-__device__ __forceinline__ void store_tile(const TcArgs& a, uint32_t tb, int off, int r, bool live,
-                                           int ntile, int f, float wt) {
-  if (!kDown) {
-    uint16_t* dst = a.h + (size_t)(off + r) * a.I + ntile * (BN / 2);
-#pragma unroll 1
-    for (int cchunk = 0; cchunk < 4; ++cchunk) {
-      uint32_t gv[32], uv[32];
-      tmem_ld32(tb + cchunk * 32, gv);
-      tmem_ld32(tb + BN / 2 + cchunk * 32, uv);
-      tmem_wait_ld();
-      if (live) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
-          const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
-          pk[j] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
-        }
-        uint4* d4 = reinterpret_cast<uint4*>(dst + cchunk * 32);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-      }
-    }
-  } else {
-    const size_t obase = (size_t)f * a.H + ntile * BN;
-#pragma unroll 1
-    for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
-      uint32_t yv[32];
-      tmem_ld32(tb + cchunk * 32, yv);
-      tmem_wait_ld();
-      if (live) {
-        if (a.partial_f32) {
-          float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.partial) + obase + cchunk * 32);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            d4[v] = make_float4(wt * __uint_as_float(yv[4 * v]), wt * __uint_as_float(yv[4 * v + 1]),
-                                wt * __uint_as_float(yv[4 * v + 2]), wt * __uint_as_float(yv[4 * v + 3]));
-        } else {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(wt * __uint_as_float(yv[2 * j]), wt * __uint_as_float(yv[2 * j + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.partial) + obase + cchunk * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
-      }
-    }
-  }
-}
-
-template <bool kDown>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcArgs a) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * kStageBytes);
-  uint64_t* empty = full + NS;
-  uint64_t* tfull = empty + NS;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  TileMeta md;
-  md.tiles = reinterpret_cast<int*>(smem + NS * kStageBytes + 256);
-  md.e = md.tiles + (kMaxLarge + 1);
-  md.m = md.e + (kMaxLarge + 1);
-  md.off = md.m + (kMaxLarge + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nlarge = *a.num_large;
-  const int nsmall = *a.num_active - nlarge;
-  const int NTN = kDown ? a.H / BN : a.I / (BN / 2);
-  const int total = a.tiles[nlarge] * NTN;
-  const int K = kDown ? a.I : a.H;
-  const int nkb = K / BK;
-  if ((int)blockIdx.x >= total) return;   // uniform for the whole CTA
-
-  for (int i = threadIdx.x; i <= nlarge; i += kThreads) {
-    md.tiles[i] = a.tiles[i];
-    if (i < nlarge) {
-      const int e = a.active[nsmall + i];
-      md.e[i] = e;
-      md.m[i] = a.counts[e];
-      md.off[i] = a.offsets[e];
-    }
-  }
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // one thread: no warp-wide synchronisation per stage
-    if (lane == 0) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(md, md.tiles, nlarge, NTN, t);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % NS;
-          const uint32_t ph = (it / NS) & 1;
-          if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
-          unsigned char* sA = smem + s * kStageBytes;
-          unsigned char* sB = sA + kTileBytesA;
-          mbar_expect_tx(&full[s], kStageBytes);
-          tma_load_2d(sA, &tmA, kb * BK, ti.off + ti.mtile * BM, &full[s]);
-          if (kDown) {
-            tma_load_2d(sB, &tmB, kb * BK, ti.e * a.H + ti.ntile * BN, &full[s]);
-          } else {
-            const int row0 = ti.e * 2 * a.I + ti.ntile * (BN / 2);
-            tma_load_2d(sB, &tmB, kb * BK, row0, &full[s]);
-            tma_load_2d(sB + kTileBytesB / 2, &tmB, kb * BK, row0 + a.I, &full[s]);
-          }
-        }
-        if (*(volatile int*)abort_flag) ok = false;
-      }
-      if (!ok) atomicOr(abort_flag, 1);
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // one thread issues every MMA; the stage loop has no warp-wide
-    // synchronisation, so that issuing keeps ahead of the tensor pipe
-    if (lane == 0) {
-      uint32_t it = 0, lt = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
-        const uint32_t b = lt & 1;
-        const uint32_t tph = (lt >> 1) & 1;
-        if (!mbar_wait(&tempty[b], tph ^ 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t tmem_d = tmem_base + b * BN;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % NS;
-          const uint32_t ph = (it / NS) & 1;
-          if (!mbar_wait(&full[s], ph)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sA = smem_u32(smem + s * kStageBytes);
-          const uint32_t sB = sA + kTileBytesA;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16(tmem_d, umma_desc(sA + kk * 32), umma_desc(sB + kk * 32),
-                      (kb | kk) != 0 ? 1u : 0u);
-          umma_commit(&empty[s]);   // frees the stage when these MMAs finish reading it
-        }
-        if (!ok) break;
-        umma_commit(&tfull[b]);     // accumulator ready
-        if (*(volatile int*)abort_flag) ok = false;
-      }
-      if (!ok) atomicOr(abort_flag, 1);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int row = q * 32 + lane;       // accumulator row = TMEM lane
-    uint32_t lt = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
-      const uint32_t b = lt & 1;
-      const uint32_t tph = (lt >> 1) & 1;
-      // the tile's rows, and for down their slots and routing weights, are
-      // fetched before waiting for the accumulator (two dependent global
-      // loads off the critical path)
-      const TileInfo ti = decode_tile(md, md.tiles, nlarge, NTN, t);
-      const int r = ti.mtile * BM + row;   // row within the expert's group
-      const bool live = r < ti.m;
-      int f = 0;
-      float wt = 0.f;
-      if (kDown && live) { f = __ldg(&a.perm[ti.off + r]); wt = __ldg(&a.topk_w[f]); }
-      if (!warp_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
-      tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
-      store_tile<kDown>(a, tb, ti.off, r, live, ti.ntile, f, wt);
-      tc_fence_before();
-      mbar_arrive(&tempty[b]);
-      if (*(volatile int*)abort_flag) break;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.status, kStatusTimeout);
-  if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols));
-  }
 }
 
 // ------------------------------------------------------------------ CTA pairs
@@ -634,47 +390,28 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
     const cudaError_t gerr = launch_gather_rows(p.x, p.perm, (int)S, p.H, p.k, p.xp, stream, launches);
     if (gerr != cudaSuccess) return gerr;
   }
-  // CTA pairs need an even number of co-resident CTAs; the single-CTA
-  // kernel serves the rest
-  const bool pair = p.num_sms >= 2;
+  // CTA pairs need at least two SMs; moe_forward sends every group to the
+  // weight-streaming kernel on a device with fewer
+  if (p.num_sms < 2) return cudaErrorInvalidConfiguration;
   CUtensorMap tmA, tmB;
   cudaError_t err;
-  if (pair) {
-    // A = weights (M), B = token rows (N)
-    if (!down) {
-      if (!make_map_gate_up_interleaved(&tmA, p.w_gate_up, p.E, p.I, p.H)) return cudaErrorInvalidValue;
-      if (!make_map(&tmB, p.xp, S, p.H, kPairRows)) return cudaErrorInvalidValue;
-    } else {
-      if (!make_map(&tmA, p.w_down, (uint64_t)p.E * p.H, p.I, kPairRows)) return cudaErrorInvalidValue;
-      if (!make_map(&tmB, p.h, S, p.I, kPairRows)) return cudaErrorInvalidValue;
-    }
-    const size_t smem = kSmemBytes2;
-    auto kern = down ? tc_gemm_pair_kernel<true> : tc_gemm_pair_kernel<false>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    // as many pairs as can be resident at once (persistent kernel)
-    int clusters = 0;
-    {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3((unsigned)(p.num_sms & ~1));
-      cfg.blockDim = dim3(kThreadsPair);
-      cfg.dynamicSmemBytes = smem;
-      cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-      if (err != cudaSuccess) return err;
-    }
-    if (clusters > p.num_sms / 2) clusters = p.num_sms / 2;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    if (launches) *launches += 1;
+  // A = weights (M), B = token rows (N)
+  if (!down) {
+    if (!make_map_gate_up_interleaved(&tmA, p.w_gate_up, p.E, p.I, p.H)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, p.xp, S, p.H, kPairRows)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_map(&tmA, p.w_down, (uint64_t)p.E * p.H, p.I, kPairRows)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, p.h, S, p.I, kPairRows)) return cudaErrorInvalidValue;
+  }
+  const size_t smem = kSmemBytes2;
+  auto kern = down ? tc_gemm_pair_kernel<true> : tc_gemm_pair_kernel<false>;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  // as many pairs as can be resident at once (persistent kernel)
+  int clusters = 0;
+  {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.gridDim = dim3((unsigned)(p.num_sms & ~1));
     cfg.blockDim = dim3(kThreadsPair);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -685,24 +422,25 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
+    err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (err != cudaSuccess) return err;
   }
-  if (!down) {
-    if (!make_map(&tmA, p.xp, S, p.H, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&tmB, p.w_gate_up, (uint64_t)p.E * 2 * p.I, p.H, BN / 2)) return cudaErrorInvalidValue;
-  } else {
-    if (!make_map(&tmA, p.h, S, p.I, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&tmB, p.w_down, (uint64_t)p.E * p.H, p.I, BN)) return cudaErrorInvalidValue;
-  }
-  const size_t smem = kSmemBytes;
-  if (down) err = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  else err = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
+  if (clusters > p.num_sms / 2) clusters = p.num_sms / 2;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
   if (launches) *launches += 1;
-  const int grid = p.num_sms;
-  if (down) tc_gemm_kernel<true><<<grid, kThreads, smem, stream>>>(tmA, tmB, a);
-  else tc_gemm_kernel<false><<<grid, kThreads, smem, stream>>>(tmA, tmB, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  cfg.blockDim = dim3(kThreadsPair);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
 }
 
 }  // namespace moe

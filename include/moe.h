@@ -195,7 +195,9 @@ int moe_read_diagnostics(const void *workspace, void *stream, int32_t *out4);
  * on every GPU that loads the library until the process exits), so it serves
  * only T*E <= 65536 and T <= 8192; larger batches return MOE_ERR_UNSUPPORTED.
  * The first call on a device looks up the array's device address (make that
- * call before any stream capture).  All calls on a device share the array:
+ * call before any stream capture) and keeps it for the life of the process:
+ * after cudaDeviceReset the address is stale, so do not call this entry point
+ * again on a device that was reset.  All calls on a device share the array:
  * calls whose GPU work overlaps (unordered streams) race and give undefined
  * results.  Device-side status is not reported (there is no workspace to
  * pass to moe_read_status).

@@ -107,6 +107,48 @@ def pin_nvfp4_layout(o):
                 assert W[e, r, k] == exp, (e, r, k, W[e, r, k], exp)
 
 
+def pin_nvfp4_forward_matches_bf16(o):
+    """The layer with NVFP4 expert weights equals the layer with the same
+    weights given as bf16 bits.  Every decoded weight (an e2m1 value times an
+    e4m3 value times a global with two significant bits) has at most 8
+    significant bits, so it is exact in bf16; the bf16 copies are built from
+    the two format tables, not from the oracle's decoder.  The globals differ
+    per expert and per projection, so taking one projection's global for the
+    other, or one expert's slice for another, changes the output."""
+    e2m1 = {c: _val(v) for c, v in _read_table("e2m1_codes.txt")}
+    e4m3 = {c: _val(v) for c, v in _read_table("e4m3_codes.txt")}
+    rng = _rng(13)
+    T, H, E, k, I = 7, 32, 3, 2, 16
+    scale_codes = np.array([c for c, v in e4m3.items() if not math.isnan(v) and 2.0 ** -9 <= abs(v) <= 8],
+                           dtype=np.uint8)
+    glob_gu = np.array([0.75, 0.375, 1.5], dtype=np.float32)
+    glob_dn = np.array([0.5, 3.0, 0.1875], dtype=np.float32)
+
+    def quantised(R, K, glob):
+        codes = rng.integers(0, 256, size=(E, R, K // 2), dtype=np.uint8)
+        scales = rng.choice(scale_codes, size=(E, R, K // 16)).astype(np.uint8)
+        vals = np.empty((E, R, K), dtype=np.float64)
+        for e in range(E):
+            for r in range(R):
+                for kk in range(K):
+                    byte = int(codes[e, r, kk // 2])
+                    nib = (byte & 0xF) if kk % 2 == 0 else (byte >> 4)
+                    vals[e, r, kk] = e2m1[nib] * e4m3[int(scales[e, r, kk // 16])] * float(glob[e])
+        bits = _bf16_round(vals.astype(np.float32))
+        back = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        assert np.array_equal(back, vals)   # the construction is bf16-exact
+        return (codes, scales, glob), bits
+
+    q_gu, b_gu = quantised(2 * I, H, glob_gu)
+    q_dn, b_dn = quantised(H, I, glob_dn)
+    xb = _rand_bf16(rng, (T, H), 1.0)
+    gb = _rand_bf16(rng, (E, H), 0.5)
+    a = o.forward(xb, gb, None, k, o.ExpertWeights(nvfp4_gate_up=q_gu, nvfp4_down=q_dn))
+    b = o.forward(xb, gb, None, k, o.ExpertWeights(b_gu, b_dn))
+    assert set(np.unique(a["idx"])) == set(range(E)), a["idx"]   # every expert's slice is used
+    assert np.array_equal(a["out"], b["out"]), np.abs(a["out"] - b["out"]).max()
+
+
 # ------------------------------------------------------------------ router
 
 def pin_router_zero_gate(o):

@@ -48,6 +48,11 @@ SMALL_CASES = {
     "nvfp4_t96": dict(T=96, H=256, E=8, k=2, I=256, nvfp4=True),
     "nvfp4_passes": dict(T=300, H=256, E=4, k=2, I=256, nvfp4=True),
     "nvfp4_h1280": dict(T=80, H=1280, E=8, k=2, I=256, nvfp4=True),
+    # more than 4096 routed slots on the weight-streaming kernel: the slot
+    # permutation is read from global memory instead of shared memory (NVFP4
+    # never takes the tensor-core kernels; bf16 with H % 256 != 0 neither)
+    "nvfp4_global_perm": dict(T=640, H=256, E=16, k=8, I=128, nvfp4=True),
+    "stream_global_perm": dict(T=600, H=384, E=16, k=8, I=128),
     # groups of >= 64 rows run on the tcgen05 kernels
     "tc_all": dict(T=512, H=256, E=8, k=2, I=128),
     "tc_mixed": dict(T=300, H=512, E=16, k=2, I=256, bias="zipf"),
@@ -220,17 +225,34 @@ def test_nvfp4_workload_sampled():
     inp = moe_inputs.make_inputs("nvfp4_256", device="cuda")
     out, idx, w, ws = gh.run_forward(inp)
     assert moe.read_status(ws) == 0
-    rows = list(range(0, inp.T, 8)) + [inp.T - 1]
+    r = oracle.route_from_inputs(inp)
+    rows = sorted(set(range(0, inp.T, 8)) | {inp.T - 1} | set(_edge_rows(r, inp.top_k)))
     orc = oracle.forward_from_inputs(inp, tokens=rows)
     gh.check_routing(inp, idx, w, orc)
     gh.check_output(inp, out, orc, rows=rows)
+
+
+def _edge_rows(r, k, n_small=4):
+    """Tokens whose slots sit in the last (ragged) token block of the most
+    loaded expert, at the first row of that expert's group, and in the
+    n_small least loaded active experts."""
+    counts, offsets, perm = r["counts"], r["offsets"], r["perm"]
+    hot = int(np.argmax(counts))
+    picks = {int(perm[offsets[hot + 1] - 1]) // k, int(perm[offsets[hot]]) // k,
+             int(perm[offsets[hot] + (counts[hot] // 256) * 256]) // k}
+    active = [e for e in np.argsort(counts, kind="stable") if counts[e] > 0][:n_small]
+    for e in active:
+        picks.add(int(perm[offsets[e]]) // k)
+        picks.add(int(perm[offsets[e + 1] - 1]) // k)
+    return sorted(picks)
 
 
 def test_prefill_workload_sampled():
     inp = moe_inputs.make_inputs("prefill8192", device="cuda")
     out, idx, w, ws = gh.run_forward(inp)
     assert moe.read_status(ws) == 0
-    rows = list(range(0, inp.T, 331)) + [inp.T - 1]
+    r = oracle.route_from_inputs(inp)
+    rows = sorted(set(range(0, inp.T, 331)) | {inp.T - 1} | set(_edge_rows(r, inp.top_k)))
     orc = oracle.forward_from_inputs(inp, tokens=rows)
     gh.check_routing(inp, idx, w, orc)
     gh.check_output(inp, out, orc, rows=rows)

@@ -158,6 +158,42 @@ def _mut_softmax_no_exp(m):
         axis=-1, keepdims=True)
 
 
+def _mut_nvfp4_globals_swapped(m):
+    # the gate/up tensor decoded with the down tensor's global and vice versa
+    def get(self, e):
+        if self.q_gu is not None:
+            (cg, sg, gg), (cd, sd, gd) = self.q_gu, self.q_dn
+            gu = m.nvfp4_dequant(cg[e:e + 1], sg[e:e + 1], gd[e:e + 1])[0]
+            dn = m.nvfp4_dequant(cd[e:e + 1], sd[e:e + 1], gg[e:e + 1])[0]
+            return gu, dn
+        return m.bf16_to_f64(self.gu_bits[e]), m.bf16_to_f64(self.dn_bits[e])
+    m.ExpertWeights.get = get
+
+
+def _mut_nvfp4_expert0_global(m):
+    # every expert decoded with expert 0's global scale
+    def get(self, e):
+        if self.q_gu is not None:
+            (cg, sg, gg), (cd, sd, gd) = self.q_gu, self.q_dn
+            gu = m.nvfp4_dequant(cg[e:e + 1], sg[e:e + 1], gg[0:1])[0]
+            dn = m.nvfp4_dequant(cd[e:e + 1], sd[e:e + 1], gd[0:1])[0]
+            return gu, dn
+        return m.bf16_to_f64(self.gu_bits[e]), m.bf16_to_f64(self.dn_bits[e])
+    m.ExpertWeights.get = get
+
+
+def _mut_nvfp4_expert0_codes(m):
+    # every expert decoded from expert 0's codes
+    def get(self, e):
+        if self.q_gu is not None:
+            (cg, sg, gg), (cd, sd, gd) = self.q_gu, self.q_dn
+            gu = m.nvfp4_dequant(cg[0:1], sg[e:e + 1], gg[e:e + 1])[0]
+            dn = m.nvfp4_dequant(cd[0:1], sd[e:e + 1], gd[e:e + 1])[0]
+            return gu, dn
+        return m.bf16_to_f64(self.gu_bits[e]), m.bf16_to_f64(self.dn_bits[e])
+    m.ExpertWeights.get = get
+
+
 MUTANTS = [v for k, v in sorted(globals().items()) if k.startswith("_mut_")]
 
 

@@ -40,16 +40,21 @@ def _noalloc(inp):
 def test_route_noalloc_matches_route_twice():
     from expert_layer_gb300 import _build
     _build.build()
+    # the first two take the small-batch router, the third (T >= 2048) the
+    # token-tiled router; all three share the one scratch array in turn
     batches = [moe_inputs.make_inputs(dict(T=64, H=2048, E=128, top_k=8, I=128, bias="zipf", nvfp4=False),
                                       seed=5, device="cuda"),
                moe_inputs.make_inputs(dict(T=37, H=512, E=64, top_k=6, I=128, bias=None, nvfp4=False),
-                                      seed=6, device="cuda")]
-    for inp in batches:                        # two calls in a row on the shared scratch
+                                      seed=6, device="cuda"),
+               moe_inputs.make_inputs(dict(T=2048, H=256, E=32, top_k=4, I=128, bias="zipf", nvfp4=False),
+                                      seed=7, device="cuda")]
+    for inp in batches:                        # calls in a row on the shared scratch
         idx_n, w_n = _noalloc(inp)
         idx_r, w_r = moe.route(inp.x, inp.gate_w, inp.bias, inp.top_k)
         torch.cuda.synchronize()
         assert torch.equal(idx_n, idx_r)
         r = oracle.route_from_inputs(inp)
+        gh.check_routing(inp, idx_n, w_n, r)   # ids bit-exact, weights within the bound
         bound = gh.weight_bound(inp, r["logits"])[:, None]
         wr = w_r.cpu().double().numpy()
         assert np.all(np.abs(w_n.cpu().double().numpy() - wr) <= bound * wr + 1e-12)
