@@ -16,6 +16,8 @@ decode8          8    2048  128     8     768  uniform router
 decode64        64    2048  128     8     768  0.5*log-Zipf(1.1) bias
 prefill8192   8192    2048  128     8     768  0.5*log-Zipf(1.1) bias
 nvfp4_256      256    2048  128     8     768  NVFP4 expert weights
+prefill8192_w4a4 8192 2048  128     8     768  NVFP4 weights and activations,
+                                               0.5*log-Zipf(1.1) bias
 =============  =====  =====  ===  =====  ====  =========================
 
 Recipe: one ``torch.Generator`` on the requested device seeded with ``seed``;
@@ -25,6 +27,15 @@ expert weights are drawn the same way in fp32 and encoded to NVFP4 instead of
 bf16.  The values depend on the generator's device (CPU and CUDA generators
 produce different streams for the same seed); every consumer of one call sees
 the same bytes.
+
+W4A4 workloads also carry the activations' NVFP4 global scales, one fp32 per
+expert for the token rows (x_global) and for the SwiGLU output (h_global),
+as an NVFP4 checkpoint stores calibrated input scales.  The recipe sets them
+from a bound on the activations' magnitude, G = bound / (6 * 448) (6 is the
+largest e2m1 value, 448 the largest e4m3 value): bound 8 for x ~ N(0,1) and
+bound 32 for the SwiGLU output, the same for every expert.  Tests pass other
+values (different per expert) through ``make_inputs(..., x_global=...,
+h_global=...)``.
 """
 from __future__ import annotations
 
@@ -39,7 +50,10 @@ WORKLOADS = {
     "decode64": dict(T=64, H=2048, E=128, top_k=8, I=768, bias="zipf", nvfp4=False),
     "prefill8192": dict(T=8192, H=2048, E=128, top_k=8, I=768, bias="zipf", nvfp4=False),
     "nvfp4_256": dict(T=256, H=2048, E=128, top_k=8, I=768, bias=None, nvfp4=True),
+    "prefill8192_w4a4": dict(T=8192, H=2048, E=128, top_k=8, I=768, bias="zipf", nvfp4=True, w4a4=True),
 }
+
+X_BOUND, H_BOUND = 8.0, 32.0
 
 
 @dataclass
@@ -71,6 +85,8 @@ class MoEInputs:
     nvfp4_gate_up: NVFP4Tensor | None = None
     nvfp4_down: NVFP4Tensor | None = None
     meta: dict = field(default_factory=dict)
+    x_global: torch.Tensor | None = None  # fp32 [E], W4A4 only
+    h_global: torch.Tensor | None = None  # fp32 [E], W4A4 only
 
     def to(self, device) -> "MoEInputs":
         def mv(t):
@@ -81,7 +97,8 @@ class MoEInputs:
 
         return MoEInputs(self.T, self.H, self.E, self.top_k, self.I, mv(self.x), mv(self.gate_w),
                          mv(self.bias), mv(self.w_gate_up), mv(self.w_down),
-                         mvq(self.nvfp4_gate_up), mvq(self.nvfp4_down), dict(self.meta))
+                         mvq(self.nvfp4_gate_up), mvq(self.nvfp4_down), dict(self.meta),
+                         mv(self.x_global), mv(self.h_global))
 
 
 def zipf_router_bias(E: int, s: float = 1.1, scale: float = 0.5) -> torch.Tensor:
@@ -158,7 +175,16 @@ def make_inputs(workload: str | dict, seed: int = 0, device: str | torch.device 
     if cfg.get("nvfp4"):
         gu = nvfp4_encode(draw((E, 2 * I, H), 0.02))
         dn = nvfp4_encode(draw((E, H, I), 0.02))
-        return MoEInputs(T, H, E, k, I, x, gate_w, bias, None, None, gu, dn, meta=cfg)
+        xg = hg = None
+        if cfg.get("w4a4"):
+            xg = cfg.get("x_global")
+            hg = cfg.get("h_global")
+            xg = (torch.full((E,), X_BOUND / (6.0 * 448.0), dtype=torch.float32) if xg is None
+                  else torch.as_tensor(xg, dtype=torch.float32)).to(dev)
+            hg = (torch.full((E,), H_BOUND / (6.0 * 448.0), dtype=torch.float32) if hg is None
+                  else torch.as_tensor(hg, dtype=torch.float32)).to(dev)
+        return MoEInputs(T, H, E, k, I, x, gate_w, bias, None, None, gu, dn, meta=cfg, x_global=xg,
+                         h_global=hg)
     w_gate_up = draw((E, 2 * I, H), 0.02).to(torch.bfloat16)
     w_down = draw((E, H, I), 0.02).to(torch.bfloat16)
     return MoEInputs(T, H, E, k, I, x, gate_w, bias, w_gate_up, w_down, meta=cfg)

@@ -8,8 +8,9 @@ from __future__ import annotations
 import numpy as np
 
 from . import moe_oracle
-from .moe_oracle import (ExpertWeights, bf16_to_f64, e2m1_to_f64, e4m3_to_f64, forward,
-                         nvfp4_dequant, permute, route, silu, softmax)
+from .moe_oracle import (ExpertWeights, bf16_to_f64, e2m1_quantize, e2m1_to_f64, e4m3_quantize,
+                         e4m3_to_f64, forward, forward_w4a4, nvfp4_dequant, nvfp4_quantize, permute,
+                         route, silu, softmax)
 
 
 def _np(t):
@@ -42,3 +43,13 @@ def route_from_inputs(inp):
     counts, offsets, perm, inv_perm = permute(idx, inp.E)
     return dict(logits=logits, idx=idx, w=w, counts=counts, offsets=offsets, perm=perm,
                 inv_perm=inv_perm)
+
+
+def forward_w4a4_from_inputs(inp, tokens=None):
+    """The W4A4 oracle on a ``moe_inputs.MoEInputs`` bundle with NVFP4 weights
+    and activation global scales (``inp.x_global``, ``inp.h_global``)."""
+    q, d = inp.nvfp4_gate_up, inp.nvfp4_down
+    weights = ExpertWeights(nvfp4_gate_up=(_np(q.codes), _np(q.scales), _np(q.glob)),
+                            nvfp4_down=(_np(d.codes), _np(d.scales), _np(d.glob)))
+    return forward_w4a4(_bits16(inp.x), _bits16(inp.gate_w), _np(inp.bias), inp.top_k, weights,
+                        _np(inp.x_global), _np(inp.h_global), tokens=tokens)

@@ -28,6 +28,22 @@ for a Qwen3-style SwiGLU MoE layer:
 NVFP4 weights are decoded exactly to fp64 (e2m1 code x e4m3 block scale x fp32
 global) and then used as in step 6.
 
+W4A4 (``forward_w4a4``): NVFP4 weights and NVFP4 activations.  The pages
+name the NVFP4 deployment (page "vLLM 0.32 升级试验：TEP2 prefill 诅咒解除 +
+decode 本机纪录", header and "背景与动机": the 176B NVFP4 MoE served through
+the "nvfp4-sm80" graft) but not its activation numerics; the reading taken
+here is the format's own recipe applied to each routed row: for expert e the
+token row x_t (step 6's input) and the SwiGLU output h (rounded to bf16, as
+on the bf16-weight path) are each cut into 16-element blocks along the
+contraction axis; a block with largest magnitude a gets the e4m3 scale
+s = RNE_e4m3(a / (6*G)) and its elements the e2m1 codes RNE_e2m1(v / (s*G)),
+G = x_global[e] or h_global[e] (fp32 constants given with the weights, like
+the calibrated input scales of NVFP4 checkpoints).  Each quotient and product
+in these decisions is taken in fp32 (the precision a kernel takes them in);
+both roundings are to nearest, ties to the even code, and saturate at the
+format's largest finite value (448 and 6).  The GEMMs then use the decoded
+values exactly in fp64.
+
 Inputs are the raw bit patterns (uint16 bf16, uint8 e2m1/e4m3) or fp32 arrays
 produced by the seeded input module; the oracle decodes them itself.
 """
@@ -237,6 +253,122 @@ def forward(x_bits, gate_w_bits, bias, top_k, weights: ExpertWeights, tokens=Non
     out = np.zeros((len(toks), x.shape[1]), dtype=np.float64)
     for i, t in enumerate(toks):
         acc = np.zeros(x.shape[1], dtype=np.float64)
+        for s in range(top_k):
+            acc = acc + w[t, s] * y[(int(t), s)]
+        out[i] = acc
+    return dict(out=out, tokens=toks, logits=logits, idx=idx, w=w, counts=counts,
+                offsets=offsets, perm=perm, inv_perm=inv_perm)
+
+
+# ----------------------------------------------------------------- W4A4
+
+
+def e4m3_quantize(v: np.ndarray) -> np.ndarray:
+    """fp32 values -> e4m3 bytes (OCP FP8 E4M3): round to nearest, ties to the
+    even mantissa, magnitudes beyond 448 saturate to 448.
+
+    Normal numbers are (1 + m/8) * 2^(e-7), e = 1..15; exponent field 0 is
+    subnormal m/8 * 2^-6.  A magnitude v >= 2^-6 is rounded on the grid of
+    its binade, 2^(floor(log2 v) - 3); below 2^-6 on the subnormal grid
+    2^-9.  Rounding up into the next binade carries into the exponent field
+    (mantissa 8 becomes exponent + 1, mantissa 0)."""
+    a = np.abs(np.asarray(v, dtype=np.float32).astype(np.float64))
+    sign = np.signbit(np.asarray(v, dtype=np.float32)).astype(np.int64)
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    code[sub] = np.rint(a[sub] / 2.0 ** -9).astype(np.int64)          # 0..8 (8 = 2^-6)
+    nrm = ~sub
+    e = np.floor(np.log2(np.where(nrm, a, 1.0))).astype(np.int64)
+    # log2 of an exact power of two is exact; guard the binade anyway
+    e = np.where(np.ldexp(1.0, e) > a, e - 1, e)
+    e = np.where(np.ldexp(1.0, e + 1) <= a, e + 1, e)
+    m = np.rint(a / np.ldexp(1.0, e - 3)).astype(np.int64)             # 8..16
+    code[nrm] = ((e[nrm] + 7) << 3) + (m[nrm] - 8)
+    code = np.minimum(code, 0x7E)                                       # 448
+    return ((sign << 7) | code).astype(np.uint8)
+
+
+def e2m1_quantize(v: np.ndarray) -> np.ndarray:
+    """fp32 values -> 4-bit e2m1 codes (OCP MX FP4 E2M1): nearest of
+    0, 0.5, 1, 1.5, 2, 3, 4, 6 in magnitude, ties to the even code (mantissa
+    bit 0), saturating at 6.  The grid is 0.5-spaced below 2, 1-spaced on
+    [2, 4), 2-spaced from 4."""
+    f = np.asarray(v, dtype=np.float32)
+    a = np.abs(f.astype(np.float64))
+    sign = np.signbit(f).astype(np.int64)
+    code = np.where(a < 2.0, np.rint(a / 0.5),                          # codes 0..4
+                    np.where(a < 4.0, np.rint(a) + 2.0,                 # 2,3,4 -> 4,5,6
+                             np.minimum(np.rint(a / 2.0), 3.0) + 4.0))  # 4,6 -> 6,7
+    return ((sign << 3) | code.astype(np.int64)).astype(np.uint8)
+
+
+def nvfp4_quantize(a: np.ndarray, glob: float):
+    """NVFP4-encode rows a [R, K] (values exact in fp32) with global scale
+    glob: per 16-element block the e4m3 scale of fp32(amax / fp32(6*glob)),
+    then the e2m1 code of fp32(v / fp32(scale*glob)) per element (code 0 when
+    scale*glob is 0).  Returns codes uint8 [R, K/2] (even k in the low nibble)
+    and scales uint8 [R, K/16]."""
+    a32 = np.asarray(a, dtype=np.float32)
+    R, K = a32.shape
+    g = np.float32(glob)
+    blocks = a32.reshape(R, K // 16, 16)
+    amax = np.abs(blocks).max(axis=2)
+    scales = e4m3_quantize(amax / (np.float32(6.0) * g))
+    denom = (e4m3_to_f64(scales).astype(np.float32) * g).astype(np.float32)
+    safe = np.where(denom > 0, denom, np.float32(1.0))[:, :, None]
+    q = (blocks / safe).astype(np.float32)
+    nib = np.where(denom[:, :, None] > 0, e2m1_quantize(q), 0).astype(np.uint8).reshape(R, K)
+    codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    return codes, scales
+
+
+def nvfp4_fake_quant(a: np.ndarray, glob: float) -> np.ndarray:
+    """Rows a [R, K] quantised to NVFP4 and decoded back to fp64."""
+    codes, scales = nvfp4_quantize(a, glob)
+    return nvfp4_dequant(codes[None], scales[None], np.array([glob], dtype=np.float32))[0]
+
+
+def bf16_round(a: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value (ties to even), via fp32
+    (an fp64 -> fp32 -> bf16 double rounding can only differ from a direct
+    rounding on values within 2^-24 relative of a bf16 midpoint)."""
+    b = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint32) << np.uint32(16)
+    return r.view(np.float32).astype(np.float64)
+
+
+def forward_w4a4(x_bits, gate_w_bits, bias, top_k, weights: ExpertWeights, x_global, h_global,
+                 tokens=None):
+    """The layer with NVFP4 weights and NVFP4 activations (the W4A4 reading in
+    the module docstring): routing and grouping as in ``forward``; for each
+    routed slot (t, s) of expert e the token row is quantised with
+    x_global[e], g and u are exact fp64 products of the decoded values,
+    h = bf16(silu(g) * u) is quantised with h_global[e], and y = W_down h.
+    The combine is step 7.  Returns the same dict as ``forward``."""
+    x = bf16_to_f64(x_bits)
+    gw = bf16_to_f64(gate_w_bits)
+    T, H = x.shape
+    E = gw.shape[0]
+    xg = np.asarray(x_global, dtype=np.float32)
+    hg = np.asarray(h_global, dtype=np.float32)
+    logits, idx, w = route(x, gw, bias, top_k)
+    counts, offsets, perm, inv_perm = permute(idx, E)
+    toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    y = {}
+    for e in np.unique(idx[toks].reshape(-1)):
+        slots = [(int(t), s) for t in toks for s in range(top_k) if idx[t, s] == e]
+        gu, dn = weights.get(int(e))
+        I = gu.shape[0] // 2
+        Xq = nvfp4_fake_quant(x[[t for t, _ in slots]], xg[e])
+        for (t, s), xr in zip(slots, Xq):
+            g = gu[:I] @ xr
+            u = gu[I:] @ xr
+            h = bf16_round(silu(g) * u)
+            hq = nvfp4_fake_quant(h[None, :], hg[e])[0]
+            y[(t, s)] = dn @ hq
+    out = np.zeros((len(toks), H), dtype=np.float64)
+    for i, t in enumerate(toks):
+        acc = np.zeros(H, dtype=np.float64)
         for s in range(top_k):
             acc = acc + w[t, s] * y[(int(t), s)]
         out[i] = acc

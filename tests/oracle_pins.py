@@ -149,6 +149,167 @@ def pin_nvfp4_forward_matches_bf16(o):
     assert np.array_equal(a["out"], b["out"]), np.abs(a["out"] - b["out"]).max()
 
 
+# ------------------------------------------------------------------ W4A4 quantiser
+
+def _torch_e4m3_bytes(v32):
+    import torch
+    return torch.from_numpy(np.asarray(v32, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_quantize_library(o):
+    """fp32 -> e4m3 rounding equals torch's float8_e4m3fn cast (round to
+    nearest even) on every e4m3 value, every midpoint between neighbours, the
+    subnormal range and random values below 464; above that the quantiser
+    saturates to 448 (0x7E) where the cast gives NaN."""
+    import torch
+    allv = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    pos = np.unique(allv[np.isfinite(allv) & (allv >= 0)]).astype(np.float64)
+    mids = (pos[:-1] + pos[1:]) / 2
+    rng = _rng(14)
+    vals = np.concatenate([pos, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                           np.nextafter(mids.astype(np.float32), np.float32(1e9)),
+                           rng.uniform(0, 2.0 ** -6, 500), rng.uniform(0, 463.9, 2000)]).astype(np.float32)
+    vals = np.concatenate([vals, -vals])
+    got = o.e4m3_quantize(vals)
+    exp = _torch_e4m3_bytes(vals)
+    bad = np.nonzero(got != exp)[0]
+    assert bad.size == 0, (vals[bad[:5]], got[bad[:5]], exp[bad[:5]])
+    sat = np.array([464.5, 500.0, 1e6, 3e38], dtype=np.float32)
+    assert (o.e4m3_quantize(sat) == 0x7E).all() and (o.e4m3_quantize(-sat) == 0xFE).all()
+
+
+def pin_e2m1_quantize_table(o):
+    """fp32 -> e2m1 rounding against the OCP FP4 E2M1 table: every table value
+    maps to its code, a midpoint between neighbours to the neighbour with the
+    even code, a value just past a midpoint to the upper neighbour, anything
+    at or above 6 to 6; negative values mirror positive ones."""
+    e2m1 = {c: _val(v) for c, v in _read_table("e2m1_codes.txt")}
+    mags = sorted((v, c) for c, v in e2m1.items() if c < 8)
+    for v, c in mags:
+        assert o.e2m1_quantize(np.array([v], dtype=np.float32))[0] == c, (v, c)
+        if v > 0:
+            assert o.e2m1_quantize(np.array([-v], dtype=np.float32))[0] == c | 8, (v, c)
+    for (v0, c0), (v1, c1) in zip(mags[:-1], mags[1:]):
+        mid = np.float32((v0 + v1) / 2)
+        even = c0 if c0 % 2 == 0 else c1
+        assert o.e2m1_quantize(np.array([mid], dtype=np.float32))[0] == even, (mid, even)
+        assert o.e2m1_quantize(np.array([-mid], dtype=np.float32))[0] == even | 8, (mid, even)
+        above = np.nextafter(mid, np.float32(10))
+        assert o.e2m1_quantize(np.array([above], dtype=np.float32))[0] == c1, (above, c1)
+        below = np.nextafter(mid, np.float32(-10))
+        assert o.e2m1_quantize(np.array([below], dtype=np.float32))[0] == c0, (below, c0)
+    big = np.array([6.0, 6.5, 7.0, 100.0, 3e38], dtype=np.float32)
+    assert (o.e2m1_quantize(big) == 7).all() and (o.e2m1_quantize(-big) == 15).all()
+
+
+def pin_nvfp4_quantize_blocks(o):
+    """NVFP4 encoding of activation rows, by brute force: per 16-element block
+    the scale byte is torch's e4m3 cast of fp32(amax / fp32(6*G)) (448 when
+    that quotient is beyond the format's range: one block here is); each
+    element's code (decoded with the format tables, even k in the low nibble)
+    is a nearest e2m1 value to fp32(v / fp32(scale*G)), ties to the even code,
+    saturating at 6; an all-zero block gets scale 0 and codes 0."""
+    e2m1 = {c: _val(v) for c, v in _read_table("e2m1_codes.txt")}
+    rng = _rng(15)
+    R, K = 5, 96
+    for G in (np.float32(0.0030517578), np.float32(1.0 / 3.0), np.float32(2.0 ** -7)):
+        a = o.bf16_to_f64(_rand_bf16(rng, (R, K), 1.0))
+        a[2, 16:32] = 0.0
+        a[3, 40] = 300.0          # a block whose scale is far above the others
+        codes, scales = o.nvfp4_quantize(a, G)
+        assert codes.shape == (R, K // 2) and scales.shape == (R, K // 16)
+        a32 = a.astype(np.float32)
+        for r in range(R):
+            for b in range(K // 16):
+                blk = a32[r, 16 * b:16 * b + 16]
+                amax = np.float32(np.abs(blk).max())
+                sv = np.float32(amax / np.float32(np.float32(6.0) * G))
+                # beyond 464 the cast gives NaN; the quantiser saturates to 448
+                exp_s = _torch_e4m3_bytes(np.array([sv]))[0] if sv < 464 else np.uint8(0x7E)
+                assert scales[r, b] == exp_s, (G, r, b, scales[r, b], exp_s)
+                sdec = np.float32(o.e4m3_to_f64(np.array([exp_s]))[0])
+                den = np.float32(sdec * G)
+                for i in range(16):
+                    kk = 16 * b + i
+                    byte = int(codes[r, kk // 2])
+                    nib = (byte & 0xF) if kk % 2 == 0 else (byte >> 4)
+                    if den == 0:
+                        assert nib == 0
+                        continue
+                    q = float(np.float32(blk[i] / den))
+                    got = e2m1[nib]
+                    best = min(abs(v - q) for v in e2m1.values())
+                    assert abs(got - q) == best, (G, r, kk, q, got)
+                    if abs(q) < 6 and sum(1 for c, v in e2m1.items() if abs(v - q) == best and
+                                          (v != 0 or c == (nib & 8))) > 1:
+                        assert nib % 2 == 0, (q, nib)        # a tie went to the even code
+                    if q != 0 and got != 0:
+                        assert (got < 0) == (q < 0)
+
+
+def pin_w4a4_forward_composition(o):
+    """The W4A4 layer on a tiny case equals its definition composed by hand:
+    routing as in the bf16 layer; per slot of expert e the token row
+    quantised with x_global[e] and decoded with the e2m1 table and torch's
+    e4m3 decoding; g and u
+    as exactly rounded sums (math.fsum) of the decoded products; h rounded to
+    bf16 by torch; h quantised with h_global[e]; y = W_down h in torch fp64;
+    the weighted sum over slots.  Globals differ per expert and between x and
+    h, so mixing them up changes the output."""
+    import torch
+    e2m1 = {c: _val(v) for c, v in _read_table("e2m1_codes.txt")}
+    e4m3 = {c: _val(v) for c, v in _read_table("e4m3_codes.txt")}
+    # every e4m3 byte decoded by torch's float8_e4m3fn (activation scales take
+    # any code, the table holds a sweep)
+    e4m3_all = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    rng = _rng(16)
+    T, H, E, k, I = 6, 32, 3, 2, 16
+    scale_codes = np.array([c for c, v in e4m3.items() if not math.isnan(v) and 2.0 ** -9 <= abs(v) <= 8],
+                           dtype=np.uint8)
+
+    def weights(R, K, glob):
+        codes = rng.integers(0, 256, size=(E, R, K // 2), dtype=np.uint8)
+        scales = rng.choice(scale_codes, size=(E, R, K // 16)).astype(np.uint8)
+        return codes, scales, glob
+
+    def decode(codes, scales, glob):   # [R, K/2], [R, K/16], float -> fp64 [R, K] via the tables
+        R, K2 = codes.shape
+        out = np.empty((R, 2 * K2))
+        for r in range(R):
+            for kk in range(2 * K2):
+                byte = int(codes[r, kk // 2])
+                nib = (byte & 0xF) if kk % 2 == 0 else (byte >> 4)
+                out[r, kk] = e2m1[nib] * e4m3_all[int(scales[r, kk // 16])] * float(glob)
+        return out
+
+    q_gu = weights(2 * I, H, np.array([0.75, 0.375, 1.5], dtype=np.float32))
+    q_dn = weights(H, I, np.array([0.5, 3.0, 0.1875], dtype=np.float32))
+    xg = np.array([0.0078125, 0.0055, 0.0021], dtype=np.float32)
+    hg = np.array([0.9, 0.41, 0.23], dtype=np.float32)
+    xb = _rand_bf16(rng, (T, H), 1.0)
+    gb = _rand_bf16(rng, (E, H), 0.5)
+    res = o.forward_w4a4(xb, gb, None, k, o.ExpertWeights(nvfp4_gate_up=q_gu, nvfp4_down=q_dn), xg, hg)
+    assert set(np.unique(res["idx"])) == set(range(E)), res["idx"]
+    x = o.bf16_to_f64(xb)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for s in range(k):
+            e = int(res["idx"][t, s])
+            gu = decode(q_gu[0][e], q_gu[1][e], q_gu[2][e])
+            dn = decode(q_dn[0][e], q_dn[1][e], q_dn[2][e])
+            xc, xs = o.nvfp4_quantize(x[t:t + 1], xg[e])
+            xq = decode(xc, xs, xg[e])[0]
+            g = np.array([math.fsum(gu[j] * xq) for j in range(I)])
+            u = np.array([math.fsum(gu[I + j] * xq) for j in range(I)])
+            h = torch.from_numpy(g / (1.0 + np.exp(-g)) * u).float().bfloat16().double().numpy()
+            hc, hs = o.nvfp4_quantize(h[None, :], hg[e])
+            hq = decode(hc, hs, hg[e])[0]
+            y = (torch.from_numpy(dn) @ torch.from_numpy(hq)).numpy()
+            ref[t] += res["w"][t, s] * y
+    assert np.allclose(res["out"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), \
+        np.abs(res["out"] - ref).max()
+
+
 # ------------------------------------------------------------------ router
 
 def pin_router_zero_gate(o):

@@ -194,6 +194,101 @@ def _mut_nvfp4_expert0_codes(m):
     m.ExpertWeights.get = get
 
 
+def _mut_w4a4_globals_swapped(m):
+    # the token rows quantised with h's global and h with x's
+    orig = m.forward_w4a4
+
+    def forward_w4a4(x_bits, gate_w_bits, bias, top_k, weights, x_global, h_global, tokens=None):
+        return orig(x_bits, gate_w_bits, bias, top_k, weights, h_global, x_global, tokens=tokens)
+    m.forward_w4a4 = forward_w4a4
+
+
+def _mut_w4a4_expert0_global(m):
+    # every expert quantises with expert 0's activation globals
+    orig = m.forward_w4a4
+
+    def forward_w4a4(x_bits, gate_w_bits, bias, top_k, weights, x_global, h_global, tokens=None):
+        xg = np.full_like(np.asarray(x_global), np.asarray(x_global)[0])
+        hg = np.full_like(np.asarray(h_global), np.asarray(h_global)[0])
+        return orig(x_bits, gate_w_bits, bias, top_k, weights, xg, hg, tokens=tokens)
+    m.forward_w4a4 = forward_w4a4
+
+
+def _mut_w4a4_h_unquantised(m):
+    # h goes to the down projection in bf16, without the NVFP4 step
+    def forward_w4a4(x_bits, gate_w_bits, bias, top_k, weights, x_global, h_global, tokens=None):
+        x = m.bf16_to_f64(x_bits)
+        logits, idx, w = m.route(x, m.bf16_to_f64(gate_w_bits), bias, top_k)
+        out = np.zeros_like(x)
+        for t in range(x.shape[0]):
+            for s in range(top_k):
+                e = int(idx[t, s])
+                gu, dn = weights.get(e)
+                I = gu.shape[0] // 2
+                xq = m.nvfp4_fake_quant(x[t:t + 1], np.asarray(x_global)[e])[0]
+                out[t] += w[t, s] * (dn @ m.bf16_round(m.silu(gu[:I] @ xq) * (gu[I:] @ xq)))
+        return dict(out=out, idx=idx, w=w, logits=logits)
+    m.forward_w4a4 = forward_w4a4
+
+
+def _mut_nvfp4_quant_block32(m):
+    # one scale per 32 elements: each pair of 16-element blocks shares the
+    # scale of the pair's larger magnitude
+    def nvfp4_quantize(a, glob):
+        a32 = np.asarray(a, dtype=np.float32)
+        R, K = a32.shape
+        g = np.float32(glob)
+        amax = np.repeat(np.abs(a32.reshape(R, K // 32, 32)).max(axis=2), 2, axis=1)
+        scales = m.e4m3_quantize(amax / (np.float32(6.0) * g))
+        denom = (m.e4m3_to_f64(scales).astype(np.float32) * g).astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = (a32.reshape(R, K // 16, 16) / denom[:, :, None]).astype(np.float32)
+        nib = np.where(denom[:, :, None] > 0, m.e2m1_quantize(q), 0).astype(np.uint8).reshape(R, K)
+        return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8), scales
+    m.nvfp4_quantize = nvfp4_quantize
+
+
+def _mut_e2m1_ties_away(m):
+    # ties rounded away from zero instead of to the even code
+    def e2m1_quantize(v):
+        f = np.asarray(v, dtype=np.float32)
+        a = np.abs(f.astype(np.float64))
+        grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+        d = np.abs(a[..., None] - grid)
+        best = d.min(axis=-1, keepdims=True)
+        code = (d == best)[..., ::-1].argmax(axis=-1)
+        code = 7 - code
+        return ((np.signbit(f).astype(np.int64) << 3) | code).astype(np.uint8)
+    m.e2m1_quantize = e2m1_quantize
+
+
+def _mut_e4m3_truncate(m):
+    # scales truncated toward zero instead of rounded to nearest
+    def e4m3_quantize(v):
+        a = np.abs(np.asarray(v, dtype=np.float32).astype(np.float64))
+        out = np.zeros(a.shape, dtype=np.uint8)
+        import torch
+        vals = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+        pos = [(float(vals[c]), c) for c in range(0x7F) if np.isfinite(vals[c])]
+        for i, x in np.ndenumerate(a):
+            out[i] = max(c for val, c in pos if val <= max(x, 0.0))
+        return out
+    m.e4m3_quantize = e4m3_quantize
+
+
+def _mut_nvfp4_scale_without_global(m):
+    # the block scale ignores the global: e4m3(amax / 6)
+    orig = m.nvfp4_quantize
+
+    def nvfp4_quantize(a, glob):
+        codes, _ = orig(a, glob)
+        a32 = np.asarray(a, dtype=np.float32)
+        R, K = a32.shape
+        amax = np.abs(a32.reshape(R, K // 16, 16)).max(axis=2)
+        return codes, m.e4m3_quantize(amax / np.float32(6.0))
+    m.nvfp4_quantize = nvfp4_quantize
+
+
 MUTANTS = [v for k, v in sorted(globals().items()) if k.startswith("_mut_")]
 
 
