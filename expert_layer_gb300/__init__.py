@@ -14,7 +14,8 @@ import os
 import torch
 
 __all__ = ["MoEError", "lib", "workspace_size", "alloc_workspace", "route", "permute", "forward",
-           "read_status", "read_diagnostics", "LIB_PATH"]
+           "read_status", "read_diagnostics", "LIB_PATH", "nvfp4_tc_scales", "nvfp4_quantize",
+           "W4A4Weights", "w4a4_weights", "forward_w4a4"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_gb300.so")
 
@@ -23,6 +24,13 @@ MOE_OK = 0
 
 class MoEError(RuntimeError):
     pass
+
+
+class _W4A4(ctypes.Structure):
+    _fields_ = [("gu_codes", ctypes.c_void_p), ("gu_scales_tc", ctypes.c_void_p),
+                ("gu_global", ctypes.c_void_p), ("dn_codes", ctypes.c_void_p),
+                ("dn_scales_tc", ctypes.c_void_p), ("dn_global", ctypes.c_void_p),
+                ("x_global", ctypes.c_void_p), ("h_global", ctypes.c_void_p)]
 
 
 class _NVFP4(ctypes.Structure):
@@ -46,6 +54,11 @@ _SIGNATURES = {
                                   _P, _P, _P, _SZ, _P, ctypes.POINTER(_P),
                                   ctypes.POINTER(ctypes.c_int32)]),
     "moe_route_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_forward_w4a4": (_I, [_P, _P, _P, ctypes.POINTER(_W4A4), _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_w4a4_profiled": (_I, [_P, _P, _P, ctypes.POINTER(_W4A4), _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                       _SZ, _P, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_int32)]),
+    "moe_nvfp4_tc_scales": (_I, [_P, _I, _I, _I, _I, _P, _P]),
+    "moe_nvfp4_quantize": (_I, [_P, _I, _I, ctypes.c_float, _P, _P, _P]),
     "moe_read_status": (_I, [_P, _P]),
     "moe_read_diagnostics": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_error_string": (ctypes.c_char_p, [_I]),
@@ -188,6 +201,83 @@ def forward(x, gate_w, bias, w_gate_up, w_down, top_k, nvfp4_gate_up=None, nvfp4
                            _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace),
                            workspace.numel(), _stream(stream))
     _check(rc, "moe_forward")
+    return out
+
+
+def nvfp4_tc_scales(scales, gate_up: bool, stream=None):
+    """NVFP4 block scales [E, rows, K/16] (uint8 e4m3) rearranged into the
+    W4A4 tensor-core layout (a new uint8 tensor of the same size)."""
+    E, rows, K16 = scales.shape
+    _want(scales, torch.uint8, (E, rows, K16), "scales")
+    out = torch.empty_like(scales)
+    _check(lib().moe_nvfp4_tc_scales(_ptr(scales), E, rows, 16 * K16, 1 if gate_up else 0, _ptr(out),
+                                     _stream(stream)), "moe_nvfp4_tc_scales")
+    return out
+
+
+def nvfp4_quantize(a, glob: float, stream=None):
+    """NVFP4-encode bf16 rows a [R, K] with global scale glob: returns
+    (codes uint8 [R, K/2], scales uint8 [R, K/16])."""
+    R, K = a.shape
+    _want(a, torch.bfloat16, (R, K), "a")
+    codes = torch.empty((R, K // 2), dtype=torch.uint8, device=a.device)
+    scales = torch.empty((R, K // 16), dtype=torch.uint8, device=a.device)
+    _check(lib().moe_nvfp4_quantize(_ptr(a), R, K, float(glob), _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_nvfp4_quantize")
+    return codes, scales
+
+
+class W4A4Weights:
+    """Expert weights of the W4A4 path: NVFP4 codes and globals, the block
+    scales in the tensor-core layout, and the activations' globals."""
+
+    def __init__(self, gate_up, down, x_global, h_global, stream=None):
+        self.gu_codes, self.gu_global = gate_up.codes, gate_up.glob
+        self.dn_codes, self.dn_global = down.codes, down.glob
+        self.gu_scales_tc = nvfp4_tc_scales(gate_up.scales, True, stream)
+        self.dn_scales_tc = nvfp4_tc_scales(down.scales, False, stream)
+        self.x_global, self.h_global = x_global, h_global
+        self.struct = _W4A4(*(t.data_ptr() for t in (self.gu_codes, self.gu_scales_tc, self.gu_global,
+                                                     self.dn_codes, self.dn_scales_tc, self.dn_global,
+                                                     self.x_global, self.h_global)))
+
+
+def w4a4_weights(inp, stream=None) -> W4A4Weights:
+    """W4A4Weights of a ``moe_inputs.MoEInputs`` bundle with NVFP4 weights and
+    activation globals."""
+    return W4A4Weights(inp.nvfp4_gate_up, inp.nvfp4_down, inp.x_global, inp.h_global, stream)
+
+
+def forward_w4a4(x, gate_w, bias, weights: W4A4Weights, top_k, out=None, workspace=None, topk_idx=None,
+                 topk_w=None, stream=None):
+    """The MoE layer forward with NVFP4 weights and NVFP4 activations; returns
+    out bf16 [T, H]."""
+    T, H = x.shape
+    E = gate_w.shape[0]
+    I = weights.gu_codes.shape[1] // 2
+    _want(x, torch.bfloat16, (T, H), "x")
+    _want(gate_w, torch.bfloat16, (E, H), "gate_w")
+    if bias is not None:
+        _want(bias, torch.float32, (E,), "bias")
+    _want(weights.gu_codes, torch.uint8, (E, 2 * I, H // 2), "gate_up codes")
+    _want(weights.gu_scales_tc, torch.uint8, (E, 2 * I, H // 16), "gate_up scales")
+    _want(weights.dn_codes, torch.uint8, (E, H, I // 2), "down codes")
+    _want(weights.dn_scales_tc, torch.uint8, (E, H, I // 16), "down scales")
+    for name in ("gu_global", "dn_global", "x_global", "h_global"):
+        _want(getattr(weights, name), torch.float32, (E,), name)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _want(out, torch.bfloat16, (T, H), "out")
+    if topk_idx is not None:
+        _want(topk_idx, torch.int32, (T, top_k), "topk_idx")
+    if topk_w is not None:
+        _want(topk_w, torch.float32, (T, top_k), "topk_w")
+    if workspace is None:
+        workspace = alloc_workspace(max(T, 1), H, E, I, top_k, x.device)
+    rc = lib().moe_forward_w4a4(_ptr(x), _ptr(gate_w), _ptr(bias), ctypes.byref(weights.struct), T, H, E, I,
+                                top_k, _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    _check(rc, "moe_forward_w4a4")
     return out
 
 

@@ -68,7 +68,12 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
   L.inv_perm = take(sizeof(int) * S);
   L.h = take(sizeof(uint16_t) * S * I);
   L.partial = take((L.partial_f32 ? 4 : 2) * (size_t)S * H);
-  L.xp = take(sizeof(uint16_t) * (size_t)S * H);   // token rows in grouped order (tensor-core path)
+  // token rows in grouped order (bf16 tensor-core path), or the W4A4 path's
+  // NVFP4 activations: codes [S, H/2] and [S, I/2] and their block scales in
+  // 128-row blocks per expert (at most S/128 + E + 1 blocks)
+  const size_t fp4 = (size_t)S * (H + I) / 2 + (size_t)(S / 128 + E + 1) * (size_t)((H + I) / 64) * 512 + 4 * 256;
+  const size_t xp = sizeof(uint16_t) * (size_t)S * H;
+  L.xp = take(xp > fp4 ? xp : fp4);
   L.x16 = take(sizeof(uint16_t) * (size_t)T * H);  // x in f16 (NVFP4 path)
   L.total = o;
   return L;

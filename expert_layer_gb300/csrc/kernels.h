@@ -104,6 +104,49 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int S, int H, int k,
                                uint16_t* xp, cudaStream_t stream, int* launches);
 
+// tc_fp4.cu -- W4A4: NVFP4 weights x NVFP4 activations on the block-scaled
+// tensor cores (tcgen05 kind::mxf4nvf4)
+struct Fp4Launch {
+  int T, H, E, I, k;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int32_t* active;     // active experts, ascending (all served here)
+  const int* num_active;
+  const uint8_t* gu_codes;   // [E, 2I, H/2]
+  const uint8_t* gu_scales_tc;
+  const float* gu_global;
+  const uint8_t* dn_codes;   // [E, H, I/2]
+  const uint8_t* dn_scales_tc;
+  const float* dn_global;
+  const float* x_global;     // [E]
+  const float* h_global;     // [E]
+  const uint8_t* xq;         // [S, H/2] token-row codes, grouped order
+  const uint8_t* xs;         // token-row scales, tensor-core layout
+  const uint8_t* hq;         // [S, I/2]
+  const uint8_t* hs;
+  const float* topk_w;
+  uint16_t* h;               // [S, I] bf16
+  void* partial;
+  bool partial_f32;
+  int* status;
+  int num_sms;
+};
+// bytes of the activation scales of S routed rows over E experts (128-row
+// blocks of each expert) for contraction length K
+inline size_t fp4_act_scale_bytes(long long S, long long E, long long K) {
+  return (size_t)(S / 128 + E + 1) * (size_t)(K / 64) * 512;
+}
+cudaError_t launch_quant_rows(bool gather, const uint16_t* src, const int32_t* perm, const int32_t* idx, int k,
+                              const int32_t* counts, const int32_t* offsets, int S, int K, int E,
+                              const float* glob, uint8_t* codes, uint8_t* sf, int* status, cudaStream_t stream,
+                              int* launches);
+cudaError_t launch_quant_plain(const uint16_t* src, int R, int K, float g, uint8_t* codes, uint8_t* scales,
+                               int* flag, cudaStream_t stream);
+cudaError_t launch_tc_scales(const uint8_t* in, int E, int R, int K, bool interleave, uint8_t* out,
+                             cudaStream_t stream);
+cudaError_t launch_tc_fp4(const Fp4Launch& p, bool down, cudaStream_t stream, int* launches);
+
 // combine.cu -- out[t] = sum_s partial[t*k+s] in slot order
 cudaError_t launch_combine(const void* partial, bool partial_f32, int T, int H, int k,
                            uint16_t* out, int num_sms, cudaStream_t stream, int* launches);

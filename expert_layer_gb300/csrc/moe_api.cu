@@ -301,6 +301,140 @@ int moe_forward_profiled(const uint16_t* x, const uint16_t* gate_w, const float*
   return rc;
 }
 
+// ------------------------------------------------------------------ W4A4
+static int check_w4a4_shape(int H, int I) {
+  // 256-wide K stages (H, I) and 128-row weight blocks; scale rows of H/16 and
+  // I/16 bytes whose 64-wide K steps are whole 4-byte words
+  return (H % 256 == 0 && I % 256 == 0) ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+static int w4a4_impl(const uint16_t* x, const uint16_t* gate_w, const float* bias, const moe_w4a4_weights* wq,
+                     int T, int H, int E, int I, int top_k, uint16_t* out, int32_t* topk_idx, float* topk_w,
+                     void* workspace, size_t workspace_bytes, void* stream, void* const* events, int* launches) {
+  MOE_TRY(check_shape(T, H, E, I, top_k));
+  if (T == 0) return MOE_OK;
+  if (!wq) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_w4a4_shape(H, I));
+  MOE_TRY(check_ptr(x));
+  MOE_TRY(check_ptr(gate_w));
+  MOE_TRY(check_ptr(out));
+  MOE_TRY(check_ptr(workspace));
+  if (bias && !aligned16(bias)) return MOE_ERR_UNSUPPORTED;
+  if (topk_idx && !aligned16(topk_idx)) return MOE_ERR_UNSUPPORTED;
+  if (topk_w && !aligned16(topk_w)) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_ptr(wq->gu_codes));
+  MOE_TRY(check_ptr(wq->gu_scales_tc));
+  MOE_TRY(check_ptr(wq->gu_global));
+  MOE_TRY(check_ptr(wq->dn_codes));
+  MOE_TRY(check_ptr(wq->dn_scales_tc));
+  MOE_TRY(check_ptr(wq->dn_global));
+  MOE_TRY(check_ptr(wq->x_global));
+  MOE_TRY(check_ptr(wq->h_global));
+  const WsLayout L = make_layout(T, H, E, I, top_k);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  int num_sms = 0;
+  MOE_TRY(check_device(&num_sms));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long long S = (long long)T * top_k;
+
+  int32_t* idx = topk_idx ? topk_idx : ws_ptr<int32_t>(workspace, L.idx);
+  float* w = topk_w ? topk_w : ws_ptr<float>(workspace, L.w);
+  int32_t* counts = ws_ptr<int32_t>(workspace, L.counts);
+  int32_t* offsets = ws_ptr<int32_t>(workspace, L.offsets);
+  int32_t* perm = ws_ptr<int32_t>(workspace, L.perm);
+  int32_t* inv_perm = ws_ptr<int32_t>(workspace, L.inv_perm);
+  WsHeader* hdr = ws_ptr<WsHeader>(workspace, L.hdr);
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+  };
+  // NVFP4 activations in the token-row region: codes, then 256-aligned scales
+  uint8_t* xq = ws_ptr<uint8_t>(workspace, L.xp);
+  uint8_t* hq = xq + align256((size_t)S * H / 2);
+  uint8_t* xs = hq + align256((size_t)S * I / 2);
+  uint8_t* hs = xs + align256(fp4_act_scale_bytes(S, E, H));
+
+  MOE_TRY_CUDA(mark(0));
+  MOE_TRY_CUDA(launch_zero(workspace, zeroed_prefix(L), s));
+  if (launches) *launches += 1;
+  MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches, nullptr));
+  MOE_TRY_CUDA(mark(1));
+  // every active expert is served by the tensor cores (128-row blocks)
+  MOE_TRY_CUDA(launch_permute(idx, T, E, top_k, counts, offsets, perm, inv_perm, workspace, L, 1, kTcRows, s,
+                              launches));
+  MOE_TRY_CUDA(mark(2));
+  MOE_TRY_CUDA(launch_quant_rows(true, x, perm, idx, top_k, counts, offsets, (int)S, H, E, wq->x_global, xq, xs,
+                                 &hdr->status, s, launches));
+  MOE_TRY_CUDA(mark(3));
+  Fp4Launch p{};
+  p.T = T; p.H = H; p.E = E; p.I = I; p.k = top_k;
+  p.counts = counts; p.offsets = offsets; p.perm = perm;
+  p.active = ws_ptr<int32_t>(workspace, L.active);
+  p.num_active = &hdr->num_active;
+  p.gu_codes = wq->gu_codes; p.gu_scales_tc = wq->gu_scales_tc; p.gu_global = wq->gu_global;
+  p.dn_codes = wq->dn_codes; p.dn_scales_tc = wq->dn_scales_tc; p.dn_global = wq->dn_global;
+  p.x_global = wq->x_global; p.h_global = wq->h_global;
+  p.xq = xq; p.xs = xs; p.hq = hq; p.hs = hs;
+  p.topk_w = w;
+  p.h = ws_ptr<uint16_t>(workspace, L.h);
+  p.partial = ws_ptr<void>(workspace, L.partial);
+  p.partial_f32 = L.partial_f32;
+  p.status = &hdr->status;
+  p.num_sms = num_sms;
+  MOE_TRY_CUDA(launch_tc_fp4(p, false, s, launches));
+  MOE_TRY_CUDA(launch_quant_rows(false, p.h, perm, idx, top_k, counts, offsets, (int)S, I, E, wq->h_global, hq, hs,
+                                 &hdr->status, s, launches));
+  MOE_TRY_CUDA(launch_tc_fp4(p, true, s, launches));
+  MOE_TRY_CUDA(mark(4));
+  MOE_TRY_CUDA(launch_combine(p.partial, L.partial_f32, T, H, top_k, out, num_sms, s, launches));
+  MOE_TRY_CUDA(mark(5));
+  return MOE_OK;
+}
+
+int moe_forward_w4a4(const uint16_t* x, const uint16_t* gate_w, const float* bias, const moe_w4a4_weights* w,
+                     int T, int H, int E, int I, int top_k, uint16_t* out, int32_t* topk_idx, float* topk_w,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  return w4a4_impl(x, gate_w, bias, w, T, H, E, I, top_k, out, topk_idx, topk_w, workspace, workspace_bytes,
+                   stream, nullptr, nullptr);
+}
+
+int moe_forward_w4a4_profiled(const uint16_t* x, const uint16_t* gate_w, const float* bias,
+                              const moe_w4a4_weights* w, int T, int H, int E, int I, int top_k, uint16_t* out,
+                              int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+                              void* stream, void* const* events, int32_t* kernels_launched) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  int n = 0;
+  const int rc = w4a4_impl(x, gate_w, bias, w, T, H, E, I, top_k, out, topk_idx, topk_w, workspace,
+                           workspace_bytes, stream, events, &n);
+  if (kernels_launched) *kernels_launched = n;
+  return rc;
+}
+
+int moe_nvfp4_tc_scales(const uint8_t* scales, int E, int rows, int K, int gate_up, uint8_t* out, void* stream) {
+  if (E <= 0 || rows <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 != 0 || K % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (gate_up && rows % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_ptr(scales));
+  MOE_TRY(check_ptr(out));
+  MOE_TRY(check_device(nullptr));
+  return cuda_status(launch_tc_scales(scales, E, rows, K, gate_up != 0, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_nvfp4_quantize(const uint16_t* a, int R, int K, float global, uint8_t* codes, uint8_t* scales,
+                       void* stream) {
+  if (R < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!(global > 0.0f) || !(global < 3.0e38f)) return MOE_ERR_INVALID_ARG;
+  if (R == 0) return MOE_OK;
+  MOE_TRY(check_ptr(a));
+  MOE_TRY(check_ptr(codes));
+  MOE_TRY(check_ptr(scales));
+  MOE_TRY(check_device(nullptr));
+  return cuda_status(launch_quant_plain(a, R, K, global, codes, scales, nullptr,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_read_status(const void* workspace, void* stream) {
   if (!workspace) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

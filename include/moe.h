@@ -205,6 +205,86 @@ int moe_read_diagnostics(const void *workspace, void *stream, int32_t *out4);
 int moe_route_noalloc(const uint16_t *x, const uint16_t *gate_w, const float *bias, int T, int H,
                       int E, int top_k, int32_t *topk_idx, float *topk_w, void *stream);
 
+/*
+ * ------------------------------------------------------------------ W4A4
+ * NVFP4 weights AND NVFP4 activations on the block-scaled tensor cores
+ * (e2m1 x e2m1 products, one e4m3 scale per 16 elements along K on both
+ * operands, fp32 accumulate).  The pages' NVFP4 deployment is the 176B MoE of
+ * page "vLLM 0.32 升级试验：TEP2 prefill 诅咒解除 + decode 本机纪录" (header,
+ * "背景与动机"); the pages give no activation numerics, so the activations are
+ * quantised with the format's own recipe, per routed row of expert e:
+ *   16-element blocks along K (H for the token rows, I for h),
+ *   block scale  s = e4m3(amax / (6 G))           round to nearest even, <= 448
+ *   element code   = e2m1(v / (s G))              round to nearest even, |.| <= 6
+ *   (0 for every element of a block whose s G is 0)
+ * with G = x_global[e] for the token rows and G = h_global[e] for the SwiGLU
+ * output h = bf16(silu(g) * u); every quotient and product in fp32 with IEEE
+ * rounding.  Then g, u = dequant(W_gu) dequant(x_q), y = dequant(W_dn)
+ * dequant(h_q), and the combine as in moe_forward.
+ *
+ * Weights: codes and globals as in moe_nvfp4_weights; the block scales in the
+ * tensor-core layout written by moe_nvfp4_tc_scales (done once, when the
+ * weights are loaded).  x_global, h_global: [E] fp32, positive and finite
+ * (device pointers), the activations' NVFP4 global scales (as NVFP4
+ * checkpoints store calibrated input scales).
+ * Shapes: H and I multiples of 256.  The output is out [T, H] bf16; an
+ * activation that is not finite is recorded as MOE_ERR_DEVICE.
+ */
+typedef struct {
+  const uint8_t *gu_codes;      /* [E, 2I, H/2] */
+  const uint8_t *gu_scales_tc;  /* moe_nvfp4_tc_scales(gu_scales, E, 2I, H, 1, ...) */
+  const float *gu_global;       /* [E] */
+  const uint8_t *dn_codes;      /* [E, H, I/2] */
+  const uint8_t *dn_scales_tc;  /* moe_nvfp4_tc_scales(dn_scales, E, H, I, 0, ...) */
+  const float *dn_global;       /* [E] */
+  const float *x_global;        /* [E] */
+  const float *h_global;        /* [E] */
+} moe_w4a4_weights;
+
+/*
+ * Rearranges NVFP4 block scales [E, rows, K/16] (row-major e4m3 bytes, as in
+ * moe_nvfp4_weights) into the layout the W4A4 tensor-core kernels read: for
+ * each block of 128 rows and each 64-wide step of K, a 512-byte atom of 32
+ * rows x 16 bytes whose row i, bytes 4j..4j+3, holds the 4 scales of row
+ * i + 32j; atoms ordered by (row block, K step).  With gate_up != 0 the
+ * tensor is w_gate_up's (rows = 2I) and the rows of each 128-row block are
+ * gate and up rows interleaved: row 2jj is gate row j0 + jj, row 2jj+1 up row
+ * I + j0 + jj (j0 = 64 * block).  `out` has the same size as `scales`
+ * (E * rows * K / 16 bytes).  rows % 128 == 0 (gate_up: % 256), K % 64 == 0.
+ * Enqueues on `stream`.
+ */
+int moe_nvfp4_tc_scales(const uint8_t *scales, int E, int rows, int K, int gate_up, uint8_t *out,
+                        void *stream);
+
+/*
+ * The W4A4 layer forward (see above).  Arguments as moe_forward, with the
+ * W4A4 weights in place of the bf16 / NVFP4 ones; workspace of
+ * moe_workspace_size(T, H, E, I, top_k) bytes.
+ */
+int moe_forward_w4a4(const uint16_t *x, const uint16_t *gate_w, const float *bias,
+                     const moe_w4a4_weights *w, int T, int H, int E, int I, int top_k, uint16_t *out,
+                     int32_t *topk_idx, float *topk_w, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
+ * moe_forward_w4a4 with timing hooks, as moe_forward_profiled; the events
+ * mark [0] start [1] routing [2] grouping [3] token rows quantised
+ * [4] gate/up, h quantised, down [5] combine.
+ */
+int moe_forward_w4a4_profiled(const uint16_t *x, const uint16_t *gate_w, const float *bias,
+                              const moe_w4a4_weights *w, int T, int H, int E, int I, int top_k,
+                              uint16_t *out, int32_t *topk_idx, float *topk_w, void *workspace,
+                              size_t workspace_bytes, void *stream, void *const *events,
+                              int32_t *kernels_launched);
+
+/*
+ * The activation quantiser of the W4A4 path on its own: rows a [R, K] (bf16)
+ * with one global G -> codes [R, K/2] (two e2m1 codes per byte, even k in the
+ * low nibble) and scales [R, K/16] (e4m3, row-major).  K % 64 == 0, G > 0.
+ */
+int moe_nvfp4_quantize(const uint16_t *a, int R, int K, float global, uint8_t *codes, uint8_t *scales,
+                       void *stream);
+
 /* Static, human-readable name of a moe_status value. */
 const char *moe_error_string(int status);
 
