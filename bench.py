@@ -48,10 +48,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HEADLINE = "decode8"
-CONFIGS = ["decode8", "decode64", "prefill8192", "nvfp4_256", "tiny"]
+CONFIGS = ["decode8", "decode64", "prefill8192", "nvfp4_256", "tiny", "prefill8192_w4a4"]
 WEIGHT_SETS = 4
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ["route", "permute", "stream", "tc", "combine"]
+# W4A4: the third boundary is the end of the token-row quantisation
+STAGES_W4A4 = ["route", "permute", "quant_x", "tc", "combine"]
+# nominal dense FP4 / bf16 tensor throughput of GB300 (13.5 / 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0
 TOL = {"bf16": 1e-2, "nvfp4": 3e-2}   # max|out - ref| <= TOL * max|ref|
 
 
@@ -224,8 +228,9 @@ def group_split(inp, counts):
     threshold rule as the library."""
     T, H, k = inp.T, inp.H, inp.top_k
     thr = 32 if T * k >= 8192 else 65
-    use_tc = inp.nvfp4_gate_up is None and T >= thr and H % 256 == 0
-    tc_all = use_tc and T * k >= 8192
+    w4a4 = getattr(inp, "x_global", None) is not None   # every group on the block-scaled tensor cores
+    use_tc = w4a4 or (inp.nvfp4_gate_up is None and T >= thr and H % 256 == 0)
+    tc_all = use_tc and (w4a4 or T * k >= 8192)
     act = [int(c) for c in counts if c > 0]
     large = [c for c in act if use_tc and (tc_all or c >= thr)]
     small = [c for c in act if not (use_tc and (tc_all or c >= thr))]
@@ -244,7 +249,8 @@ def algorithmic_bytes(inp, split):
         "route": E * H * 2 + T * H * 2 + S * 8,
         "permute": S * 4 * 4 + E * 12,
         "stream": split["A_s"] * 3 * I * H * wb + split["S_s"] * per_row,
-        "tc": split["A_l"] * 3 * I * H * 2 + split["S_l"] * per_row,
+        "tc": split["A_l"] * 3 * I * H * wb + split["S_l"] * per_row,
+        "quant_x": S * H * 2 + S * H * (0.5 + 1.0 / 16),
         "combine": S * H * pb + T * H * 2,
         "weights": A * 3 * I * H * wb,
     }
@@ -274,9 +280,14 @@ if meta["nvfp4"]:
 else:
     W = oracle.ExpertWeights(ld("w_gate_up"), ld("w_down"))
 x, gw, k = np.array(ld("x")), np.array(ld("gate_w")), meta["top_k"]
+if meta.get("w4a4"):
+    xg, hg = np.array(ld("x_global")), np.array(ld("h_global"))
+    fwd = lambda xx, tokens=None: oracle.forward_w4a4(xx, gw, bias, k, W, xg, hg, tokens=tokens)
+else:
+    fwd = lambda xx, tokens=None: oracle.forward(xx, gw, bias, k, W, tokens=tokens)
 if job["mode"] == "parity":
     # whole-batch routing and grouping, outputs of the sampled rows
-    r = oracle.forward(x, gw, bias, k, W, tokens=job["rows"])
+    r = fwd(x, tokens=job["rows"])
     np.savez(os.path.join(d, "parity.npz"), **{n: r[n] for n in
              ("out", "idx", "w", "counts", "offsets", "perm", "inv_perm")})
     print(json.dumps({"ok": True}))
@@ -294,7 +305,7 @@ while not os.path.exists(os.path.join(d, "go_" + job["tag"])):
     time.sleep(0.005)
 t0 = time.perf_counter(); reps = 0
 while True:
-    r = oracle.forward(xs, gw, bias, k, W)
+    r = fwd(xs)
     reps += 1
     if time.perf_counter() - t0 >= job["budget"] or reps >= job["max_reps"]:
         break
@@ -327,9 +338,13 @@ def dump_inputs(inp, d):
     else:
         save("w_gate_up", mi.bf16_bits(inp.w_gate_up))
         save("w_down", mi.bf16_bits(inp.w_down))
+    w4a4 = getattr(inp, "x_global", None) is not None
+    if w4a4:
+        save("x_global", inp.x_global.cpu().numpy())
+        save("h_global", inp.h_global.cpu().numpy())
     with open(os.path.join(d, "meta.json"), "w") as f:
         json.dump({"bias": inp.bias is not None, "nvfp4": inp.nvfp4_gate_up is not None,
-                   "top_k": inp.top_k}, f)
+                   "top_k": inp.top_k, "w4a4": w4a4}, f)
 
 
 def _child(d, job):
@@ -474,10 +489,19 @@ def measure(name, args, ctx, headline):
     nv = inp.nvfp4_gate_up is not None
 
     # weight sets cycled across steps
+    w4a4 = inp.x_global is not None
+    stages = STAGES_W4A4 if w4a4 else STAGES
     sets = []
     nsets = max(1, args.weight_sets)
     for r in range(nsets):
-        if nv:
+        if w4a4:
+            q = inp.nvfp4_gate_up if r == 0 else moe_inputs.NVFP4Tensor(
+                inp.nvfp4_gate_up.codes.clone(), inp.nvfp4_gate_up.scales, inp.nvfp4_gate_up.glob.clone())
+            d = inp.nvfp4_down if r == 0 else moe_inputs.NVFP4Tensor(
+                inp.nvfp4_down.codes.clone(), inp.nvfp4_down.scales, inp.nvfp4_down.glob.clone())
+            wq = moe.W4A4Weights(q, d, inp.x_global, inp.h_global)
+            sets.append((None, None, ctypes.byref(wq.struct), (q, d, wq)))
+        elif nv:
             q = inp.nvfp4_gate_up if r == 0 else moe_inputs.NVFP4Tensor(
                 inp.nvfp4_gate_up.codes.clone(), inp.nvfp4_gate_up.scales.clone(), inp.nvfp4_gate_up.glob.clone())
             d = inp.nvfp4_down if r == 0 else moe_inputs.NVFP4Tensor(
@@ -504,15 +528,22 @@ def measure(name, args, ctx, headline):
 
     def step(i, xp=x_p, op=o_p):
         gu, dn, nvp, _ = sets[i % nsets]
-        rc = lib.moe_forward(xp, g_p, b_p, gu, dn, nvp, T, H, E, I, k, op, None, None, ws_p, wsn, sptr)
+        if w4a4:
+            rc = lib.moe_forward_w4a4(xp, g_p, b_p, nvp, T, H, E, I, k, op, None, None, ws_p, wsn, sptr)
+        else:
+            rc = lib.moe_forward(xp, g_p, b_p, gu, dn, nvp, T, H, E, I, k, op, None, None, ws_p, wsn, sptr)
         if rc != 0:
             raise moe.MoEError(lib.moe_error_string(rc).decode())
 
     # ---- 1. one forward, the parity gate, and (rank 0, one GPU) the CPU baselines
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     wts = torch.empty((T, k), dtype=torch.float32, device=dev)
-    moe.forward(inp.x, inp.gate_w, inp.bias, inp.w_gate_up, inp.w_down, k, nvfp4_gate_up=inp.nvfp4_gate_up,
-                nvfp4_down=inp.nvfp4_down, out=out, workspace=ws, topk_idx=idx, topk_w=wts)
+    if w4a4:
+        moe.forward_w4a4(inp.x, inp.gate_w, inp.bias, sets[0][3][2], k, out=out, workspace=ws, topk_idx=idx,
+                         topk_w=wts)
+    else:
+        moe.forward(inp.x, inp.gate_w, inp.bias, inp.w_gate_up, inp.w_down, k, nvfp4_gate_up=inp.nvfp4_gate_up,
+                    nvfp4_down=inp.nvfp4_down, out=out, workspace=ws, topk_idx=idx, topk_w=wts)
     status = moe.read_status(ws)
     diag = moe.read_diagnostics(ws)
     grp = moe.permute(idx, E)
@@ -577,12 +608,17 @@ def measure(name, args, ctx, headline):
     nk = ctypes.c_int32(0)
     for i in range(K2):
         gu, dn, nvp, _ = sets[i % nsets]
-        rc = lib.moe_forward_profiled(x_p, g_p, b_p, gu, dn, nvp, T, H, E, I, k, o_p, None, None, ws_p,
-                                      wsn, sptr, ev_ptrs[i], ctypes.byref(nk))
+        if w4a4:
+            rc = lib.moe_forward_w4a4_profiled(x_p, g_p, b_p, nvp, T, H, E, I, k, o_p, None, None, ws_p, wsn,
+                                               sptr, ev_ptrs[i], ctypes.byref(nk))
+        else:
+            rc = lib.moe_forward_profiled(x_p, g_p, b_p, gu, dn, nvp, T, H, E, I, k, o_p, None, None, ws_p,
+                                          wsn, sptr, ev_ptrs[i], ctypes.byref(nk))
         assert rc == 0
     torch.cuda.synchronize()
     stage_ms = {s: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K2))
-                for j, s in enumerate(STAGES)}
+                for j, s in enumerate(stages)}
+    stage_ms.setdefault("stream", 0.0)
     kernels_per_step = nk.value
 
     # ---- 4b. end to end through the C ABI with host buffers: every step copies
@@ -635,18 +671,22 @@ def measure(name, args, ctx, headline):
     peaks, peak_src = load_peaks()
     byt = algorithmic_bytes(inp, split)
     flops = algorithmic_flops(inp, split)
-    dom = max(("stream", "tc", "route", "combine", "permute"), key=lambda s: stage_ms[s])
+    dom = max(stage_ms, key=lambda s: stage_ms[s])
     dom_s = stage_ms[dom] / 1e3
     src = f"{peak_src} MEASURED_PEAKS.json" if peak_src == "measured" else "fallback"
     if dom == "tc":
         # the tensor-core kernels run for well under a millisecond per step:
-        # the burst peak is the denominator; the sustained one is shown too
-        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        # the burst peak is the denominator; the sustained one is shown too.
+        # FP4 x FP4 takes the bf16 peak times the nominal FP4 / bf16 ratio.
+        ratio = FP4_OVER_BF16 if w4a4 else 1.0
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * ratio
+        sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * ratio
         achieved = flops[dom] / dom_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": measured_traffic(wname, dom),
-                "peak_source": f"{src} (bf16 burst)", "frac_of_sustained": achieved / sus}
+                "peak_source": (f"{src} (bf16 burst x {FP4_OVER_BF16:g}, the nominal dense FP4 / bf16 ratio)"
+                                if w4a4 else f"{src} (bf16 burst)"),
+                "frac_of_sustained": achieved / sus}
     else:
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         achieved = byt[dom] / dom_s / 1e9
@@ -664,20 +704,22 @@ def measure(name, args, ctx, headline):
     layer = {"weights_bytes": byt["weights"], "weights_gbs": byt["weights"] / (step_ms / 1e3) / 1e9,
              "weights_frac_of_hbm": byt["weights"] / (step_ms / 1e3) / 1e9 / hbm,
              "active_experts": diag["num_active"], "groups": split,
-             "stage_us": {s: round(stage_ms[s] * 1e3, 2) for s in STAGES}, "router": router_diag}
+             "stage_us": {s: round(stage_ms[s] * 1e3, 2) for s in stages}, "router": router_diag}
     if split["S_l"] > 0:
         layer["flops"] = 2 * T * k * 3 * I * H + 2 * T * E * H
         layer["tflops"] = layer["flops"] / (step_ms / 1e3) / 1e12
         layer["frac_of_bf16_burst"] = layer["tflops"] / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        if w4a4:
+            layer["frac_of_fp4_burst"] = layer["frac_of_bf16_burst"] / FP4_OVER_BF16
     rec = {
         "value": value if passed_all else None,
         "unit": "tokens/s",
         "steps": K,
         "warmup": W,
         "ms_per_step": step_ms,
-        "dtype": "nvfp4-w4a16/bf16/f32acc" if nv else "bf16/f32acc",
+        "dtype": "nvfp4-w4a4/f32acc" if w4a4 else "nvfp4-w4a16/bf16/f32acc" if nv else "bf16/f32acc",
         "config": {"workload": wname, "T": T, "H": H, "E": E, "top_k": k, "I": I,
-                   "weights": "nvfp4" if nv else "bf16",
+                   "weights": "nvfp4" if nv else "bf16", "activations": "nvfp4" if w4a4 else "bf16",
                    "router_bias": "0.5*log-Zipf(1.1)" if inp.bias is not None else None,
                    "seed": args.seed, "parallelism": f"replicas x{world}",
                    "l2": f"{nsets} rotating expert-weight sets of {weight_bytes_per_set / 1e9:.3f} GB "

@@ -101,7 +101,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the hardware exponential and an approximate
+// division: relative error of a few 1e-7, far below the bf16 (or f16, or
+// NVFP4) rounding that h receives next; for z < -87 the quotient is 0.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // mma.sync m16n8k16, bf16 inputs, fp32 accumulate (in place).
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,

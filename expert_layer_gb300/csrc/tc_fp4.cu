@@ -8,9 +8,9 @@
 // cores.  Here the activations are quantised on the fly with the format's
 // own recipe, per routed row of expert e: 16-element blocks along K, block
 // scale s = e4m3_rn_satfinite(amax / (6 G)), element code
-// e2m1_rn_satfinite(v / (s G)), with G = x_global[e] for the token rows and
-// G = h_global[e] for the SwiGLU output (each quotient and product in fp32,
-// IEEE round to nearest).
+// e2m1_rn_satfinite(v * r) with r = 1 / (s G) once per block, G = x_global[e]
+// for the token rows and G = h_global[e] for the SwiGLU output (each
+// quotient, reciprocal and product in fp32, IEEE round to nearest).
 //
 // Pipeline of one W4A4 layer (after routing and grouping):
 //   quant x      token rows in grouped order -> e2m1 codes [S, H/2] and block
@@ -35,14 +35,26 @@
 // written in it by the quantiser, with blocks of 128 rows of one expert
 // (block = the expert's first block + row within the expert / 128).
 //
-// GEMM kernel: one persistent CTA per SM, 10 warps:
+// GEMM kernel: one persistent CTA per SM, 14 warps:
 //   warp 0      one thread issues the TMA loads (codes: tiled, 128-byte
 //               swizzle) and bulk copies (scale atoms) of a 5-stage ring
-//   warp 1      allocates tensor memory; one thread issues, per 256-wide K
-//               stage, four tcgen05.cp per operand and four MMAs
-//               (M = 128 weight rows, N = the tile's token rows rounded up to
-//               16, K = 64 each)
-//   warps 2-9   epilogue: two warps per TMEM lane quadrant, alternate
+//   warp 1      allocates tensor memory; one thread issues four MMAs per
+//               256-wide K stage (M = 128 weight rows, N = the tile's token
+//               rows rounded up to 16, K = 64 each)
+//   warps 2-5   scale warps, one per TMEM lane quadrant: they read a stage's
+//               scale atoms from shared memory and write them into tensor
+//               memory with tcgen05.st, then signal the MMA thread.  (A
+//               tcgen05.cp of an atom costs ~53 cycles of the same pipe as
+//               the MMAs, ~65 cycles for a 128 x 128 x 64 FP4 MMA: copying
+//               the eight atoms of a stage that way took more pipe time than
+//               its four MMAs.)  The MMA reads A row m's scales of K step kk
+//               at (lane m, column sa + 4kk + m/32) and B column n's at
+//               (lane 32q + n%32, column sb + 4kk + n/32) for the
+//               accumulator lanes of quadrant q, so quadrant q writes, in its
+//               own lanes, A's scales at columns sa + 4kk + q (zeros in the
+//               other columns of the 16, which only other quadrants read in
+//               their own lanes) and the full 16 columns of B's.
+//   warps 6-13  epilogue: two warps per TMEM lane quadrant, alternate
 //               32-column chunks
 // Two 128-column accumulators let the epilogue of one tile overlap the
 // mainloop of the next.  Every mbarrier wait is bounded; a timeout sets
@@ -66,8 +78,9 @@ constexpr int kAtomBytes = 512;                     // scales of 128 rows x one 
 constexpr int kSfBytes = 4 * kAtomBytes;            // per operand per stage
 constexpr int kStage = 2 * kCodeBytes + 2 * kSfBytes;   // 36 KB
 constexpr int NSF = 5;
+constexpr int kSfWarps = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kThreads = (2 + kSfWarps + kEpiWarps) * 32;
 constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kSfColBase = 2 * kAccCols;       // scale columns after the two accumulators
 constexpr uint32_t kSfColsStage = 32;               // SFA 16 + SFB 16 per stage
@@ -112,19 +125,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
       : "memory");
 }
-// shared-memory matrix descriptor, no swizzle: 8-row x 16-byte core matrices,
-// 8-row groups 128 bytes apart (a dense [rows][16 B] array)
-__device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
-  d |= (uint64_t)(128 >> 4) << 16;
-  d |= (uint64_t)(128 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  return d;
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
-__device__ __forceinline__ void sf_copy(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void mma_fp4(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t sfa, uint32_t sfb, uint32_t accum) {
   asm volatile(
@@ -170,44 +179,60 @@ __device__ __forceinline__ size_t tc_scale_offset(size_t blk, int row, int kb, i
 }
 
 // One row of K values (bf16 bits) to NVFP4 with global g: one warp; lane l
-// takes the 16-element blocks l, l + 32, ...  Codes are written to
-// codes[0 .. K/2); scale bytes via put_scale(kb, byte) (4 consecutive blocks'
-// bytes gathered in lane 4w, written as one 32-bit word by put_word(w4, word)).
+// takes the 16-element blocks l, l + 32, ..., loading up to four of them
+// before converting any (the rows come from L2: several requests in flight
+// per lane).  Codes are written to codes[0 .. K/2); the scale bytes of 4
+// consecutive blocks (one 64-wide K step) are gathered in lane 4w and
+// written as one 32-bit word by put_word(step, word).
 template <typename PutWord>
 __device__ __forceinline__ bool quantize_row(const uint16_t* __restrict__ src, int K, float g,
                                              uint8_t* __restrict__ codes, PutWord put_word) {
   const int lane = threadIdx.x & 31;
   const float g6 = __fmul_rn(6.0f, g);
+  const int nb = K / 16;
   bool bad = false;
-  for (int kb0 = 0; kb0 < K / 16; kb0 += 32) {
-    const int kb = kb0 + lane;
-    uint32_t sbyte = 0;
-    if (kb < K / 16) {
-      const uint4 p0 = *reinterpret_cast<const uint4*>(src + (size_t)kb * 16);
-      const uint4 p1 = *reinterpret_cast<const uint4*>(src + (size_t)kb * 16 + 8);
-      const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-      float v[16];
+  for (int kb0 = 0; kb0 < nb; kb0 += 128) {
+    uint4 p[4][2];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { v[2 * i] = bf16lo(w[i]); v[2 * i + 1] = bf16hi(w[i]); }
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-      bad |= !(amax <= 3.0e38f);
-      sbyte = f32_to_e4m3(__fdiv_rn(amax, g6));
-      const float den = __fmul_rn(e4m3_to_f32(sbyte), g);
-      uint32_t c[2] = {0u, 0u};
-      if (den > 0.f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          c[i >> 2] |= f32x2_to_e2m1x2(__fdiv_rn(v[2 * i], den), __fdiv_rn(v[2 * i + 1], den)) << (8 * (i & 3));
+    for (int u = 0; u < 4; ++u) {
+      const int kb = kb0 + 32 * u + lane;
+      p[u][0] = p[u][1] = make_uint4(0, 0, 0, 0);
+      if (kb < nb) {
+        p[u][0] = *reinterpret_cast<const uint4*>(src + (size_t)kb * 16);
+        p[u][1] = *reinterpret_cast<const uint4*>(src + (size_t)kb * 16 + 8);
       }
-      *reinterpret_cast<uint2*>(codes + (size_t)kb * 8) = make_uint2(c[0], c[1]);
     }
-    // lanes 4w .. 4w+3 hold the scales of one 64-wide K step
-    const uint32_t b1 = __shfl_down_sync(0xffffffffu, sbyte, 1);
-    const uint32_t b2 = __shfl_down_sync(0xffffffffu, sbyte, 2);
-    const uint32_t b3 = __shfl_down_sync(0xffffffffu, sbyte, 3);
-    if ((lane & 3) == 0 && kb < K / 16) put_word(kb >> 2, sbyte | (b1 << 8) | (b2 << 16) | (b3 << 24));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int kb = kb0 + 32 * u + lane;
+      uint32_t sbyte = 0;
+      if (kb < nb) {
+        const uint32_t w[8] = {p[u][0].x, p[u][0].y, p[u][0].z, p[u][0].w,
+                               p[u][1].x, p[u][1].y, p[u][1].z, p[u][1].w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { v[2 * i] = bf16lo(w[i]); v[2 * i + 1] = bf16hi(w[i]); }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        bad |= !(amax <= 3.0e38f);
+        sbyte = f32_to_e4m3(__fdiv_rn(amax, g6));
+        const float den = __fmul_rn(e4m3_to_f32(sbyte), g);
+        uint32_t c[2] = {0u, 0u};
+        if (den > 0.f) {
+          const float r = __frcp_rn(den);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            c[i >> 2] |= f32x2_to_e2m1x2(__fmul_rn(v[2 * i], r), __fmul_rn(v[2 * i + 1], r)) << (8 * (i & 3));
+        }
+        *reinterpret_cast<uint2*>(codes + (size_t)kb * 8) = make_uint2(c[0], c[1]);
+      }
+      // lanes 4w .. 4w+3 hold the scales of one 64-wide K step
+      const uint32_t b1 = __shfl_down_sync(0xffffffffu, sbyte, 1);
+      const uint32_t b2 = __shfl_down_sync(0xffffffffu, sbyte, 2);
+      const uint32_t b3 = __shfl_down_sync(0xffffffffu, sbyte, 3);
+      if ((lane & 3) == 0 && kb < nb) put_word(kb >> 2, sbyte | (b1 << 8) | (b2 << 16) | (b3 << 24));
+    }
   }
   return bad;
 }
@@ -305,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSF * kStage);
   uint64_t* empty = full + NSF;
-  uint64_t* tfull = empty + NSF;
+  uint64_t* sfull = empty + NSF;    // a stage's scales are in tensor memory
+  uint64_t* tfull = sfull + NSF;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -368,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NSF; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < NSF; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], kSfWarps); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], kEpiWarps); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -433,24 +459,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kc = 0; kc < nkc; ++kc, ++it) {
           const int s = it % NSF;
           const uint32_t ph = (it / NSF) & 1;
-          if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+          // the codes have landed (full) and the scale warps have written
+          // this stage's scales into tensor memory (sfull)
+          if (!mbar_wait(&full[s], ph) || !mbar_wait(&sfull[s], ph)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + s * kStage);
           const uint32_t sB = sA + kCodeBytes;
-          const uint32_t sSA = sB + kCodeBytes;
-          const uint32_t sSB = sSA + kSfBytes;
           const uint32_t tsa = tmem_base + kSfColBase + s * kSfColsStage;
           const uint32_t tsb = tsa + 16;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            sf_copy(tsa + 4 * kk, desc_atom(sSA + kk * kAtomBytes));
-            sf_copy(tsb + 4 * kk, desc_atom(sSB + kk * kAtomBytes));
-          }
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_fp4(tmem_d, umma_desc(sA + kk * 32), umma_desc(sB + kk * 32), idesc, tsa + 4 * kk,
                     tsb + 4 * kk, (kc | kk) != 0 ? 1u : 0u);
-          umma_commit(&empty[s]);   // frees the stage once these copies and MMAs are done
+          umma_commit(&empty[s]);   // frees the stage (shared and tensor memory) once these MMAs are done
         }
         if (!ok) break;
         umma_commit(&tfull[b]);
@@ -459,11 +480,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) atomicOr(abort_flag, 1);
     }
     __syncwarp();
+  } else if (warp < 2 + kSfWarps) {
+    // ------------------------------------------------------------ scale warps
+    const int q = warp & 3;
+    const uint32_t lanes = (uint32_t)(q * 32) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int kc = 0; kc < nkc; ++kc, ++it) {
+        const int s = it % NSF;
+        const uint32_t ph = (it / NSF) & 1;
+        if (!warp_wait(&full[s], ph)) { ok = false; break; }
+        // atom kk, row `lane`: words j = scales of rows / columns lane + 32j
+        const uint4* atA = reinterpret_cast<const uint4*>(smem + s * kStage + 2 * kCodeBytes);
+        const uint4* atB = atA + kSfBytes / 16;
+        uint32_t va[16], vb[16];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 wa = atA[kk * 32 + lane];
+          va[4 * kk + 0] = q == 0 ? wa.x : 0u;
+          va[4 * kk + 1] = q == 1 ? wa.y : 0u;
+          va[4 * kk + 2] = q == 2 ? wa.z : 0u;
+          va[4 * kk + 3] = q == 3 ? wa.w : 0u;
+          const uint4 wb = atB[kk * 32 + lane];
+          vb[4 * kk + 0] = wb.x; vb[4 * kk + 1] = wb.y; vb[4 * kk + 2] = wb.z; vb[4 * kk + 3] = wb.w;
+        }
+        const uint32_t tsa = tmem_base + lanes + kSfColBase + s * kSfColsStage;
+        tmem_st16(tsa, va);
+        tmem_st16(tsa + 16, vb);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[s]);
+      }
+      if (*(volatile int*)abort_flag) ok = false;
+    }
+    if (!ok && lane == 0) atomicOr(abort_flag, 1);
   } else {
     // ------------------------------------------------------------ epilogue
     // warp w reads TMEM lanes 32(w % 4) .. +31, 32-column chunks 2i + hc
     const int q = warp & 3;
-    const int hc = (warp - 2) >> 2;
+    const int hc = (warp - 2 - kSfWarps) >> 2;
     uint32_t lt = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       const uint32_t b = lt & 1;

@@ -215,11 +215,11 @@ int moe_route_noalloc(const uint16_t *x, const uint16_t *gate_w, const float *bi
  * quantised with the format's own recipe, per routed row of expert e:
  *   16-element blocks along K (H for the token rows, I for h),
  *   block scale  s = e4m3(amax / (6 G))           round to nearest even, <= 448
- *   element code   = e2m1(v / (s G))              round to nearest even, |.| <= 6
+ *   element code   = e2m1(v * r), r = 1 / (s G)  round to nearest even, |.| <= 6
  *   (0 for every element of a block whose s G is 0)
  * with G = x_global[e] for the token rows and G = h_global[e] for the SwiGLU
- * output h = bf16(silu(g) * u); every quotient and product in fp32 with IEEE
- * rounding.  Then g, u = dequant(W_gu) dequant(x_q), y = dequant(W_dn)
+ * output h = bf16(silu(g) * u); every quotient, reciprocal and product in
+ * fp32 with IEEE rounding.  Then g, u = dequant(W_gu) dequant(x_q), y = dequant(W_dn)
  * dequant(h_q), and the combine as in moe_forward.
  *
  * Weights: codes and globals as in moe_nvfp4_weights; the block scales in the

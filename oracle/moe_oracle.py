@@ -36,7 +36,9 @@ here is the format's own recipe applied to each routed row: for expert e the
 token row x_t (step 6's input) and the SwiGLU output h (rounded to bf16, as
 on the bf16-weight path) are each cut into 16-element blocks along the
 contraction axis; a block with largest magnitude a gets the e4m3 scale
-s = RNE_e4m3(a / (6*G)) and its elements the e2m1 codes RNE_e2m1(v / (s*G)),
+s = RNE_e4m3(a / (6*G)) and its elements the e2m1 codes RNE_e2m1(v * r) with
+r = 1 / (s*G) (one reciprocal per block, as the format's deployed
+quantisers compute it),
 G = x_global[e] or h_global[e] (fp32 constants given with the weights, like
 the calibrated input scales of NVFP4 checkpoints).  Each quotient and product
 in these decisions is taken in fp32 (the precision a kernel takes them in);
@@ -305,9 +307,9 @@ def e2m1_quantize(v: np.ndarray) -> np.ndarray:
 def nvfp4_quantize(a: np.ndarray, glob: float):
     """NVFP4-encode rows a [R, K] (values exact in fp32) with global scale
     glob: per 16-element block the e4m3 scale of fp32(amax / fp32(6*glob)),
-    then the e2m1 code of fp32(v / fp32(scale*glob)) per element (code 0 when
-    scale*glob is 0).  Returns codes uint8 [R, K/2] (even k in the low nibble)
-    and scales uint8 [R, K/16]."""
+    the block's reciprocal r = fp32(1 / fp32(scale*glob)), then the e2m1 code
+    of fp32(v * r) per element (code 0 when scale*glob is 0).  Returns codes
+    uint8 [R, K/2] (even k in the low nibble) and scales uint8 [R, K/16]."""
     a32 = np.asarray(a, dtype=np.float32)
     R, K = a32.shape
     g = np.float32(glob)
@@ -315,8 +317,8 @@ def nvfp4_quantize(a: np.ndarray, glob: float):
     amax = np.abs(blocks).max(axis=2)
     scales = e4m3_quantize(amax / (np.float32(6.0) * g))
     denom = (e4m3_to_f64(scales).astype(np.float32) * g).astype(np.float32)
-    safe = np.where(denom > 0, denom, np.float32(1.0))[:, :, None]
-    q = (blocks / safe).astype(np.float32)
+    recip = (np.float32(1.0) / np.where(denom > 0, denom, np.float32(1.0))).astype(np.float32)
+    q = (blocks * recip[:, :, None]).astype(np.float32)
     nib = np.where(denom[:, :, None] > 0, e2m1_quantize(q), 0).astype(np.uint8).reshape(R, K)
     codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
     return codes, scales

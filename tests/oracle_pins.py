@@ -207,8 +207,8 @@ def pin_nvfp4_quantize_blocks(o):
     the scale byte is torch's e4m3 cast of fp32(amax / fp32(6*G)) (448 when
     that quotient is beyond the format's range: one block here is); each
     element's code (decoded with the format tables, even k in the low nibble)
-    is a nearest e2m1 value to fp32(v / fp32(scale*G)), ties to the even code,
-    saturating at 6; an all-zero block gets scale 0 and codes 0."""
+    is a nearest e2m1 value to fp32(v * fp32(1 / fp32(scale*G))), ties to the
+    even code, saturating at 6; an all-zero block gets scale 0 and codes 0."""
     e2m1 = {c: _val(v) for c, v in _read_table("e2m1_codes.txt")}
     rng = _rng(15)
     R, K = 5, 96
@@ -236,7 +236,7 @@ def pin_nvfp4_quantize_blocks(o):
                     if den == 0:
                         assert nib == 0
                         continue
-                    q = float(np.float32(blk[i] / den))
+                    q = float(np.float32(blk[i] * np.float32(np.float32(1.0) / den)))
                     got = e2m1[nib]
                     best = min(abs(v - q) for v in e2m1.values())
                     assert abs(got - q) == best, (G, r, kk, q, got)

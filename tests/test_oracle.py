@@ -241,8 +241,8 @@ def _mut_nvfp4_quant_block32(m):
         amax = np.repeat(np.abs(a32.reshape(R, K // 32, 32)).max(axis=2), 2, axis=1)
         scales = m.e4m3_quantize(amax / (np.float32(6.0) * g))
         denom = (m.e4m3_to_f64(scales).astype(np.float32) * g).astype(np.float32)
-        with np.errstate(divide="ignore", invalid="ignore"):
-            q = (a32.reshape(R, K // 16, 16) / denom[:, :, None]).astype(np.float32)
+        recip = (np.float32(1.0) / np.where(denom > 0, denom, np.float32(1.0))).astype(np.float32)
+        q = (a32.reshape(R, K // 16, 16) * recip[:, :, None]).astype(np.float32)
         nib = np.where(denom[:, :, None] > 0, m.e2m1_quantize(q), 0).astype(np.uint8).reshape(R, K)
         return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8), scales
     m.nvfp4_quantize = nvfp4_quantize
