@@ -17,7 +17,10 @@ __all__ = ["MoEError", "lib", "workspace_size", "alloc_workspace", "route", "per
            "read_status", "read_diagnostics", "LIB_PATH", "nvfp4_tc_scales", "nvfp4_quantize",
            "W4A4Weights", "w4a4_weights", "forward_w4a4"]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_gb300.so")
+# MOE_GB300_LIB selects another build of the library (e.g. the index-checking
+# MOE_DEBUG_BOUNDS build); the default is the in-tree libmoe_gb300.so.
+LIB_PATH = os.environ.get("MOE_GB300_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                           "libmoe_gb300.so")
 
 MOE_OK = 0
 
@@ -60,6 +63,7 @@ _SIGNATURES = {
     "moe_nvfp4_tc_scales": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "moe_nvfp4_quantize": (_I, [_P, _I, _I, ctypes.c_float, _P, _P, _P]),
     "moe_read_status": (_I, [_P, _P]),
+    "moe_debug_force_wait_timeout": (_I, [_I]),
     "moe_read_diagnostics": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_error_string": (ctypes.c_char_p, [_I]),
     "moe_version": (_I, []),

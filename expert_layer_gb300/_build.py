@@ -39,8 +39,14 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
+def build(verbose: bool = False, extra_flags: list[str] | None = None, build_dir: str | None = None,
+          lib_path: str | None = None) -> str:
+    """Compile and link the library; returns its path.  ``extra_flags`` go to
+    every nvcc compile (e.g. ["-DMOE_DEBUG_BOUNDS"] for the index-checking
+    build, which then needs its own ``build_dir`` and ``lib_path``)."""
     nvcc = _nvcc()
+    BUILD = build_dir or globals()["BUILD"]
+    LIB = lib_path or globals()["LIB"]
     os.makedirs(BUILD, exist_ok=True)
     newest_hdr = max(os.path.getmtime(h) for h in _headers())
     flags = NVCC_FLAGS + list(extra_flags or [])

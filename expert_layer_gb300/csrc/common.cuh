@@ -14,7 +14,23 @@ enum : int {
   kStatusBadExpert = 1,   // moe_permute saw an expert id outside [0, E)
   kStatusTimeout = 2,     // a bounded device-side wait gave up
   kStatusRange = 4,       // NVFP4 path: an activation (x or h) beyond the f16 range
+  kStatusBounds = 8,      // MOE_DEBUG_BOUNDS builds: an index read from a device array was out of range
 };
+
+// Index checks of MOE_DEBUG_BOUNDS builds.  Every index that an expert-GEMM,
+// gather or quantiser kernel reads from a device array (the slot
+// permutation, the flat expert ids, group offsets and counts) is checked
+// before it addresses memory; a bad one is recorded as kStatusBounds
+// (MOE_ERR_DEVICE for moe_read_status) and replaced by a safe index by the
+// caller.  Normal builds compile the checks away.
+#ifdef MOE_DEBUG_BOUNDS
+__device__ __forceinline__ bool bounds_ok(bool ok, int* status) {
+  if (!ok) atomicOr(status, kStatusBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool bounds_ok(bool, int*) { return true; }
+#endif
 
 // Workspace header (first 256 bytes of every workspace).
 struct WsHeader {

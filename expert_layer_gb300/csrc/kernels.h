@@ -19,6 +19,14 @@ struct GroupOut {
   int nzero;
 };
 
+// moe_api.cu -- test-only settings of the bounded device waits (0, 0 in
+// normal use; moe_debug_force_wait_timeout)
+struct DebugWaits {
+  int spin_limit;   // polls before a wait gives up (0: the default)
+  int force;        // nonzero: waits aim at a count no unit reaches
+};
+DebugWaits debug_waits();
+
 // moe_api.cu -- clears the first `bytes` (a multiple of 16) of the workspace;
 // lets the next kernel (a programmatic dependent) start launching at once
 cudaError_t launch_zero(void* ws, size_t bytes, cudaStream_t stream);
@@ -68,6 +76,11 @@ struct StreamGemmArgs {
   int* dep;
   int* status;               // workspace status word (kStatusTimeout)
   int num_sms;
+  // bounded waits: polls before a down unit's wait gives up; with
+  // wait_extra > 0 the wait aims at a count that no unit reaches (test-only
+  // forced timeout, see moe_debug_force_wait_timeout)
+  int spin_limit;
+  int wait_extra;
 };
 // gate/up then down of the small groups, one persistent launch
 cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
@@ -102,7 +115,7 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
 
 // tc_gemm.cu -- xp[r] = x[perm[r] / k]: token rows in grouped order
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int S, int H, int k,
-                               uint16_t* xp, cudaStream_t stream, int* launches);
+                               uint16_t* xp, int* status, cudaStream_t stream, int* launches);
 
 // tc_fp4.cu -- W4A4: NVFP4 weights x NVFP4 activations on the block-scaled
 // tensor cores (tcgen05 kind::mxf4nvf4)

@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "../../include/moe.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -23,6 +25,14 @@ __global__ void __launch_bounds__(256) zero_kernel(uint4* __restrict__ p, int n1
     p[i] = make_uint4(0, 0, 0, 0);
 }
 }  // namespace
+
+namespace {
+// Test-only wait settings (moe_debug_force_wait_timeout); zero in normal use.
+std::atomic<int> g_debug_spin{0};
+std::atomic<int> g_debug_force{0};
+}  // namespace
+
+DebugWaits debug_waits() { return DebugWaits{g_debug_spin.load(), g_debug_force.load()}; }
 
 cudaError_t launch_zero(void* ws, size_t bytes, cudaStream_t stream) {
   const int n16 = (int)(bytes / 16);
@@ -435,6 +445,13 @@ int moe_nvfp4_quantize(const uint16_t* a, int R, int K, float global, uint8_t* c
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_debug_force_wait_timeout(int polls) {
+  if (polls < 0) return MOE_ERR_INVALID_ARG;
+  moe::g_debug_spin.store(polls);
+  moe::g_debug_force.store(polls > 0 ? 1 : 0);
+  return MOE_OK;
+}
+
 int moe_read_status(const void* workspace, void* stream) {
   if (!workspace) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -443,7 +460,7 @@ int moe_read_status(const void* workspace, void* stream) {
   if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (st & kStatusTimeout) return MOE_ERR_DEVICE_TIMEOUT;
-  if (st & (kStatusBadExpert | kStatusRange)) return MOE_ERR_DEVICE;
+  if (st & (kStatusBadExpert | kStatusRange | kStatusBounds)) return MOE_ERR_DEVICE;
   return MOE_OK;
 }
 

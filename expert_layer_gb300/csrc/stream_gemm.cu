@@ -92,6 +92,7 @@ struct StreamCfg {
 
 // Bounded waits: polls before a wait gives up (and the kernel records
 // kStatusTimeout); with the sleep between polls this is well over a second.
+// (StreamGemmArgs.spin_limit overrides it in tests.)
 constexpr int kSpinLimit = 1 << 22;
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -208,8 +209,11 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
   const int S = a.T * a.k;
   const bool perm_smem = S <= kPermSmem;
   for (int i = threadIdx.x; i < nsmall; i += blockDim.x) {
-    const int e = a.active[i];
-    smeta[i] = make_int4(e, a.counts[e], a.offsets[e], 0);
+    int e = a.active[i];
+    if (!bounds_ok((unsigned)e < (unsigned)a.E, a.status)) e = 0;
+    int m = a.counts[e], off = a.offsets[e];
+    if (!bounds_ok(off >= 0 && m >= 0 && off + m <= a.T * a.k, a.status)) m = 0, off = 0;
+    smeta[i] = make_int4(e, m, off, 0);
   }
   if (perm_smem)
     for (int i = threadIdx.x; i < S; i += blockDim.x) sperm[i] = a.perm[i];
@@ -310,8 +314,8 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
       // h of this expert is complete once every gate/up unit of it published
       if (lane == 0) {
         int n = 0;
-        while (ld_acquire(a.dep + ct.slot) < qs.UPEg) {
-          if (++n > kSpinLimit) { atomicOr(a.status, kStatusTimeout); break; }
+        while (ld_acquire(a.dep + ct.slot) < qs.UPEg + a.wait_extra) {
+          if (++n > a.spin_limit) { atomicOr(a.status, kStatusTimeout); break; }
           __nanosleep(128);
         }
       }
@@ -328,7 +332,11 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
         bsrc[nt] = nullptr;
         if (n < ct.m) {
           if (ct.down) bsrc[nt] = a.h + (size_t)(ct.off + n) * a.I;
-          else bsrc[nt] = (kFp4 ? a.x16 : a.x) + (size_t)(permp[ct.off + n] / a.k) * a.H;
+          else {
+            int f = permp[ct.off + n];
+            if (!bounds_ok((unsigned)f < (unsigned)(a.T * a.k), a.status)) f = 0;
+            bsrc[nt] = (kFp4 ? a.x16 : a.x) + (size_t)(f / a.k) * a.H;
+          }
         }
       }
       // down: the epilogue's slots and routing weights, fetched now
@@ -343,6 +351,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
           ew[nt][h2] = 0.f;
           if (ct.down && n < ct.m) {
             ef[nt][h2] = permp[ct.off + n];
+            if (!bounds_ok((unsigned)ef[nt][h2] < (unsigned)(a.T * a.k), a.status)) ef[nt][h2] = 0;
             ew[nt][h2] = a.topk_w[ef[nt][h2]];
           }
         }
@@ -591,8 +600,12 @@ cudaError_t launch_to_f16(const uint16_t* x, size_t n, uint16_t* y, int* status,
   return cudaGetLastError();
 }
 
-cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches) {
+cudaError_t launch_stream_gemm(const StreamGemmArgs& args, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
+  StreamGemmArgs a = args;
+  const DebugWaits dw = debug_waits();
+  a.spin_limit = dw.spin_limit > 0 ? dw.spin_limit : kSpinLimit;
+  a.wait_extra = dw.force ? 1 : 0;
   // a group never holds more rows than the batch has tokens: one 8-row tile
   // per pass for T <= 8, two above; NVFP4 takes four (32-row passes) once
   // the experts average 24 rows or more (measured: 16-row passes faster at

@@ -262,9 +262,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   const int warp = threadIdx.x >> 5;
   bool bad = false;
   for (long long r = (long long)blockIdx.x * 8 + warp; r < S; r += (long long)gridDim.x * 8) {
-    const int f = perm[r];
-    const int e = idx[f];
-    const int rl = (int)r - offsets[e];
+    int f = perm[r];
+    if (!bounds_ok((unsigned)f < (unsigned)S, status)) f = 0;
+    int e = idx[f];
+    if (!bounds_ok((unsigned)e < (unsigned)E, status)) e = 0;
+    int rl = (int)r - offsets[e];
+    if (!bounds_ok(rl >= 0 && rl < counts[e], status)) rl = 0;
     const size_t blk = (size_t)tpre[e] + rl / kRows;
     const uint16_t* row = kGather ? src + (size_t)(f / k) * K : src + (size_t)r * K;
     uint32_t* sfw = reinterpret_cast<uint32_t*>(sf);
@@ -349,10 +352,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkc = K / kKStage;
 
   for (int i = threadIdx.x; i < nact; i += kThreads) {
-    const int e = a.active[i];
+    int e = a.active[i];
+    if (!bounds_ok((unsigned)e < (unsigned)a.E, a.status)) e = 0;
+    int m = a.counts[e], off = a.offsets[e];
+    if (!bounds_ok(off >= 0 && m >= 0 && off + m <= a.T * a.k, a.status)) m = 0, off = 0;
     s_e[i] = e;
-    s_m[i] = a.counts[e];
-    s_off[i] = a.offsets[e];
+    s_m[i] = m;
+    s_off[i] = off;
   }
   if (threadIdx.x == 0) {
     int acc = 0;
@@ -537,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
           const int c = 32 * (2 * i + hc) + lane;
           fl[i] = c < ncols ? __ldg(&a.perm[ti.off + tok0 + c]) : 0;
+          if (!bounds_ok((unsigned)fl[i] < (unsigned)(a.T * a.k), a.status)) fl[i] = 0;
           wl[i] = c < ncols ? __ldg(&a.topk_w[fl[i]]) * scale : 0.f;
         }
       }

@@ -157,10 +157,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const int nkb = K / (kHalves * BK);
 
   for (int i = threadIdx.x; i < nlarge; i += kThreadsPair) {
-    const int e = a.active[nsmall + i];
+    int e = a.active[nsmall + i];
+    if (!bounds_ok((unsigned)e < (unsigned)a.E, a.status)) e = 0;
+    int m = a.counts[e], off = a.offsets[e];
+    if (!bounds_ok(off >= 0 && m >= 0 && off + m <= a.T * a.k, a.status)) m = 0, off = 0;
     md.e[i] = e;
-    md.m[i] = a.counts[e];
-    md.off[i] = a.offsets[e];
+    md.m[i] = m;
+    md.off[i] = off;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         for (int i = 0; i < 4; ++i) {
           const int c = 32 * (2 * i + hc) + lane;
           fl[i] = c < ncols ? __ldg(&a.perm[ti.off + tok0 + c]) : 0;
+          if (!bounds_ok((unsigned)fl[i] < (unsigned)(a.T * a.k), a.status)) fl[i] = 0;
           wl[i] = c < ncols ? __ldg(&a.topk_w[fl[i]]) : 0.f;
         }
       }
@@ -353,10 +357,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 // 16-byte vectors (x stays in L2; this is one streaming write of S*H bf16).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm, int S,
-                                                          int H, int k, uint16_t* __restrict__ xp) {
+                                                          int H, int k, uint16_t* __restrict__ xp,
+                                                          int* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (long long r = (long long)blockIdx.x * 8 + warp; r < S; r += (long long)gridDim.x * 8) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(perm[r] / k) * H);
+    int f = perm[r];
+    if (!bounds_ok((unsigned)f < (unsigned)S, status)) f = 0;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(f / k) * H);
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * H);
     for (int v = lane; v < H / 8; v += 32) dst[v] = src[v];
   }
@@ -371,9 +378,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 }  // namespace
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int S, int H, int k,
-                               uint16_t* xp, cudaStream_t stream, int* launches) {
+                               uint16_t* xp, int* status, cudaStream_t stream, int* launches) {
   const long long blocks = ((long long)S + 7) / 8;
-  gather_rows_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(x, perm, S, H, k, xp);
+  gather_rows_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(x, perm, S, H, k, xp,
+                                                                                     status);
   if (launches) *launches += 1;
   return cudaGetLastError();
 }
@@ -387,7 +395,7 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
   a.status = p.status;
   const long long S = (long long)p.T * p.k;
   if (!down) {
-    const cudaError_t gerr = launch_gather_rows(p.x, p.perm, (int)S, p.H, p.k, p.xp, stream, launches);
+    const cudaError_t gerr = launch_gather_rows(p.x, p.perm, (int)S, p.H, p.k, p.xp, p.status, stream, launches);
     if (gerr != cudaSuccess) return gerr;
   }
   // CTA pairs need at least two SMs; moe_forward sends every group to the

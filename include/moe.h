@@ -285,6 +285,19 @@ int moe_forward_w4a4_profiled(const uint16_t *x, const uint16_t *gate_w, const f
 int moe_nvfp4_quantize(const uint16_t *a, int R, int K, float global, uint8_t *codes, uint8_t *scales,
                        void *stream);
 
+/*
+ * TEST ONLY.  With polls > 0, every moe_forward launched afterwards in this
+ * process makes the weight-streaming kernel's bounded waits (a down-
+ * projection unit waiting for its expert's gate/up units) aim at a count
+ * that no unit ever reaches and give up after `polls` polls: the call then
+ * completes, its output is unspecified, and moe_read_status reports
+ * MOE_ERR_DEVICE_TIMEOUT.  polls == 0 restores normal operation (the
+ * default).  Process-wide setting, not thread-safe with concurrent calls;
+ * it exists so that tests can exercise the timeout path without a hung or
+ * faulted GPU.
+ */
+int moe_debug_force_wait_timeout(int polls);
+
 /* Static, human-readable name of a moe_status value. */
 const char *moe_error_string(int status);
 
