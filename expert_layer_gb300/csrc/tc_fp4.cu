@@ -58,7 +58,8 @@
 //               32-column chunks
 // Two 128-column accumulators let the epilogue of one tile overlap the
 // mainloop of the next.  Every mbarrier wait is bounded; a timeout sets
-// kStatusTimeout and the CTA leaves its loops.
+// kStatusTimeout, the CTA leaves its loops, waits (bounded again) for the
+// copies and MMAs it has issued, frees its tensor memory and returns.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -336,7 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sfull = empty + NSF;    // a stage's scales are in tensor memory
   uint64_t* tfull = sfull + NSF;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* drain = tempty + 2;   // after a timeout: the issued MMAs are complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* s_e = reinterpret_cast<int*>(smem + NSF * kStage + 256);
   int* s_m = s_e + (kMaxE + 1);
@@ -402,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSF; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], kSfWarps); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], kEpiWarps); }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -444,7 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (*(volatile int*)abort_flag) ok = false;
       }
-      if (!ok) atomicOr(abort_flag, 1);
+      if (!ok) {
+        atomicOr(abort_flag, 1);
+        // after a timeout: the copies already issued land before the CTA exits
+        for (uint32_t j = it > (uint32_t)NSF ? it - NSF : 0; j < it; ++j) mbar_wait(&full[j % NSF], (j / NSF) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -483,7 +490,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&tfull[b]);
         if (*(volatile int*)abort_flag) ok = false;
       }
-      if (!ok) atomicOr(abort_flag, 1);
+      if (!ok) {
+        atomicOr(abort_flag, 1);
+        // after a timeout: the MMAs already issued finish before the tensor
+        // memory they write is freed
+        umma_commit(drain);
+        mbar_wait(drain, 0);
+      }
     }
     __syncwarp();
   } else if (warp < 2 + kSfWarps) {

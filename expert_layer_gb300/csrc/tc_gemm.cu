@@ -15,7 +15,9 @@
 // address by 32 bytes).
 //
 // Every wait on an mbarrier is bounded; on a timeout the CTA records
-// kStatusTimeout in the workspace status word and leaves its loops.
+// kStatusTimeout in the workspace status word, leaves its loops, waits
+// (bounded again) for the TMA loads and MMAs it has issued, frees its tensor
+// memory and returns.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -139,7 +141,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   uint64_t* empty = full + NS2;
   uint64_t* tfull = empty + NS2;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* drain = tempty + 2;   // after a timeout: the issued MMAs are complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   TileMeta md;
   md.tiles = reinterpret_cast<int*>(smem + NS2 * kStageBytes2 + 256);   // [nlarge+1] token-block prefix
@@ -181,6 +184,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS2; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 2 * kEpiWarps); }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -226,7 +230,14 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         }
         if (*(volatile int*)abort_flag) ok = false;
       }
-      if (!ok) atomicOr(abort_flag, 1);
+      if (!ok) {
+        atomicOr(abort_flag, 1);
+        // after a timeout: the loads already issued land before either CTA
+        // may exit (CTA 0's full barriers count both CTAs' bytes; the final
+        // cluster barrier holds CTA 1 until CTA 0 is done)
+        if (rank == 0)
+          for (uint32_t j = it > (uint32_t)NS2 ? it - NS2 : 0; j < it; ++j) mbar_wait(&full[j % NS2], (j / NS2) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -262,7 +273,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         umma_commit_pair(&tfull[b]);     // both CTAs' accumulators ready
         if (*(volatile int*)abort_flag) ok = false;
       }
-      if (!ok) atomicOr(abort_flag, 1);
+      if (!ok) {
+        atomicOr(abort_flag, 1);
+        // after a timeout: the MMAs already issued finish before the tensor
+        // memory they write is freed
+        umma_commit_pair(drain);
+        mbar_wait(drain, 0);
+      }
     }
     __syncwarp();
   } else {
