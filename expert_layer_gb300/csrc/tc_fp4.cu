@@ -87,8 +87,8 @@ constexpr uint32_t kSfColBase = 2 * kAccCols;       // scale columns after the t
 constexpr uint32_t kSfColsStage = 32;               // SFA 16 + SFB 16 per stage
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxE = 1024;
-// ring + alignment slack + barriers + per-expert metadata (e, m, off, tile prefix, scale-block prefix)
-constexpr size_t kSmemBytes = (size_t)NSF * kStage + 1024 + 256 + 5 * 4 * (kMaxE + 1);
+// ring + alignment slack + barriers + per-expert metadata (e, m, off, tile prefix)
+constexpr size_t kSmemBytes = (size_t)NSF * kStage + 1024 + 256 + 4 * 4 * (kMaxE + 1);
 
 static_assert(NSF * kSfColsStage + kSfColBase <= kTmemCols, "tensor memory columns");
 
@@ -162,6 +162,15 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   asm("{\n .reg .b16 h;\n mov.b32 {h, _}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}" : "=r"(d) : "r"(b));
   return __half2float(__ushort_as_half((unsigned short)(d & 0xffffu)));
 }
+// (lo * r, hi * r) as one packed fp32x2 multiply: each product rounded to
+// nearest even exactly as a separate fp32 multiply would be
+__device__ __forceinline__ void mul2_rn(float lo, float hi, float r, float& plo, float& phi) {
+  unsigned long long x, y, z;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(lo), "f"(hi));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(r));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(plo), "=f"(phi) : "l"(z));
+}
 // two e2m1 codes: lo -> low nibble, hi -> high nibble; round to nearest even,
 // saturating at 6
 __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
@@ -223,8 +232,11 @@ __device__ __forceinline__ bool quantize_row(const uint16_t* __restrict__ src, i
         if (den > 0.f) {
           const float r = __frcp_rn(den);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            c[i >> 2] |= f32x2_to_e2m1x2(__fmul_rn(v[2 * i], r), __fmul_rn(v[2 * i + 1], r)) << (8 * (i & 3));
+          for (int i = 0; i < 8; ++i) {
+            float plo, phi;
+            mul2_rn(v[2 * i], v[2 * i + 1], r, plo, phi);
+            c[i >> 2] |= f32x2_to_e2m1x2(plo, phi) << (8 * (i & 3));
+          }
         }
         *reinterpret_cast<uint2*>(codes + (size_t)kb * 8) = make_uint2(c[0], c[1]);
       }
@@ -251,13 +263,28 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
                                                          uint8_t* __restrict__ codes,
                                                          uint8_t* __restrict__ sf, int* status) {
   __shared__ int tpre[kMaxE + 1];
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      tpre[e] = acc;
-      acc += (counts[e] + kRows - 1) / kRows;
+  // 128-row blocks before each expert: every thread loads counts, one warp
+  // scans (lane l owns experts [32l .. 32l + 31] of at most 1024)
+  for (int e = threadIdx.x; e < E; e += blockDim.x) tpre[e] = (counts[e] + kRows - 1) / kRows;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int l = threadIdx.x;
+    const int lo = min(E, 32 * l), hi = min(E, 32 * l + 32);
+    int sum = 0;
+    for (int e = lo; e < hi; ++e) sum += tpre[e];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (l >= o) incl += v;
     }
-    tpre[E] = acc;
+    int acc = incl - sum;
+    for (int e = lo; e < hi; ++e) {
+      const int nb = tpre[e];
+      tpre[e] = acc;
+      acc += nb;
+    }
+    if (l == 31) tpre[E] = incl;
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5;
@@ -323,6 +350,7 @@ __global__ void __launch_bounds__(256) tc_scales_kernel(const uint8_t* __restric
 // ------------------------------------------------------------------ GEMM
 struct TileF {
   int e, m, off, wblk, ttile;
+  int sblk;   // the expert's first 128-row activation-scale block
 };
 
 template <bool kDown>
@@ -344,7 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_m = s_e + (kMaxE + 1);
   int* s_off = s_m + (kMaxE + 1);
   int* s_tiles = s_off + (kMaxE + 1);   // token-tile prefix over the active list
-  int* s_tpre = s_tiles + (kMaxE + 1);  // 128-row scale-block prefix by expert index
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nact = *a.num_active;
@@ -361,13 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_e[i] = e;
     s_m[i] = m;
     s_off[i] = off;
-  }
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int e = 0; e < a.E; ++e) {
-      s_tpre[e] = acc;
-      acc += (a.counts[e] + kRows - 1) / kRows;
-    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -398,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ti.off = s_off[lo];
     ti.wblk = local / mt;
     ti.ttile = local % mt;
+    ti.sblk = s_tiles[lo];
     return ti;
   };
 
@@ -428,7 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileF ti = decode(t);
         const int brow = ti.off + ti.ttile * kRows;
         const size_t ablk = (size_t)ti.e * NWB + ti.wblk;
-        const size_t bblk = (size_t)s_tpre[ti.e] + ti.ttile;
+        // the active list is ascending and holds every expert with rows, so
+        // its tile prefix is also the activation scales' block prefix
+        const size_t bblk = (size_t)ti.sblk + ti.ttile;
         for (int kc = 0; kc < nkc; ++kc, ++it) {
           const int s = it % NSF;
           const uint32_t ph = (it / NSF) & 1;
@@ -638,7 +661,10 @@ cudaError_t launch_quant_rows(bool gather, const uint16_t* src, const int32_t* p
                               int* launches) {
   if (launches) *launches += 1;
   const long long blocks = ((long long)S + 7) / 8;
-  const unsigned grid = (unsigned)(blocks < 2048 ? (blocks > 0 ? blocks : 1) : 2048);
+  int dev = 0, nsm = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const long long cap = 3ll * nsm;   // grid-stride rows: the CTAs that are resident at once
+  const unsigned grid = (unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
   if (gather)
     quant_rows_kernel<true><<<grid, 256, 0, stream>>>(src, perm, idx, k, counts, offsets, S, K, E, glob, codes,
                                                       sf, status);
