@@ -18,6 +18,7 @@ prefill8192   8192    2048  128     8     768  0.5*log-Zipf(1.1) bias
 nvfp4_256      256    2048  128     8     768  NVFP4 expert weights
 prefill8192_w4a4 8192 2048  128     8     768  NVFP4 weights and activations,
                                                0.5*log-Zipf(1.1) bias
+int8_256       256    2048  128     8     768  int8 block expert weights
 =============  =====  =====  ===  =====  ====  =========================
 
 Recipe: one ``torch.Generator`` on the requested device seeded with ``seed``;
@@ -51,6 +52,7 @@ WORKLOADS = {
     "prefill8192": dict(T=8192, H=2048, E=128, top_k=8, I=768, bias="zipf", nvfp4=False),
     "nvfp4_256": dict(T=256, H=2048, E=128, top_k=8, I=768, bias=None, nvfp4=True),
     "prefill8192_w4a4": dict(T=8192, H=2048, E=128, top_k=8, I=768, bias="zipf", nvfp4=True, w4a4=True),
+    "int8_256": dict(T=256, H=2048, E=128, top_k=8, I=768, bias=None, nvfp4=False, q8=True),
 }
 
 X_BOUND, H_BOUND = 8.0, 32.0
@@ -71,6 +73,15 @@ class NVFP4Tensor:
 
 
 @dataclass
+class Q8Tensor:
+    """One int8 block-quantised weight tensor of logical shape [E, R, K]:
+    codes int8 [E, R, K], scales fp16 [E, R, K/32] (one per 32 consecutive K);
+    W = code * scale."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+
+
+@dataclass
 class MoEInputs:
     T: int
     H: int
@@ -87,6 +98,8 @@ class MoEInputs:
     meta: dict = field(default_factory=dict)
     x_global: torch.Tensor | None = None  # fp32 [E], W4A4 only
     h_global: torch.Tensor | None = None  # fp32 [E], W4A4 only
+    q8_gate_up: Q8Tensor | None = None    # int8 block weights
+    q8_down: Q8Tensor | None = None
 
     def to(self, device) -> "MoEInputs":
         def mv(t):
@@ -95,10 +108,13 @@ class MoEInputs:
         def mvq(q):
             return None if q is None else NVFP4Tensor(mv(q.codes), mv(q.scales), mv(q.glob))
 
+        def mv8(q):
+            return None if q is None else Q8Tensor(mv(q.codes), mv(q.scales))
+
         return MoEInputs(self.T, self.H, self.E, self.top_k, self.I, mv(self.x), mv(self.gate_w),
                          mv(self.bias), mv(self.w_gate_up), mv(self.w_down),
                          mvq(self.nvfp4_gate_up), mvq(self.nvfp4_down), dict(self.meta),
-                         mv(self.x_global), mv(self.h_global))
+                         mv(self.x_global), mv(self.h_global), mv8(self.q8_gate_up), mv8(self.q8_down))
 
 
 def zipf_router_bias(E: int, s: float = 1.1, scale: float = 0.5) -> torch.Tensor:
@@ -154,6 +170,21 @@ def nvfp4_encode(w: torch.Tensor) -> NVFP4Tensor:
     return NVFP4Tensor(codes, scales.contiguous(), glob.float().contiguous())
 
 
+# ---------------------------------------------------------------- int8 encode
+def q8_encode(w: torch.Tensor) -> Q8Tensor:
+    """Encode fp32 weights [E, R, K] (K % 32 == 0) to int8 blocks: per 32
+    consecutive K the scale d = fp16(amax / 127) (torch's round to nearest
+    even) and the codes round(w / d) (half to even) clamped to [-127, 127]."""
+    E, R, K = w.shape
+    assert K % 32 == 0
+    blocks = w.float().view(E, R, K // 32, 32)
+    d = (blocks.abs().amax(dim=-1) / 127.0).to(torch.float16)
+    d32 = d.float().unsqueeze(-1)
+    q = torch.where(d32 > 0, blocks / d32, torch.zeros_like(blocks))
+    codes = torch.round(q).clamp(-127, 127).to(torch.int8).view(E, R, K)
+    return Q8Tensor(codes.contiguous(), d.contiguous())
+
+
 # ---------------------------------------------------------------- generator
 def make_inputs(workload: str | dict, seed: int = 0, device: str | torch.device = "cpu",
                 **overrides) -> MoEInputs:
@@ -185,6 +216,10 @@ def make_inputs(workload: str | dict, seed: int = 0, device: str | torch.device 
                   else torch.as_tensor(hg, dtype=torch.float32)).to(dev)
         return MoEInputs(T, H, E, k, I, x, gate_w, bias, None, None, gu, dn, meta=cfg, x_global=xg,
                          h_global=hg)
+    if cfg.get("q8"):
+        gu = q8_encode(draw((E, 2 * I, H), 0.02))
+        dn = q8_encode(draw((E, H, I), 0.02))
+        return MoEInputs(T, H, E, k, I, x, gate_w, bias, None, None, meta=cfg, q8_gate_up=gu, q8_down=dn)
     w_gate_up = draw((E, 2 * I, H), 0.02).to(torch.bfloat16)
     w_down = draw((E, H, I), 0.02).to(torch.bfloat16)
     return MoEInputs(T, H, E, k, I, x, gate_w, bias, w_gate_up, w_down, meta=cfg)

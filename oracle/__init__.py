@@ -9,8 +9,8 @@ import numpy as np
 
 from . import moe_oracle
 from .moe_oracle import (ExpertWeights, bf16_to_f64, e2m1_quantize, e2m1_to_f64, e4m3_quantize,
-                         e4m3_to_f64, forward, forward_w4a4, nvfp4_dequant, nvfp4_quantize, permute,
-                         route, silu, softmax)
+                         e4m3_to_f64, f16_to_f64, forward, forward_w4a4, nvfp4_dequant, nvfp4_quantize,
+                         permute, q8_dequant, route, silu, softmax)
 
 
 def _np(t):
@@ -24,7 +24,11 @@ def _bits16(t):
 def forward_from_inputs(inp, tokens=None):
     """Run the oracle on a ``moe_inputs.MoEInputs`` bundle (torch tensors on
     any device; they are copied to the host as raw bits)."""
-    if inp.nvfp4_gate_up is not None:
+    if getattr(inp, "q8_gate_up", None) is not None:
+        q, d = inp.q8_gate_up, inp.q8_down
+        weights = ExpertWeights(q8_gate_up=(_np(q.codes), _bits16(q.scales)),
+                                q8_down=(_np(d.codes), _bits16(d.scales)))
+    elif inp.nvfp4_gate_up is not None:
         q = inp.nvfp4_gate_up
         d = inp.nvfp4_down
         weights = ExpertWeights(nvfp4_gate_up=(_np(q.codes), _np(q.scales), _np(q.glob)),

@@ -26,7 +26,8 @@ for a Qwen3-style SwiGLU MoE layer:
   7. combine         out[t] = sum_{s=0..k-1} w[t,s]*y[t,s], summed in s order
 
 NVFP4 weights are decoded exactly to fp64 (e2m1 code x e4m3 block scale x fp32
-global) and then used as in step 6.
+global) and then used as in step 6.  Int8 block weights (``q8_dequant``:
+int8 code x fp16 scale per 32 consecutive elements along K) likewise.
 
 W4A4 (``forward_w4a4``): NVFP4 weights and NVFP4 activations.  The pages
 name the NVFP4 deployment (page "vLLM 0.32 升级试验：TEP2 prefill 诅咒解除 +
@@ -106,6 +107,31 @@ def nvfp4_dequant(codes: np.ndarray, scales: np.ndarray, glob: np.ndarray) -> np
     elem *= np.repeat(sc, 16, axis=2)
     elem *= np.asarray(glob, dtype=np.float32).astype(np.float64).reshape(E, 1, 1)
     return elem
+
+
+def f16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Decode IEEE binary16 bit patterns: 1 sign bit, 5 exponent bits (bias
+    15), 10 fraction bits; exponent field 0 is subnormal (0.f x 2^-14),
+    field 31 is infinity / NaN."""
+    b = np.asarray(bits, dtype=np.int64) & 0xFFFF
+    sign = np.where(b >> 15, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = b & 0x3FF
+    mag = np.where(e == 0, np.ldexp(f / 1024.0, -14), np.ldexp(1.0 + f / 1024.0, e - 15))
+    mag = np.where(e == 31, np.where(f == 0, np.inf, np.nan), mag)
+    return sign * mag
+
+
+def q8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Decode int8 block weights [E, R, K] to fp64.
+
+    codes  int8 [E, R, K]: one signed byte per element
+    scales fp16 bits (uint16) [E, R, K/32]: the scale of the 32-element block k//32
+    W[e,r,k] = code * scale[e,r,k//32]; each product is exact in fp64 (an
+    8-bit and an 11-bit significand)."""
+    c = np.asarray(codes, dtype=np.int8).astype(np.float64)
+    sc = f16_to_f64(np.asarray(scales, dtype=np.uint16))
+    return c * np.repeat(sc, 32, axis=2)
 
 
 # ----------------------------------------------------------------- router
@@ -212,11 +238,19 @@ def expert_swiglu(X: np.ndarray, w_gu: np.ndarray, w_dn: np.ndarray) -> np.ndarr
 class ExpertWeights:
     """Expert weights decoded to fp64 on demand, one expert at a time."""
 
-    def __init__(self, w_gate_up_bits=None, w_down_bits=None, nvfp4_gate_up=None, nvfp4_down=None):
+    def __init__(self, w_gate_up_bits=None, w_down_bits=None, nvfp4_gate_up=None, nvfp4_down=None,
+                 q8_gate_up=None, q8_down=None):
         self.gu_bits, self.dn_bits = w_gate_up_bits, w_down_bits
         self.q_gu, self.q_dn = nvfp4_gate_up, nvfp4_down
+        self.q8_gu, self.q8_dn = q8_gate_up, q8_down
 
     def get(self, e: int):
+        if self.q8_gu is not None:
+            c, s = self.q8_gu
+            gu = q8_dequant(c[e:e + 1], s[e:e + 1])[0]
+            c, s = self.q8_dn
+            dn = q8_dequant(c[e:e + 1], s[e:e + 1])[0]
+            return gu, dn
         if self.q_gu is not None:
             c, s, g = self.q_gu
             gu = nvfp4_dequant(c[e:e + 1], s[e:e + 1], g[e:e + 1])[0]

@@ -149,6 +149,69 @@ def pin_nvfp4_forward_matches_bf16(o):
     assert np.array_equal(a["out"], b["out"]), np.abs(a["out"] - b["out"]).max()
 
 
+# ------------------------------------------------------------------ int8 block weights
+
+def pin_f16_table(o):
+    """fp16 decoding against the binary16 table (exact fractions) and numpy's
+    float16 (a library routine) on every pattern."""
+    for code, val in _read_table("f16_bits.txt"):
+        got = o.f16_to_f64(np.array([code], dtype=np.uint16))[0]
+        if val == "nan":
+            assert math.isnan(got), hex(code)
+        elif val in ("inf", "-inf"):
+            assert got == float(val), hex(code)
+        else:
+            exp = _val(val)
+            assert got == exp and math.copysign(1, got) == math.copysign(1, exp), (hex(code), got, val)
+    allb = np.arange(65536, dtype=np.uint16)
+    lib = allb.view(np.float16).astype(np.float64)
+    got = o.f16_to_f64(allb)
+    fin = np.isfinite(lib)
+    assert np.array_equal(got[fin], lib[fin]) and np.array_equal(np.isnan(got), np.isnan(lib))
+
+
+def pin_q8_layout(o):
+    """Element k of an int8 block row is its signed code times the fp16 scale
+    of block k//32 (numpy's float16 decoding, exact products)."""
+    rng = _rng(17)
+    E, R, K = 2, 3, 96
+    codes = rng.integers(-128, 128, size=(E, R, K)).astype(np.int8)
+    scales = rng.integers(0, 0x7C00, size=(E, R, K // 32)).astype(np.uint16)
+    W = o.q8_dequant(codes, scales)
+    sc = scales.view(np.float16).astype(np.float64)
+    for e in range(E):
+        for r in range(R):
+            for k in range(K):
+                assert W[e, r, k] == float(codes[e, r, k]) * sc[e, r, k // 32], (e, r, k)
+
+
+def pin_q8_forward_matches_bf16(o):
+    """The layer with int8 block weights equals the layer with the same
+    weights as bf16 bits: scales that are powers of two (different per
+    expert, projection and block) times 8-bit codes are exact in bf16."""
+    rng = _rng(18)
+    T, H, E, k, I = 7, 64, 3, 2, 32
+
+    def q8(R, K, lo, hi):
+        codes = rng.integers(-127, 128, size=(E, R, K)).astype(np.int8)
+        exps = rng.integers(lo, hi, size=(E, R, K // 32))
+        scales = np.ldexp(1.0, exps).astype(np.float16).view(np.uint16)
+        vals = codes.astype(np.float64) * np.repeat(np.ldexp(1.0, exps), 32, axis=2)
+        bits = _bf16_round(vals.astype(np.float32))
+        back = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        assert np.array_equal(back, vals)   # the construction is bf16-exact
+        return (codes, scales), bits
+
+    q_gu, b_gu = q8(2 * I, H, -9, -5)
+    q_dn, b_dn = q8(H, I, -8, -4)
+    xb = _rand_bf16(rng, (T, H), 1.0)
+    gb = _rand_bf16(rng, (E, H), 0.5)
+    a = o.forward(xb, gb, None, k, o.ExpertWeights(q8_gate_up=q_gu, q8_down=q_dn))
+    b = o.forward(xb, gb, None, k, o.ExpertWeights(b_gu, b_dn))
+    assert set(np.unique(a["idx"])) == set(range(E)), a["idx"]
+    assert np.array_equal(a["out"], b["out"]), np.abs(a["out"] - b["out"]).max()
+
+
 # ------------------------------------------------------------------ W4A4 quantiser
 
 def _torch_e4m3_bytes(v32):

@@ -289,6 +289,47 @@ def _mut_nvfp4_scale_without_global(m):
     m.nvfp4_quantize = nvfp4_quantize
 
 
+def _mut_q8_block16(m):
+    # one scale per 16 elements instead of 32
+    def q8_dequant(codes, scales):
+        c = np.asarray(codes, dtype=np.int8).astype(np.float64)
+        sc = m.f16_to_f64(np.asarray(scales, dtype=np.uint16))
+        rep = np.repeat(sc, 16, axis=2)
+        rep = np.concatenate([rep, rep], axis=2)[:, :, :c.shape[2]]
+        return c * rep
+    m.q8_dequant = q8_dequant
+
+
+def _mut_q8_unsigned(m):
+    # codes read as unsigned bytes
+    def q8_dequant(codes, scales):
+        c = np.asarray(codes, dtype=np.int8).view(np.uint8).astype(np.float64)
+        return c * np.repeat(m.f16_to_f64(np.asarray(scales, dtype=np.uint16)), 32, axis=2)
+    m.q8_dequant = q8_dequant
+
+
+def _mut_f16_bias(m):
+    # fp16 exponent bias taken as 16
+    orig = m.f16_to_f64
+    m.f16_to_f64 = lambda bits: orig(bits) * 0.5
+
+
+def _mut_q8_expert0_scales(m):
+    # every expert decoded with expert 0's scales
+    def get(self, e):
+        if self.q8_gu is not None:
+            (cg, sg), (cd, sd) = self.q8_gu, self.q8_dn
+            return m.q8_dequant(cg[e:e + 1], sg[0:1])[0], m.q8_dequant(cd[e:e + 1], sd[0:1])[0]
+        if self.q_gu is not None:
+            c, s, g = self.q_gu
+            gu = m.nvfp4_dequant(c[e:e + 1], s[e:e + 1], g[e:e + 1])[0]
+            c, s, g = self.q_dn
+            dn = m.nvfp4_dequant(c[e:e + 1], s[e:e + 1], g[e:e + 1])[0]
+            return gu, dn
+        return m.bf16_to_f64(self.gu_bits[e]), m.bf16_to_f64(self.dn_bits[e])
+    m.ExpertWeights.get = get
+
+
 MUTANTS = [v for k, v in sorted(globals().items()) if k.startswith("_mut_")]
 
 
