@@ -6,8 +6,8 @@
 A step is one moe_forward (router, grouping, gate/up + SwiGLU, down, combine)
 over one batch of a workload.  Without --workload the run measures every
 workload: decode8 (T=8, the headline `value`), then decode64, prefill8192,
-nvfp4_256 and tiny under "configs", each with its own value, roofline,
-parity and CPU baseline.  With --workload only that one is measured.
+nvfp4_256, tiny, prefill8192_w4a4 and int8_256 under "configs", each with its
+own value, roofline, parity and CPU baseline.  With --workload only that one is measured.
 
 Per workload, in this order:
   1. one forward through the C ABI, then the parity gate: expert ids,
@@ -48,7 +48,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HEADLINE = "decode8"
-CONFIGS = ["decode8", "decode64", "prefill8192", "nvfp4_256", "tiny", "prefill8192_w4a4"]
+CONFIGS = ["decode8", "decode64", "prefill8192", "nvfp4_256", "tiny", "prefill8192_w4a4", "int8_256"]
 WEIGHT_SETS = 4
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ["route", "permute", "stream", "tc", "combine"]
@@ -56,7 +56,7 @@ STAGES = ["route", "permute", "stream", "tc", "combine"]
 STAGES_W4A4 = ["route", "permute", "quant_x", "tc", "combine"]
 # nominal dense FP4 / bf16 tensor throughput of GB300 (13.5 / 2.25 PFLOP/s)
 FP4_OVER_BF16 = 6.0
-TOL = {"bf16": 1e-2, "nvfp4": 3e-2}   # max|out - ref| <= TOL * max|ref|
+TOL = {"bf16": 1e-2, "nvfp4": 3e-2, "int8": 1e-2}   # max|out - ref| <= TOL * max|ref|
 
 
 def parse_args(argv=None):
@@ -229,7 +229,8 @@ def group_split(inp, counts):
     T, H, k = inp.T, inp.H, inp.top_k
     thr = 32 if T * k >= 8192 else 65
     w4a4 = getattr(inp, "x_global", None) is not None   # every group on the block-scaled tensor cores
-    use_tc = w4a4 or (inp.nvfp4_gate_up is None and T >= thr and H % 256 == 0)
+    bf16 = inp.nvfp4_gate_up is None and getattr(inp, "q8_gate_up", None) is None
+    use_tc = w4a4 or (bf16 and T >= thr and H % 256 == 0)
     tc_all = use_tc and (w4a4 or T * k >= 8192)
     act = [int(c) for c in counts if c > 0]
     large = [c for c in act if use_tc and (tc_all or c >= thr)]
@@ -241,7 +242,8 @@ def algorithmic_bytes(inp, split):
     """Compulsory HBM bytes per stage for one forward."""
     T, H, E, k, I = inp.T, inp.H, inp.E, inp.top_k, inp.I
     S = T * k
-    wb = 0.5 + 1.0 / 16 if inp.nvfp4_gate_up is not None else 2.0   # bytes per weight
+    # bytes per weight: NVFP4 codes + e4m3 scale per 16, int8 + fp16 scale per 32, bf16
+    wb = 0.5 + 1.0 / 16 if inp.nvfp4_gate_up is not None else 1.0 + 2.0 / 32 if inp.q8_gate_up is not None else 2.0
     pb = 4 if S * H * 4 <= (32 << 20) else 2                        # bytes per partial
     per_row = H * 2 + 2 * I * 2 + H * pb   # token row in, h out and back in, partial out
     A = split["A_s"] + split["A_l"]
@@ -277,6 +279,8 @@ bias = np.array(ld("bias")) if meta["bias"] else None
 if meta["nvfp4"]:
     W = oracle.ExpertWeights(nvfp4_gate_up=(ld("gu_codes"), ld("gu_scales"), ld("gu_glob")),
                              nvfp4_down=(ld("dn_codes"), ld("dn_scales"), ld("dn_glob")))
+elif meta.get("int8"):
+    W = oracle.ExpertWeights(q8_gate_up=(ld("gu_q8"), ld("gu_q8s")), q8_down=(ld("dn_q8"), ld("dn_q8s")))
 else:
     W = oracle.ExpertWeights(ld("w_gate_up"), ld("w_down"))
 x, gw, k = np.array(ld("x")), np.array(ld("gate_w")), meta["top_k"]
@@ -320,6 +324,7 @@ _CHILD_ENV = dict(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS
 def dump_inputs(inp, d):
     """Raw input bits of one workload (weight set 0) for the oracle children."""
     import numpy as np
+    import torch
 
     import moe_inputs as mi
 
@@ -335,6 +340,10 @@ def dump_inputs(inp, d):
             save(pre + "_codes", q.codes.cpu().numpy())
             save(pre + "_scales", q.scales.cpu().numpy())
             save(pre + "_glob", q.glob.cpu().numpy())
+    elif inp.q8_gate_up is not None:
+        for pre, q in (("gu", inp.q8_gate_up), ("dn", inp.q8_down)):
+            save(pre + "_q8", q.codes.cpu().numpy())
+            save(pre + "_q8s", q.scales.cpu().view(torch.int16).numpy().view("uint16"))
     else:
         save("w_gate_up", mi.bf16_bits(inp.w_gate_up))
         save("w_down", mi.bf16_bits(inp.w_down))
@@ -344,7 +353,7 @@ def dump_inputs(inp, d):
         save("h_global", inp.h_global.cpu().numpy())
     with open(os.path.join(d, "meta.json"), "w") as f:
         json.dump({"bias": inp.bias is not None, "nvfp4": inp.nvfp4_gate_up is not None,
-                   "top_k": inp.top_k, "w4a4": w4a4}, f)
+                   "int8": inp.q8_gate_up is not None, "top_k": inp.top_k, "w4a4": w4a4}, f)
 
 
 def _child(d, job):
@@ -462,7 +471,7 @@ def parity_gate(inp, out, idx, w, grp, ref, rows):
     o = out.float().cpu().double().numpy()[rows]
     scale = float(np.abs(ref["out"]).max())
     rel = float(np.abs(o - ref["out"]).max() / scale) if scale > 0 else float(np.abs(o).max())
-    tol = TOL["nvfp4" if inp.nvfp4_gate_up is not None else "bf16"]
+    tol = TOL["nvfp4" if inp.nvfp4_gate_up is not None else "int8" if inp.q8_gate_up is not None else "bf16"]
     ok = bad_tokens == 0 and grouping_exact and rel <= tol and w_rel <= 1e-4
     return {"pass": bool(ok), "ids_tokens_checked": int(inp.T), "ids_tokens_differing": bad_tokens,
             "grouping_bit_exact": grouping_exact, "weights_max_rel_err": w_rel,
@@ -487,6 +496,7 @@ def measure(name, args, ctx, headline):
     wname = workload_name(name, args.tokens)
     T, H, E, k, I = inp.T, inp.H, inp.E, inp.top_k, inp.I
     nv = inp.nvfp4_gate_up is not None
+    q8 = inp.q8_gate_up is not None
 
     # weight sets cycled across steps
     w4a4 = inp.x_global is not None
@@ -509,13 +519,20 @@ def measure(name, args, ctx, headline):
             st = moe._NVFP4(q.codes.data_ptr(), q.scales.data_ptr(), q.glob.data_ptr(),
                             d.codes.data_ptr(), d.scales.data_ptr(), d.glob.data_ptr())
             sets.append((None, None, ctypes.byref(st), (q, d, st)))
+        elif q8:
+            q = inp.q8_gate_up if r == 0 else moe_inputs.Q8Tensor(inp.q8_gate_up.codes.clone(),
+                                                                  inp.q8_gate_up.scales.clone())
+            d = inp.q8_down if r == 0 else moe_inputs.Q8Tensor(inp.q8_down.codes.clone(), inp.q8_down.scales.clone())
+            st = moe.int8_struct(q, d)
+            sets.append((None, None, ctypes.byref(st), (q, d, st)))
         else:
             gu = inp.w_gate_up if r == 0 else inp.w_gate_up.clone()
             dn = inp.w_down if r == 0 else inp.w_down.clone()
             sets.append((ctypes.c_void_p(gu.data_ptr()), ctypes.c_void_p(dn.data_ptr()), None, (gu, dn)))
     weight_bytes_per_set = (sum(t.numel() * t.element_size() for t in (
         [inp.nvfp4_gate_up.codes, inp.nvfp4_gate_up.scales, inp.nvfp4_down.codes, inp.nvfp4_down.scales]
-        if nv else [inp.w_gate_up, inp.w_down])))
+        if nv else [inp.q8_gate_up.codes, inp.q8_gate_up.scales, inp.q8_down.codes, inp.q8_down.scales]
+        if q8 else [inp.w_gate_up, inp.w_down])))
 
     ws = moe.alloc_workspace(T, H, E, I, k, dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -530,6 +547,8 @@ def measure(name, args, ctx, headline):
         gu, dn, nvp, _ = sets[i % nsets]
         if w4a4:
             rc = lib.moe_forward_w4a4(xp, g_p, b_p, nvp, T, H, E, I, k, op, None, None, ws_p, wsn, sptr)
+        elif q8:
+            rc = lib.moe_forward_int8(xp, g_p, b_p, nvp, T, H, E, I, k, op, None, None, ws_p, wsn, sptr)
         else:
             rc = lib.moe_forward(xp, g_p, b_p, gu, dn, nvp, T, H, E, I, k, op, None, None, ws_p, wsn, sptr)
         if rc != 0:
@@ -541,6 +560,9 @@ def measure(name, args, ctx, headline):
     if w4a4:
         moe.forward_w4a4(inp.x, inp.gate_w, inp.bias, sets[0][3][2], k, out=out, workspace=ws, topk_idx=idx,
                          topk_w=wts)
+    elif q8:
+        moe.forward_int8(inp.x, inp.gate_w, inp.bias, inp.q8_gate_up, inp.q8_down, k, out=out, workspace=ws,
+                         topk_idx=idx, topk_w=wts)
     else:
         moe.forward(inp.x, inp.gate_w, inp.bias, inp.w_gate_up, inp.w_down, k, nvfp4_gate_up=inp.nvfp4_gate_up,
                     nvfp4_down=inp.nvfp4_down, out=out, workspace=ws, topk_idx=idx, topk_w=wts)
@@ -610,6 +632,9 @@ def measure(name, args, ctx, headline):
         gu, dn, nvp, _ = sets[i % nsets]
         if w4a4:
             rc = lib.moe_forward_w4a4_profiled(x_p, g_p, b_p, nvp, T, H, E, I, k, o_p, None, None, ws_p, wsn,
+                                               sptr, ev_ptrs[i], ctypes.byref(nk))
+        elif q8:
+            rc = lib.moe_forward_int8_profiled(x_p, g_p, b_p, nvp, T, H, E, I, k, o_p, None, None, ws_p, wsn,
                                                sptr, ev_ptrs[i], ctypes.byref(nk))
         else:
             rc = lib.moe_forward_profiled(x_p, g_p, b_p, gu, dn, nvp, T, H, E, I, k, o_p, None, None, ws_p,
@@ -717,9 +742,10 @@ def measure(name, args, ctx, headline):
         "steps": K,
         "warmup": W,
         "ms_per_step": step_ms,
-        "dtype": "nvfp4-w4a4/f32acc" if w4a4 else "nvfp4-w4a16/bf16/f32acc" if nv else "bf16/f32acc",
+        "dtype": ("nvfp4-w4a4/f32acc" if w4a4 else "nvfp4-w4a16/bf16/f32acc" if nv
+                  else "int8-w8a16/f16/f32acc" if q8 else "bf16/f32acc"),
         "config": {"workload": wname, "T": T, "H": H, "E": E, "top_k": k, "I": I,
-                   "weights": "nvfp4" if nv else "bf16", "activations": "nvfp4" if w4a4 else "bf16",
+                   "weights": "nvfp4" if nv else "int8" if q8 else "bf16", "activations": "nvfp4" if w4a4 else "bf16",
                    "router_bias": "0.5*log-Zipf(1.1)" if inp.bias is not None else None,
                    "seed": args.seed, "parallelism": f"replicas x{world}",
                    "l2": f"{nsets} rotating expert-weight sets of {weight_bytes_per_set / 1e9:.3f} GB "

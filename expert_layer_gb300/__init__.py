@@ -42,6 +42,11 @@ class _NVFP4(ctypes.Structure):
                 ("dn_scales", ctypes.c_void_p), ("dn_global", ctypes.c_void_p)]
 
 
+class _INT8(ctypes.Structure):
+    _fields_ = [("gu_codes", ctypes.c_void_p), ("gu_scales", ctypes.c_void_p),
+                ("dn_codes", ctypes.c_void_p), ("dn_scales", ctypes.c_void_p)]
+
+
 _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -59,6 +64,9 @@ _SIGNATURES = {
     "moe_route_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_forward_w4a4": (_I, [_P, _P, _P, ctypes.POINTER(_W4A4), _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_w4a4_profiled": (_I, [_P, _P, _P, ctypes.POINTER(_W4A4), _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                       _SZ, _P, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_int32)]),
+    "moe_forward_int8": (_I, [_P, _P, _P, ctypes.POINTER(_INT8), _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_int8_profiled": (_I, [_P, _P, _P, ctypes.POINTER(_INT8), _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                        _SZ, _P, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_int32)]),
     "moe_nvfp4_tc_scales": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "moe_nvfp4_quantize": (_I, [_P, _I, _I, ctypes.c_float, _P, _P, _P]),
@@ -282,6 +290,47 @@ def forward_w4a4(x, gate_w, bias, weights: W4A4Weights, top_k, out=None, workspa
                                 top_k, _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace),
                                 workspace.numel(), _stream(stream))
     _check(rc, "moe_forward_w4a4")
+    return out
+
+
+def int8_struct(gate_up, down):
+    """The ``moe_int8_weights`` struct of two int8 block tensors (objects with
+    ``codes`` int8 [E, R, K] and ``scales`` float16 [E, R, K/32])."""
+    return _INT8(gate_up.codes.data_ptr(), gate_up.scales.data_ptr(), down.codes.data_ptr(),
+                 down.scales.data_ptr())
+
+
+def forward_int8(x, gate_w, bias, gate_up, down, top_k, out=None, workspace=None, topk_idx=None,
+                 topk_w=None, stream=None):
+    """The MoE layer forward with int8 block expert weights (W8A16); returns
+    out bf16 [T, H].  ``gate_up`` / ``down``: objects with ``codes`` (int8
+    [E, 2I, H] / [E, H, I]) and ``scales`` (float16, one per 32 elements
+    along K)."""
+    T, H = x.shape
+    E = gate_w.shape[0]
+    I = gate_up.codes.shape[1] // 2
+    _want(x, torch.bfloat16, (T, H), "x")
+    _want(gate_w, torch.bfloat16, (E, H), "gate_w")
+    if bias is not None:
+        _want(bias, torch.float32, (E,), "bias")
+    _want(gate_up.codes, torch.int8, (E, 2 * I, H), "gate_up codes")
+    _want(gate_up.scales, torch.float16, (E, 2 * I, H // 32), "gate_up scales")
+    _want(down.codes, torch.int8, (E, H, I), "down codes")
+    _want(down.scales, torch.float16, (E, H, I // 32), "down scales")
+    st = int8_struct(gate_up, down)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _want(out, torch.bfloat16, (T, H), "out")
+    if topk_idx is not None:
+        _want(topk_idx, torch.int32, (T, top_k), "topk_idx")
+    if topk_w is not None:
+        _want(topk_w, torch.float32, (T, top_k), "topk_w")
+    if workspace is None:
+        workspace = alloc_workspace(max(T, 1), H, E, I, top_k, x.device)
+    rc = lib().moe_forward_int8(_ptr(x), _ptr(gate_w), _ptr(bias), ctypes.byref(st), T, H, E, I, top_k,
+                                _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(),
+                                _stream(stream))
+    _check(rc, "moe_forward_int8")
     return out
 
 

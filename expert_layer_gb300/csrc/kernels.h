@@ -61,12 +61,16 @@ struct StreamGemmArgs {
   const uint8_t* gu_codes;   // NVFP4 (or null)
   const uint8_t* gu_scales;
   const float* gu_global;
-  uint16_t* h;               // [S, I] grouped order: bf16, or f16 on the NVFP4 path
+  const int8_t* gu_q8;       // int8 block weights [E, 2I, H] (or null)
+  const uint16_t* gu_q8s;    // their fp16 scales [E, 2I, H/32]
+  uint16_t* h;               // [S, I] grouped order: bf16, or f16 on the NVFP4 and int8 paths
   // down
   const uint16_t* w_down;    // [E, H, I]
   const uint8_t* dn_codes;
   const uint8_t* dn_scales;
   const float* dn_global;
+  const int8_t* dn_q8;       // [E, H, I]
+  const uint16_t* dn_q8s;    // [E, H, I/32]
   const float* topk_w;       // [S]
   void* partial;             // [S, H] fp32 or bf16, slot order
   bool partial_f32;

@@ -164,7 +164,7 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int top_k, int32_t* count
 
 static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* bias,
                         const uint16_t* w_gate_up, const uint16_t* w_down,
-                        const moe_nvfp4_weights* nvfp4, int T, int H, int E, int I, int top_k,
+                        const moe_nvfp4_weights* nvfp4, const moe_int8_weights* q8, int T, int H, int E, int I, int top_k,
                         uint16_t* out, int32_t* topk_idx, float* topk_w, void* workspace,
                         size_t workspace_bytes, void* stream, void* const* events,
                         int* launches) {
@@ -177,7 +177,13 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   if (bias && !aligned16(bias)) return MOE_ERR_UNSUPPORTED;
   if (topk_idx && !aligned16(topk_idx)) return MOE_ERR_UNSUPPORTED;
   if (topk_w && !aligned16(topk_w)) return MOE_ERR_UNSUPPORTED;
-  if (nvfp4) {
+  if (q8) {
+    if (w_gate_up || w_down || nvfp4) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ptr(q8->gu_codes));
+    MOE_TRY(check_ptr(q8->gu_scales));
+    MOE_TRY(check_ptr(q8->dn_codes));
+    MOE_TRY(check_ptr(q8->dn_scales));
+  } else if (nvfp4) {
     if (w_gate_up || w_down) return MOE_ERR_INVALID_ARG;
     MOE_TRY(check_ptr(nvfp4->gu_codes));
     MOE_TRY(check_ptr(nvfp4->gu_scales));
@@ -211,7 +217,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   // exceed T rows, so small batches skip them.
   const bool prefill = (long long)T * top_k >= 8192;
   const int large = prefill ? kLargeGroupPrefill : kLargeGroupDecode;
-  const bool use_tc = !nvfp4 && T >= large && H % 256 == 0 && num_sms >= 2;
+  const bool use_tc = !nvfp4 && !q8 && T >= large && H % 256 == 0 && num_sms >= 2;
   // At prefill sizes every group goes to the tensor-core kernels: a 128-row
   // tile of a small group costs the whole GPU about 0.7 us of tensor time,
   // less than streaming that expert's 9.4 MB of weights, and the streaming
@@ -252,6 +258,10 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
     a.gu_codes = nvfp4->gu_codes; a.gu_scales = nvfp4->gu_scales; a.gu_global = nvfp4->gu_global;
     a.dn_codes = nvfp4->dn_codes; a.dn_scales = nvfp4->dn_scales; a.dn_global = nvfp4->dn_global;
   }
+  if (q8) {
+    a.gu_q8 = q8->gu_codes; a.gu_q8s = q8->gu_scales;
+    a.dn_q8 = q8->dn_codes; a.dn_q8s = q8->dn_scales;
+  }
   a.h = ws_ptr<uint16_t>(workspace, L.h);
   a.topk_w = w;
   a.partial = ws_ptr<void>(workspace, L.partial);
@@ -269,8 +279,8 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   tc.h = a.h; tc.partial = a.partial; tc.partial_f32 = L.partial_f32;
   tc.status = &hdr->status; tc.num_sms = num_sms;
 
-  if (nvfp4) {
-    // the NVFP4 expert kernels multiply in f16: x converted once per call
+  if (nvfp4 || q8) {
+    // the NVFP4 and int8 expert kernels multiply in f16: x converted once per call
     a.x16 = ws_ptr<uint16_t>(workspace, L.x16);
     MOE_TRY_CUDA(launch_to_f16(x, (size_t)T * H, ws_ptr<uint16_t>(workspace, L.x16), &hdr->status, s,
                                launches));
@@ -291,8 +301,8 @@ int moe_forward(const uint16_t* x, const uint16_t* gate_w, const float* bias,
                 const uint16_t* w_gate_up, const uint16_t* w_down, const moe_nvfp4_weights* nvfp4,
                 int T, int H, int E, int I, int top_k, uint16_t* out, int32_t* topk_idx,
                 float* topk_w, void* workspace, size_t workspace_bytes, void* stream) {
-  return forward_impl(x, gate_w, bias, w_gate_up, w_down, nvfp4, T, H, E, I, top_k, out, topk_idx,
-                      topk_w, workspace, workspace_bytes, stream, nullptr, nullptr);
+  return forward_impl(x, gate_w, bias, w_gate_up, w_down, nvfp4, nullptr, T, H, E, I, top_k, out,
+                      topk_idx, topk_w, workspace, workspace_bytes, stream, nullptr, nullptr);
 }
 
 int moe_forward_profiled(const uint16_t* x, const uint16_t* gate_w, const float* bias,
@@ -305,7 +315,31 @@ int moe_forward_profiled(const uint16_t* x, const uint16_t* gate_w, const float*
   for (int i = 0; i < 6; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   int n = 0;
-  const int rc = forward_impl(x, gate_w, bias, w_gate_up, w_down, nvfp4, T, H, E, I, top_k, out,
+  const int rc = forward_impl(x, gate_w, bias, w_gate_up, w_down, nvfp4, nullptr, T, H, E, I, top_k,
+                              out, topk_idx, topk_w, workspace, workspace_bytes, stream, events, &n);
+  if (kernels_launched) *kernels_launched = n;
+  return rc;
+}
+
+// ------------------------------------------------------------------ int8
+int moe_forward_int8(const uint16_t* x, const uint16_t* gate_w, const float* bias, const moe_int8_weights* w,
+                     int T, int H, int E, int I, int top_k, uint16_t* out, int32_t* topk_idx, float* topk_w,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  return forward_impl(x, gate_w, bias, nullptr, nullptr, nullptr, w, T, H, E, I, top_k, out, topk_idx,
+                      topk_w, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+int moe_forward_int8_profiled(const uint16_t* x, const uint16_t* gate_w, const float* bias,
+                              const moe_int8_weights* w, int T, int H, int E, int I, int top_k,
+                              uint16_t* out, int32_t* topk_idx, float* topk_w, void* workspace,
+                              size_t workspace_bytes, void* stream, void* const* events,
+                              int32_t* kernels_launched) {
+  if (!w || !events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  int n = 0;
+  const int rc = forward_impl(x, gate_w, bias, nullptr, nullptr, nullptr, w, T, H, E, I, top_k, out,
                               topk_idx, topk_w, workspace, workspace_bytes, stream, events, &n);
   if (kernels_launched) *kernels_launched = n;
   return rc;

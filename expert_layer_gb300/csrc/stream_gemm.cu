@@ -42,6 +42,15 @@
 // path: exact for activations of magnitude 2^-14 .. 65504, below that
 // rounded to the f16 subnormal grid (absolute error <= 2^-25), above it
 // flagged (kStatusRange).
+//
+// Int8 block weights (W8A16): int8 codes with one fp16 scale per 32
+// consecutive elements along K.  Thread (g, c) loads, per 64-wide K block, 8
+// codes of each of the block's two scale blocks (k = 8c..8c+7 and
+// 32+8c..32+8c+7), so every mma step stays inside one scale block.  Codes
+// become f16 exactly (integers of magnitude <= 127), the mma sums code x
+// activation over one scale block on the f16 token rows (the products are
+// exact in the fp32 accumulator), and the row's scale multiplies that fp32
+// partial sum before it joins the accumulator.
 #include <type_traits>
 
 #include "common.cuh"
@@ -61,31 +70,61 @@ __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
   const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem) : "memory");
 }
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(gmem) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+namespace q8 {
+// Four int8 codes (byte i = element i) to two f16x2 pairs, exact: each byte,
+// offset by 128 with the sign-bit flip, becomes the mantissa of the f16
+// 1024 + (q + 128) (0x64 in the high byte), and 1152 is subtracted.
+__device__ __forceinline__ void s8x4_f16x2(uint32_t w, uint32_t& p01, uint32_t& p23) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+  const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(p01) : "r"(lo), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(p23) : "r"(hi), "r"(0x64806480u));
+}
+// The f16 in the low (hf = 0) or high half of v, as fp32 (exact).
+__device__ __forceinline__ float f16_half_to_f32(uint32_t v, int hf) {
+  float f;
+  const uint32_t h = hf ? v >> 16 : v & 0xffffu;
+  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.f32.f16 %0, t;\n}" : "=f"(f) : "r"(h));
+  return f;
+}
+}  // namespace q8
+
+// Weight formats of the streaming kernel.
+enum : int { kFmtBf16 = 0, kFmtFp4 = 1, kFmtQ8 = 2 };
+
 // Pipeline shape per variant (NT = 8-row token tiles per pass).  A unit is
-// FR fragments of 16 weight rows.  NVFP4 units are two or four fragments
-// tall: each token-row fragment a thread loads then feeds FR mma instead of
-// one, which matters because 4-bit weights make the token rows (16-bit) the
-// larger stream whenever an expert holds more than a few rows.  With four
-// token tiles (32 rows per pass, for experts averaging 24 rows or more) the
-// unit is two fragments tall, so that an expert of up to 32 rows decodes its
-// weights once.
-template <bool kFp4, int NT = 1>
+// FR fragments of 16 weight rows.  NVFP4 and int8 units are two or four
+// fragments tall: each token-row fragment a thread loads then feeds FR mma
+// instead of one, which matters because 4- and 8-bit weights make the token
+// rows (16-bit) the larger stream whenever an expert holds more than a few
+// rows.  With four token tiles (32 rows per pass, for experts averaging 24
+// rows or more) the unit is two fragments tall, so that an expert of up to
+// 32 rows decodes its weights once.
+template <int F, int NT = 1>
 struct StreamCfg {
-  static constexpr int KB = kFp4 ? 128 : 32;      // K elements per block
-  static constexpr int KG = kFp4 ? 1 : 4;         // blocks per pipelined group
-  static constexpr int FR = kFp4 ? (NT >= 4 ? 2 : 4) : 1;   // 16-row fragments per unit
-  static constexpr int NS = kFp4 ? (NT >= 4 ? 5 : 3) : 4;   // groups in the ring (NS-1 in flight)
-  static constexpr int kWarps = kFp4 ? 8 : 12;
+  static constexpr bool kFp4 = F == kFmtFp4, kQ8 = F == kFmtQ8;
+  static constexpr bool kDec = kFp4 || kQ8;       // decoded weights, f16 operands
+  static constexpr int KB = kFp4 ? 128 : kQ8 ? 64 : 32;   // K elements per block
+  static constexpr int KG = kDec ? 1 : 4;         // blocks per pipelined group
+  static constexpr int FR = kDec ? (NT >= 4 ? 2 : 4) : 1;   // 16-row fragments per unit
+  static constexpr int NS = kDec ? (NT >= 4 ? 5 : 3) : 4;   // groups in the ring (NS-1 in flight)
+  static constexpr int kWarps = kDec ? 8 : 12;
   // per-warp ring: [NS][KG][FR][2 rows][32 lanes] x 16 B of weights (codes),
-  // plus [NS][KG][FR][2][32] x 8 B of scales for NVFP4
+  // plus the block scales of the decoded formats
   static constexpr int kWBytes = NS * KG * FR * 2 * 32 * 16;
-  // NVFP4 scales: per fragment and block the 8 scale bytes of each of its 16
-  // weight rows (one copy per row, read by the four lanes that use it)
-  static constexpr int kSBytes = kFp4 ? NS * KG * FR * 16 * 8 : 0;
+  // per fragment and block the scales of each of its 16 weight rows (one
+  // copy per row, read by the four lanes that use it): NVFP4 8 e4m3 bytes,
+  // int8 two fp16 scales
+  static constexpr int kSBytes = kFp4 ? NS * KG * FR * 16 * 8 : kQ8 ? NS * KG * FR * 16 * 4 : 0;
   static constexpr int kWarpBytes = kWBytes + kSBytes;
   static constexpr int kLutBytes = 0;
 };
@@ -175,9 +214,10 @@ __device__ __forceinline__ void load_b(uint32_t (&b)[KG][4], const uint16_t* bsr
 // rows (B) of the next group are loaded into registers one group ahead.
 // Experts with more than 8*NT routed rows take several passes; later passes
 // re-read the unit's weights from L2.
-template <bool kFp4, int NT>
-__global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_gemm_kernel(StreamGemmArgs a) {
-  using C = StreamCfg<kFp4, NT>;
+template <int F, int NT>
+__global__ void __launch_bounds__(StreamCfg<F, NT>::kWarps * 32, 1) stream_gemm_kernel(StreamGemmArgs a) {
+  using C = StreamCfg<F, NT>;
+  constexpr bool kFp4 = C::kFp4, kQ8 = C::kQ8;
   constexpr int KB = C::KB, KG = C::KG, NS = C::NS, NW = C::kWarps;
   constexpr int kFifo = 8;   // > NS: unit ids the producer may hold ahead of the consumer
   extern __shared__ __align__(16) unsigned char smem[];
@@ -274,6 +314,28 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
               cp_async8(sring + ((slot_w * KG + i) * FR + f) * 16 + lane,
                         sb + ((size_t)it.e * NR + srow) * (K / 16) + (size_t)kb * 8);
             }
+          } else if constexpr (kQ8) {
+            // 8 codes of each of the block's two 32-element scale blocks:
+            // k = 8c..8c+7 and 32+8c..32+8c+7, so that every mma step stays
+            // inside one scale block
+            const int8_t* cb = it.down ? a.dn_q8 : a.gu_q8;
+            const uint16_t* sb = it.down ? a.dn_q8s : a.gu_q8s;
+            const size_t kc = (size_t)kb * 64 + 8 * c;
+            unsigned char* dl = reinterpret_cast<unsigned char*>(d);
+            unsigned char* dh = reinterpret_cast<unsigned char*>(d + 32);
+            cp_async8(dl, cb + Rlo * K + kc);
+            cp_async8(dl + 8, cb + Rlo * K + kc + 32);
+            cp_async8(dh, cb + Rhi * K + kc);
+            cp_async8(dh + 8, cb + Rhi * K + kc + 32);
+            // lanes 0-7: the two fp16 scales of row g = lane of the low half,
+            // lanes 8-15 of the high half
+            if (lane < 16) {
+              const int r = lane & 7;
+              const int srow = it.down ? (it.blk * FR + f) * 16 + r + (lane & 8)
+                                       : (it.blk * FR + f) * 8 + r + ((lane & 8) ? a.I : 0);
+              cp_async4(reinterpret_cast<uint32_t*>(sring) + ((slot_w * KG + i) * FR + f) * 16 + lane,
+                        sb + ((size_t)it.e * NR + srow) * (K / 32) + (size_t)kb * 2);
+            }
           } else {
             const uint16_t* wb = it.down ? a.w_down : a.w_gate_up;
             const size_t kc = (size_t)kb * 32 + 8 * c;
@@ -335,7 +397,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
           else {
             int f = permp[ct.off + n];
             if (!bounds_ok((unsigned)f < (unsigned)(a.T * a.k), a.status)) f = 0;
-            bsrc[nt] = (kFp4 ? a.x16 : a.x) + (size_t)(f / a.k) * a.H;
+            bsrc[nt] = (C::kDec ? a.x16 : a.x) + (size_t)(f / a.k) * a.H;
           }
         }
       }
@@ -437,6 +499,78 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
           slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
           issue_next();
         }
+      } else if constexpr (kQ8) {
+        // int8: token rows double-buffered per 32-element scale block (one
+        // 16-byte piece per token tile: k = 8c..8c+7 of the block)
+        uint32_t bh[2][NP][4];
+        auto load_half = [&](uint32_t (&b)[NP][4], int kb, int hf) {
+  #pragma unroll
+          for (int nt = 0; nt < NP; ++nt) {
+            uint4 t = make_uint4(0, 0, 0, 0);
+            if (nt < ntiles && bsrc[nt] && kb < ct.nkb) {
+              const uint4* pp = reinterpret_cast<const uint4*>(bsrc[nt] + (size_t)kb * 64 + 32 * hf + 8 * c);
+              t = ct.down ? __ldcg(pp) : *pp;
+            }
+            b[nt][0] = t.x; b[nt][1] = t.y; b[nt][2] = t.z; b[nt][3] = t.w;
+          }
+        };
+        const uint32_t* qring = reinterpret_cast<const uint32_t*>(sring);
+        load_half(bh[0], 0, 0);
+  #pragma unroll 1
+        for (int gi = 0; gi < ct.ngroups; ++gi) {   // KG = 1: group gi = block gi
+          load_half(bh[1], gi, 1);
+          cp_async_wait<NS - 2>();
+          __syncwarp();   // the scale rows were copied by other lanes
+  #pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            if (hf == 1) load_half(bh[0], gi + 1, 0);
+            // the block's codes and scales of all FR fragments; the mma sums
+            // code x activation of one scale block (exact products, fp32
+            // sums), then the scale multiplies the fp32 partial
+            uint32_t clo[FR][2], chi[FR][2];
+            float slo[FR], shi[FR];
+  #pragma unroll
+            for (int f = 0; f < FR; ++f) {
+              const int rs = ((slot_r * FR + f) * 2) * 32 + lane;
+              const uint4 alo = ring[rs];
+              const uint4 ahi = ring[rs + 32];
+              slo[f] = q8::f16_half_to_f32(qring[(slot_r * FR + f) * 16 + g], hf);
+              shi[f] = q8::f16_half_to_f32(qring[(slot_r * FR + f) * 16 + 8 + g], hf);
+              clo[f][0] = hf ? alo.z : alo.x;
+              clo[f][1] = hf ? alo.w : alo.y;
+              chi[f][0] = hf ? ahi.z : ahi.x;
+              chi[f][1] = hf ? ahi.w : ahi.y;
+            }
+            float part[FR][NP][4];
+  #pragma unroll
+            for (int f = 0; f < FR; ++f)
+  #pragma unroll
+              for (int nt = 0; nt < NP; ++nt) part[f][nt][0] = part[f][nt][1] = part[f][nt][2] = part[f][nt][3] = 0.f;
+  #pragma unroll
+            for (int q = 0; q < 2; ++q) {
+  #pragma unroll
+              for (int f = 0; f < FR; ++f) {
+                uint32_t a0, a2, a1, a3;
+                q8::s8x4_f16x2(clo[f][q], a0, a2);
+                q8::s8x4_f16x2(chi[f][q], a1, a3);
+  #pragma unroll
+                for (int nt = 0; nt < NP; ++nt)
+                  if (nt < ntiles) mma_f16_16816(part[f][nt], a0, a1, a2, a3, bh[hf][nt][2 * q], bh[hf][nt][2 * q + 1]);
+              }
+            }
+  #pragma unroll
+            for (int f = 0; f < FR; ++f)
+  #pragma unroll
+              for (int nt = 0; nt < NP; ++nt) {
+                acc[f][nt][0] = fmaf(slo[f], part[f][nt][0], acc[f][nt][0]);
+                acc[f][nt][1] = fmaf(slo[f], part[f][nt][1], acc[f][nt][1]);
+                acc[f][nt][2] = fmaf(shi[f], part[f][nt][2], acc[f][nt][2]);
+                acc[f][nt][3] = fmaf(shi[f], part[f][nt][3], acc[f][nt][3]);
+              }
+          }
+          slot_r = slot_r + 1 == NS ? 0 : slot_r + 1;
+          issue_next();
+        }
       } else {
       uint32_t bc[NP][KG][4], bn[NP][KG][4];
     #pragma unroll
@@ -498,7 +632,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
               const float gv = acc[fr][nt][h2] * gscale, uv = acc[fr][nt][2 + h2] * gscale;
               const float hv = silu(gv) * uv;
               uint16_t hb;
-              if constexpr (kFp4) {
+              if constexpr (C::kDec) {
                 hb = f2h(hv);   // the down units' f16 operand
                 if ((hb & 0x7c00u) == 0x7c00u) atomicOr(a.status, kStatusRange);
               } else {
@@ -522,7 +656,7 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
         }
       }
     };
-    if constexpr (!kFp4 && NT > 1) {
+    if constexpr (F == kFmtBf16 && NT > 1) {
       // a pass with at most 8 rows left runs the one-tile loop
       if (ct.m - p0 <= 8) run_pass(std::integral_constant<int, 1>{});
       else run_pass(std::integral_constant<int, NT>{});
@@ -540,9 +674,9 @@ __global__ void __launch_bounds__(StreamCfg<kFp4, NT>::kWarps * 32, 1) stream_ge
   cp_async_wait<0>();
 }
 
-template <bool kFp4, int NT>
+template <int F, int NT>
 cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
-  using C = StreamCfg<kFp4, NT>;
+  using C = StreamCfg<F, NT>;
   const long long S = (long long)a.T * a.k;
   const long long max_active = S < a.E ? S : a.E;
   const long long units = max_active * (a.I / (8 * C::FR) + a.H / (16 * C::FR));
@@ -552,7 +686,7 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   if (grid < 1) grid = 1;
   const int smem = C::kWarpBytes * C::kWarps + C::kLutBytes + 16 * a.E +
                    (S <= kPermSmem ? 4 * (int)S : 0);
-  cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<kFp4, NT>,
+  cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<F, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -565,7 +699,7 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<kFp4, NT>, a);
+  return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<F, NT>, a);
 }
 
 // y = f16(x), eight values per thread; a value that rounds beyond the f16
@@ -611,13 +745,18 @@ cudaError_t launch_stream_gemm(const StreamGemmArgs& args, cudaStream_t stream, 
   // the experts average 24 rows or more (measured: 16-row passes faster at
   // 16 rows per expert, 32-row passes at 32 and 64)
   const bool two = a.T > 8;
+  const long long S = (long long)a.T * a.k;
+  const long long avg = S / (S < a.E ? S : a.E);
+  const bool four = a.T > 16 && avg >= 24;
   if (a.gu_codes != nullptr) {
-    const long long S = (long long)a.T * a.k;
-    const long long avg = S / (S < a.E ? S : a.E);
-    if (a.T > 16 && avg >= 24) return launch_variant<true, 4>(a, stream);
-    return two ? launch_variant<true, 2>(a, stream) : launch_variant<true, 1>(a, stream);
+    if (four) return launch_variant<kFmtFp4, 4>(a, stream);
+    return two ? launch_variant<kFmtFp4, 2>(a, stream) : launch_variant<kFmtFp4, 1>(a, stream);
   }
-  return two ? launch_variant<false, 2>(a, stream) : launch_variant<false, 1>(a, stream);
+  if (a.gu_q8 != nullptr) {
+    if (four) return launch_variant<kFmtQ8, 4>(a, stream);
+    return two ? launch_variant<kFmtQ8, 2>(a, stream) : launch_variant<kFmtQ8, 1>(a, stream);
+  }
+  return two ? launch_variant<kFmtBf16, 2>(a, stream) : launch_variant<kFmtBf16, 1>(a, stream);
 }
 
 }  // namespace moe

@@ -286,6 +286,49 @@ int moe_nvfp4_quantize(const uint16_t *a, int R, int K, float global, uint8_t *c
                        void *stream);
 
 /*
+ * Int8 block expert weights (W8A16): the "fused int8" expert types of the
+ * pages' serving stack (page "第 9 章 prefill：最大的瓶颈", sec. 9.9), taken as
+ * the plain int8 block format -- one signed 8-bit code per element and one
+ * fp16 scale per 32 consecutive elements along K:
+ *   W[e,r,k] = code[e,r,k] * scale[e,r,k/32]
+ *   gu_codes  [E, 2I, H] int8     gu_scales [E, 2I, H/32] fp16 bit patterns
+ *   dn_codes  [E, H, I] int8      dn_scales [E, H, I/32]  fp16 bit patterns
+ * Rows [0, I) of the gate/up tensor are the gate projection, rows [I, 2I) the
+ * up projection.  All pointers are device pointers, 16-byte aligned.
+ * The expert products run on f16 operands as on the NVFP4 path (codes exact
+ * in f16; x and h converted to f16, out-of-range values recorded as
+ * MOE_ERR_DEVICE); every expert, whatever its row count, takes the
+ * weight-streaming kernel.
+ */
+typedef struct {
+  const int8_t *gu_codes;
+  const uint16_t *gu_scales;
+  const int8_t *dn_codes;
+  const uint16_t *dn_scales;
+} moe_int8_weights;
+
+/*
+ * The layer forward with int8 block expert weights: arguments and results as
+ * moe_forward, with `w` (host struct holding device pointers) in place of the
+ * bf16 / NVFP4 weights; workspace of moe_workspace_size(T, H, E, I, top_k)
+ * bytes.
+ */
+int moe_forward_int8(const uint16_t *x, const uint16_t *gate_w, const float *bias,
+                     const moe_int8_weights *w, int T, int H, int E, int I, int top_k, uint16_t *out,
+                     int32_t *topk_idx, float *topk_w, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
+ * moe_forward_int8 with the timing hooks of moe_forward_profiled (same six
+ * events; [4] follows [3] directly: no tensor-core stage).
+ */
+int moe_forward_int8_profiled(const uint16_t *x, const uint16_t *gate_w, const float *bias,
+                              const moe_int8_weights *w, int T, int H, int E, int I, int top_k,
+                              uint16_t *out, int32_t *topk_idx, float *topk_w, void *workspace,
+                              size_t workspace_bytes, void *stream, void *const *events,
+                              int32_t *kernels_launched);
+
+/*
  * TEST ONLY.  With polls > 0, every moe_forward launched afterwards in this
  * process makes the weight-streaming kernel's bounded waits (a down-
  * projection unit waiting for its expert's gate/up units) aim at a count

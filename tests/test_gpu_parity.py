@@ -29,8 +29,8 @@ def _built():
     moe.lib()
 
 
-def _small(T, H, E, k, I, bias=None, seed=0, nvfp4=False):
-    return moe_inputs.make_inputs(dict(T=T, H=H, E=E, top_k=k, I=I, bias=bias, nvfp4=nvfp4), seed=seed,
+def _small(T, H, E, k, I, bias=None, seed=0, nvfp4=False, q8=False):
+    return moe_inputs.make_inputs(dict(T=T, H=H, E=E, top_k=k, I=I, bias=bias, nvfp4=nvfp4, q8=q8), seed=seed,
                                   device="cuda")
 
 
@@ -53,6 +53,15 @@ SMALL_CASES = {
     # never takes the tensor-core kernels; bf16 with H % 256 != 0 neither)
     "nvfp4_global_perm": dict(T=640, H=256, E=16, k=8, I=128, nvfp4=True),
     "stream_global_perm": dict(T=600, H=384, E=16, k=8, I=128),
+    # int8 block weights: one 8-row tile per pass (T <= 8), two, four (groups
+    # averaging >= 24 rows) with several passes, a 1280-wide H, a batch large
+    # enough for the tensor-core kernels on bf16 (int8 stays on the streaming
+    # kernel) and the slot permutation in global memory
+    "int8_t4": dict(T=4, H=256, E=8, k=2, I=128, q8=True),
+    "int8_t24": dict(T=24, H=256, E=8, k=2, I=128, q8=True),
+    "int8_passes": dict(T=300, H=256, E=4, k=2, I=256, q8=True),
+    "int8_h1280": dict(T=80, H=1280, E=8, k=2, I=256, q8=True, bias="zipf"),
+    "int8_global_perm": dict(T=640, H=256, E=16, k=8, I=128, q8=True),
     # groups of >= 64 rows run on the tcgen05 kernels
     "tc_all": dict(T=512, H=256, E=8, k=2, I=128),
     "tc_mixed": dict(T=300, H=512, E=16, k=2, I=256, bias="zipf"),
@@ -68,7 +77,8 @@ SMALL_CASES = {
 @pytest.mark.parametrize("name", list(SMALL_CASES))
 def test_forward_small(name):
     c = SMALL_CASES[name]
-    inp = _small(c["T"], c["H"], c["E"], c["k"], c["I"], bias=c.get("bias"), nvfp4=c.get("nvfp4", False))
+    inp = _small(c["T"], c["H"], c["E"], c["k"], c["I"], bias=c.get("bias"), nvfp4=c.get("nvfp4", False),
+                 q8=c.get("q8", False))
     out, idx, w, ws = gh.run_forward(inp)
     assert moe.read_status(ws) == 0
     if name.startswith("tc_"):
@@ -230,6 +240,28 @@ def test_nvfp4_workload_sampled():
     orc = oracle.forward_from_inputs(inp, tokens=rows)
     gh.check_routing(inp, idx, w, orc)
     gh.check_output(inp, out, orc, rows=rows)
+
+
+def test_int8_workload_sampled():
+    inp = moe_inputs.make_inputs("int8_256", device="cuda")
+    out, idx, w, ws = gh.run_forward(inp)
+    assert moe.read_status(ws) == 0
+    r = oracle.route_from_inputs(inp)
+    rows = sorted(set(range(0, inp.T, 8)) | {inp.T - 1} | set(_edge_rows(r, inp.top_k)))
+    orc = oracle.forward_from_inputs(inp, tokens=rows)
+    gh.check_routing(inp, idx, w, orc)
+    gh.check_output(inp, out, orc, rows=rows)
+
+
+def test_int8_activation_beyond_f16_is_flagged():
+    """The int8 expert path multiplies in f16 too: an activation beyond the
+    f16 range is reported as MOE_ERR_DEVICE."""
+    inp = _small(24, 256, 8, 2, 128, q8=True)
+    x = inp.x.clone()
+    x[3, 5] = 1.0e5
+    inp.x = x
+    _, _, _, ws = gh.run_forward(inp)
+    assert moe.read_status(ws) == -5   # MOE_ERR_DEVICE
 
 
 def _edge_rows(r, k, n_small=4):
