@@ -88,6 +88,10 @@ struct StreamGemmArgs {
 };
 // gate/up then down of the small groups, one persistent launch
 cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int* launches);
+// the same for NVFP4 / int8 weights with a TMA producer warp (stream_dec.cu);
+// stream_dec_supported: decoded weights and H, I multiples of 256
+bool stream_dec_supported(const StreamGemmArgs& a);
+cudaError_t launch_stream_dec(const StreamGemmArgs& a, cudaStream_t stream);
 // y = f16(x) for n bf16 values (n % 8 == 0); sets kStatusRange in *status
 // when a value rounds beyond the f16 range
 cudaError_t launch_to_f16(const uint16_t* x, size_t n, uint16_t* y, int* status, cudaStream_t stream,

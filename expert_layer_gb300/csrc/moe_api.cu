@@ -7,7 +7,7 @@
 
 #include <atomic>
 
-#include "../../include/moe.h"
+#include "moe.h"
 #include "common.cuh"
 #include "kernels.h"
 

@@ -26,7 +26,7 @@
 // array and give undefined results.
 #include <mutex>
 
-#include "../../include/moe.h"
+#include "moe.h"
 #include "common.cuh"
 #include "kernels.h"
 

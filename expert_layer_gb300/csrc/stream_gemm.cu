@@ -56,50 +56,14 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "nvfp4.cuh"
+#include "stream_common.cuh"
 
 namespace moe {
 
 namespace {
 
+using namespace stream;
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-namespace q8 {
-// Four int8 codes (byte i = element i) to two f16x2 pairs, exact: each byte,
-// offset by 128 with the sign-bit flip, becomes the mantissa of the f16
-// 1024 + (q + 128) (0x64 in the high byte), and 1152 is subtracted.
-__device__ __forceinline__ void s8x4_f16x2(uint32_t w, uint32_t& p01, uint32_t& p23) {
-  const uint32_t u = w ^ 0x80808080u;
-  const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
-  const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(p01) : "r"(lo), "r"(0x64806480u));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(p23) : "r"(hi), "r"(0x64806480u));
-}
-// The f16 in the low (hf = 0) or high half of v, as fp32 (exact).
-__device__ __forceinline__ float f16_half_to_f32(uint32_t v, int hf) {
-  float f;
-  const uint32_t h = hf ? v >> 16 : v & 0xffffu;
-  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.f32.f16 %0, t;\n}" : "=f"(f) : "r"(h));
-  return f;
-}
-}  // namespace q8
-
-// Weight formats of the streaming kernel.
-enum : int { kFmtBf16 = 0, kFmtFp4 = 1, kFmtQ8 = 2 };
 
 // Pipeline shape per variant (NT = 8-row token tiles per pass).  A unit is
 // FR fragments of 16 weight rows.  NVFP4 and int8 units are two or four
@@ -128,57 +92,6 @@ struct StreamCfg {
   static constexpr int kWarpBytes = kWBytes + kSBytes;
   static constexpr int kLutBytes = 0;
 };
-
-// Bounded waits: polls before a wait gives up (and the kernel records
-// kStatusTimeout); with the sleep between polls this is well over a second.
-// (StreamGemmArgs.spin_limit overrides it in tests.)
-constexpr int kSpinLimit = 1 << 22;
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Queue positions [0, Ug) are gate/up units, [Ug, Q) down units, each in
-// active-list order (unit = 16 weight rows of one expert over all of K).
-struct Queue {
-  int UPEg, UPEd, Ug, Q, nkb_g, nkb_d;
-};
-
-// One unit of a warp, taken in passes of 8*NT of the expert's token rows
-// (pass p covers rows 8NTp..).
-struct Task {
-  int q;         // queue position, < 0 when the warp has no more work
-  bool down;
-  int slot, e, blk, m, off, pass, npass, nkb, ngroups;
-};
-
-// Rows of the routed-slot permutation kept in shared memory (else read from
-// global memory).
-constexpr int kPermSmem = 4096;
-
-template <int KG, int NT>
-__device__ __forceinline__ void task_load(Task& t, const int4* smeta, const Queue& qs, int q) {
-  if (q < 0 || q >= qs.Q) { t.q = -1; return; }
-  t.q = q;
-  t.down = q >= qs.Ug;
-  const int r = t.down ? q - qs.Ug : q;
-  const int upe = t.down ? qs.UPEd : qs.UPEg;
-  t.slot = r / upe;
-  t.blk = r - t.slot * upe;
-  const int4 md = smeta[t.slot];   // expert, rows, first grouped row
-  t.e = md.x;
-  t.m = md.y;
-  t.off = md.z;
-  t.pass = 0;
-  t.npass = (t.m + 8 * NT - 1) / (8 * NT);
-  t.nkb = t.down ? qs.nkb_d : qs.nkb_g;
-  t.ngroups = (t.nkb + KG - 1) / KG;
-}
 
 // B (token rows) of one K group for this thread (bf16 weights): row g of
 // the pass, k = 8c..8c+7 of each 32-wide block.  Down reads h, written
@@ -417,7 +330,10 @@ __global__ void __launch_bounds__(StreamCfg<F, NT>::kWarps * 32, 1) stream_gemm_
             ew[nt][h2] = a.topk_w[ef[nt][h2]];
           }
         }
-      const int ntiles = min(NP, (ct.m - p0 + 7) / 8);
+      // tiles of the pass that hold rows: bf16 and int8 passes run with NP =
+      // that count (the caller's dispatch); NVFP4 keeps one NP = NT copy of
+      // its long decode loop and skips the empty tiles' mma
+      const int ntiles = kFp4 ? min(NP, (ct.m - p0 + 7) / 8) : NP;
       float acc[FR][NP][4];
   #pragma unroll
       for (int f = 0; f < FR; ++f)
@@ -656,12 +572,23 @@ __global__ void __launch_bounds__(StreamCfg<F, NT>::kWarps * 32, 1) stream_gemm_
         }
       }
     };
-    if constexpr (F == kFmtBf16 && NT > 1) {
-      // a pass with at most 8 rows left runs the one-tile loop
-      if (ct.m - p0 <= 8) run_pass(std::integral_constant<int, 1>{});
-      else run_pass(std::integral_constant<int, NT>{});
-    } else {
+    // bf16 and int8 passes run with a compile-time number of token tiles
+    // equal to the tiles that hold rows, so no mma sits behind a per-tile
+    // branch (measured: int8_256 stream stage 336 -> 319 us); NVFP4 is
+    // faster with one copy of its decode loop (205 us against 224 us with
+    // per-count copies and 223 us with NT tiles always)
+    const int tiles = min(NT, (ct.m - p0 + 7) / 8);
+    if constexpr (NT == 1 || kFp4) {
       run_pass(std::integral_constant<int, NT>{});
+    } else if constexpr (NT == 2) {
+      if (tiles == 2) run_pass(std::integral_constant<int, 2>{});
+      else run_pass(std::integral_constant<int, 1>{});
+    } else {
+      static_assert(NT == 4, "token tiles per pass: 1, 2 or 4");
+      if (tiles == 4) run_pass(std::integral_constant<int, 4>{});
+      else if (tiles == 3) run_pass(std::integral_constant<int, 3>{});
+      else if (tiles == 2) run_pass(std::integral_constant<int, 2>{});
+      else run_pass(std::integral_constant<int, 1>{});
     }
     if (++ct.pass < ct.npass) continue;
     if (!ct.down) {
@@ -744,6 +671,8 @@ cudaError_t launch_stream_gemm(const StreamGemmArgs& args, cudaStream_t stream, 
   // per pass for T <= 8, two above; NVFP4 takes four (32-row passes) once
   // the experts average 24 rows or more (measured: 16-row passes faster at
   // 16 rows per expert, 32-row passes at 32 and 64)
+  // NVFP4 and int8 weights with 256-multiple H and I: the TMA-fed kernel
+  if (stream_dec_supported(a)) return launch_stream_dec(a, stream);
   const bool two = a.T > 8;
   const long long S = (long long)a.T * a.k;
   const long long avg = S / (S < a.E ? S : a.E);

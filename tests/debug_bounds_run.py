@@ -21,6 +21,9 @@ CASES = [
     dict(T=300, H=512, E=16, top_k=2, I=256, bias="zipf", nvfp4=False),         # streaming + tensor cores
     dict(T=1024, H=256, E=512, top_k=8, I=128, bias="zipf", nvfp4=False),       # prefill-sized grouping
     dict(T=24, H=256, E=8, top_k=2, I=128, bias=None, nvfp4=True),              # NVFP4 weights
+    dict(T=640, H=256, E=16, top_k=8, I=256, bias=None, nvfp4=True),            # NVFP4, TMA-fed kernel
+    dict(T=40, H=256, E=8, top_k=2, I=256, bias=None, q8=True),                 # int8, TMA-fed kernel
+    dict(T=24, H=256, E=8, top_k=2, I=128, bias=None, q8=True),                 # int8, cp.async kernel
     dict(T=300, H=512, E=4, top_k=2, I=256, bias="zipf", nvfp4=True, w4a4=True),  # W4A4
 ]
 

@@ -36,11 +36,13 @@ def _built():
     moe.lib()
 
 
-def test_forced_wait_timeout_is_reported_and_next_call_is_clean():
-    # decode-sized batch: every group on the weight-streaming kernel, whose
-    # down units wait for their expert's gate/up units
-    inp = moe_inputs.make_inputs(dict(T=8, H=256, E=16, top_k=4, I=128, bias=None, nvfp4=False), seed=3,
-                                 device="cuda")
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4_tma"])
+def test_forced_wait_timeout_is_reported_and_next_call_is_clean(fmt):
+    # decode-sized batch: every group on a weight-streaming kernel, whose
+    # down units wait for their expert's gate/up units (bf16: the cp.async
+    # kernel; NVFP4 with H, I multiples of 256: the TMA-fed kernel)
+    shape = dict(T=8, H=256, E=16, top_k=4, I=128) if fmt == "bf16" else dict(T=8, H=256, E=16, top_k=4, I=256)
+    inp = moe_inputs.make_inputs(dict(shape, bias=None, nvfp4=fmt != "bf16"), seed=3, device="cuda")
     lib = moe.lib()
     assert lib.moe_debug_force_wait_timeout(2000) == 0
     try:

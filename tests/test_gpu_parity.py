@@ -62,6 +62,14 @@ SMALL_CASES = {
     "int8_passes": dict(T=300, H=256, E=4, k=2, I=256, q8=True),
     "int8_h1280": dict(T=80, H=1280, E=8, k=2, I=256, q8=True, bias="zipf"),
     "int8_global_perm": dict(T=640, H=256, E=16, k=8, I=128, q8=True),
+    # H and I multiples of 256 take the TMA-fed decoded-weight kernel: one,
+    # two and four token tiles per pass, and the slot permutation in global
+    # memory (T*k > 4096)
+    "nvfp4_tma_t4": dict(T=4, H=256, E=8, k=2, I=256, nvfp4=True),
+    "nvfp4_tma_global_perm": dict(T=640, H=512, E=16, k=8, I=256, nvfp4=True, bias="zipf"),
+    "int8_tma_t4": dict(T=4, H=512, E=8, k=2, I=256, q8=True),
+    "int8_tma_t40": dict(T=40, H=256, E=8, k=2, I=512, q8=True),
+    "int8_tma_global_perm": dict(T=640, H=256, E=16, k=8, I=256, q8=True),
     # groups of >= 64 rows run on the tcgen05 kernels
     "tc_all": dict(T=512, H=256, E=8, k=2, I=128),
     "tc_mixed": dict(T=300, H=512, E=16, k=2, I=256, bias="zipf"),
