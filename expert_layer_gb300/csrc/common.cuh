@@ -148,6 +148,20 @@ __device__ __forceinline__ uint16_t f2h(float f) {
   return h;
 }
 
+// Eight bf16 (a 16-byte vector) to eight f16, round to nearest even; `bad`
+// is set when a value rounds beyond the f16 range (or is not finite).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& bad) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint16_t lo = f2h(__uint_as_float(w[j] << 16)), hi = f2h(__uint_as_float(w[j] & 0xffff0000u));
+    bad |= ((lo & 0x7c00u) == 0x7c00u) | ((hi & 0x7c00u) == 0x7c00u);
+    o[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -32,11 +32,14 @@ DebugWaits debug_waits();
 cudaError_t launch_zero(void* ws, size_t bytes, cudaStream_t stream);
 
 // router.cu -- logits, certified top-k, renormalised weights; with `group`
-// (only where route_can_group) also the grouping, in the same launch
+// (only where route_can_group) also the grouping, in the same launch; with
+// x16 also x converted to f16 ([T, H], for the decoded-weight expert
+// kernels; a value beyond the f16 range sets kStatusRange)
 bool route_can_group(int T, int E, int k);
 cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
                          int E, int k, int32_t* idx, float* w, void* ws, const WsLayout& L,
-                         cudaStream_t stream, int* launches, const GroupOut* group);
+                         cudaStream_t stream, int* launches, const GroupOut* group,
+                         uint16_t* x16 = nullptr);
 
 // permute.cu -- histogram, exclusive scan, stable permutation, active list
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* counts,
@@ -92,11 +95,6 @@ cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream, int
 // stream_dec_supported: decoded weights and H, I multiples of 256
 bool stream_dec_supported(const StreamGemmArgs& a);
 cudaError_t launch_stream_dec(const StreamGemmArgs& a, cudaStream_t stream);
-// y = f16(x) for n bf16 values (n % 8 == 0); sets kStatusRange in *status
-// when a value rounds beyond the f16 range
-cudaError_t launch_to_f16(const uint16_t* x, size_t n, uint16_t* y, int* status, cudaStream_t stream,
-                          int* launches);
-
 // tc_gemm.cu -- tcgen05/TMEM grouped GEMMs for experts with many rows (bf16 weights)
 struct TcLaunch {
   int T, H, E, I, k;

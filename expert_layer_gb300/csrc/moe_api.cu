@@ -226,6 +226,9 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   const int large_threshold = tc_all ? 1 : use_tc ? large : INT_MAX;
   // Small batches fuse the grouping into the router.
   const bool fuse = !use_tc && route_can_group(T, E, top_k);
+  // the NVFP4 and int8 expert kernels multiply in f16: the router writes x
+  // converted to f16 while it reads x for the logits
+  uint16_t* x16 = (nvfp4 || q8) ? ws_ptr<uint16_t>(workspace, L.x16) : nullptr;
 
   MOE_TRY_CUDA(mark(0));
   MOE_TRY_CUDA(launch_zero(workspace, zeroed_prefix(L), s));
@@ -233,12 +236,12 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   if (fuse) {
     GroupOut go{counts, offsets, perm, inv_perm, ws_ptr<int32_t>(workspace, L.active),
                 ws_ptr<int32_t>(workspace, L.tiles), large_threshold, kTcRows, nullptr, 0};
-    MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches, &go));
+    MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches, &go, x16));
     MOE_TRY_CUDA(mark(1));
     MOE_TRY_CUDA(mark(2));
   } else {
     MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches,
-                              nullptr));
+                              nullptr, x16));
     MOE_TRY_CUDA(mark(1));
     MOE_TRY_CUDA(launch_permute(idx, T, E, top_k, counts, offsets, perm, inv_perm, workspace, L,
                                 large_threshold, kTcRows, s, launches));
@@ -279,12 +282,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   tc.h = a.h; tc.partial = a.partial; tc.partial_f32 = L.partial_f32;
   tc.status = &hdr->status; tc.num_sms = num_sms;
 
-  if (nvfp4 || q8) {
-    // the NVFP4 and int8 expert kernels multiply in f16: x converted once per call
-    a.x16 = ws_ptr<uint16_t>(workspace, L.x16);
-    MOE_TRY_CUDA(launch_to_f16(x, (size_t)T * H, ws_ptr<uint16_t>(workspace, L.x16), &hdr->status, s,
-                               launches));
-  }
+  a.x16 = x16;
   if (!tc_all) MOE_TRY_CUDA(launch_stream_gemm(a, s, launches));
   MOE_TRY_CUDA(mark(3));
   if (use_tc) {

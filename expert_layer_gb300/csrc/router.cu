@@ -485,7 +485,7 @@ __device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float c) {
 // chunk's tokens or past H).  All loads are issued before the stores.
 template <int kTT>
 __device__ __forceinline__ void stage_tokens(const uint16_t* __restrict__ x, int t0, int nt, int H,
-                                             int hb, uint16_t* xs) {
+                                             int hb, uint16_t* xs, uint16_t* __restrict__ x16, int* status) {
   constexpr int kRowVecs = kXCols / 8;
   constexpr int kPer = kTT * kRowVecs / (kSmallWarps * 32);
   static_assert(kTT * kRowVecs % (kSmallWarps * 32) == 0, "whole vectors per thread");
@@ -499,6 +499,17 @@ __device__ __forceinline__ void stage_tokens(const uint16_t* __restrict__ x, int
   }
 #pragma unroll
   for (int i = 0; i < kPer; ++i) reinterpret_cast<uint4*>(xs)[threadIdx.x + i * kSmallWarps * 32] = v[i];
+  if (x16) {   // the f16 copy of the token rows (decoded-weight expert kernels)
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int q = threadIdx.x + i * kSmallWarps * 32;
+      const int tt = q / kRowVecs, h = hb + (q % kRowVecs) * 8;
+      if (tt < nt && h < H)
+        *reinterpret_cast<uint4*>(x16 + (size_t)(t0 + tt) * H + h) = bf16x8_to_f16x8(v[i], bad);
+    }
+    if (bad) atomicOr(status, kStatusRange);
+  }
 }
 
 template <int kTT, bool kGroup>
@@ -506,7 +517,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
     int T, int H, int E, int k, float gamma, float* __restrict__ logits,
     float* __restrict__ wnorm, float* __restrict__ xnorm, double* __restrict__ l64,
-    int* __restrict__ cnt, int32_t* __restrict__ idx, float* __restrict__ w, void* ws, GroupOut go) {
+    int* __restrict__ cnt, int32_t* __restrict__ idx, float* __restrict__ w, void* ws, GroupOut go,
+    uint16_t* __restrict__ x16) {
   using Cfg = SmallCfg<kTT>;
   constexpr int kEPW = Cfg::kEPW;
   extern __shared__ __align__(16) int dsm[];
@@ -545,7 +557,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
       }
     if constexpr (Cfg::kStaged) {
       if (hb > 0) __syncthreads();   // every warp is done with the previous block
-      stage_tokens<kTT>(x, t0, nt, H, hb, xs);
+      // the y = 0 CTAs also write the chunk's f16 token rows (when asked)
+      stage_tokens<kTT>(x, t0, nt, H, hb, xs, blockIdx.y == 0 ? x16 : nullptr, &hdr->status);
       __syncthreads();
     }
 #pragma unroll
@@ -592,6 +605,15 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
         const int h = hb + lane * 8 + 256 * v;
         xv[v] = (nt > 0 && h < H) ? *reinterpret_cast<const uint4*>(x + (size_t)t0 * H + h)
                                   : make_uint4(0, 0, 0, 0);
+      }
+      if (x16 && blockIdx.y == 0 && warp == 0 && nt > 0) {   // the token's f16 row (when asked)
+        bool bad = false;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const int h = hb + lane * 8 + 256 * v;
+          if (h < H) *reinterpret_cast<uint4*>(x16 + (size_t)t0 * H + h) = bf16x8_to_f16x8(xv[v], bad);
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&hdr->status, kStatusRange);
       }
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
@@ -738,7 +760,8 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 
 __global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
-    int T, int H, int E, float* __restrict__ logits, float* __restrict__ xnorm) {
+    int T, int H, int E, float* __restrict__ logits, float* __restrict__ xnorm, uint16_t* __restrict__ x16,
+    int* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // [pair][buf]: x tile [kTileK][kTileT] then w tile [kTileK][kTileE], fp32
   float* tiles = reinterpret_cast<float*>(smem_raw);
@@ -765,6 +788,17 @@ __global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
       const int row = v % kTileT, col = (v / kTileT) * 8;
       const int t = t0 + row;
       rx[i] = (t < T) ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + col) : make_uint4(0, 0, 0, 0);
+    }
+    if (x16) {   // the f16 copy of the token rows (each vector is loaded once per CTA)
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int v = ptid + 64 * i;
+        const int row = v % kTileT, col = (v / kTileT) * 8;
+        const int t = t0 + row;
+        if (t < T) *reinterpret_cast<uint4*>(x16 + (size_t)t * H + k0 + col) = bf16x8_to_f16x8(rx[i], bad);
+      }
+      if (bad) atomicOr(status, kStatusRange);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -964,7 +998,7 @@ bool route_can_group(int T, int E, int k) {
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
                          int E, int k, int32_t* idx, float* w, void* ws, const WsLayout& L,
-                         cudaStream_t stream, int* launches, const GroupOut* group) {
+                         cudaStream_t stream, int* launches, const GroupOut* group, uint16_t* x16) {
   float* wnorm = ws_ptr<float>(ws, L.wnorm);
   double* l64 = ws_ptr<double>(ws, L.logits64);
   const bool tiled = T >= 2048 && E <= kTileE;
@@ -977,8 +1011,8 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
     cudaError_t err = cudaFuncSetAttribute(router_tile_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    router_tile_kernel<<<(T + kTileT - 1) / kTileT, kTileThreads, smem, stream>>>(x, gate_w, bias, T, H, E,
-                                                                         logits, xnorm);
+    router_tile_kernel<<<(T + kTileT - 1) / kTileT, kTileThreads, smem, stream>>>(
+        x, gate_w, bias, T, H, E, logits, xnorm, x16, &reinterpret_cast<WsHeader*>(ws)->status);
     const size_t smem2 = sizeof(WarpScratch) * 8;
     err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem2);
@@ -1015,7 +1049,7 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, x, gate_w, bias, T, H, E, k, gamma, logits, wnorm, xnorm,
-                              l64, cnt, idx, w, ws, go);
+                              l64, cnt, idx, w, ws, go, x16);
   };
   if (grp) {
     if (tt == 1) return run(router_small_kernel<1, true>);

@@ -38,7 +38,7 @@
 // value has at most 6 significant bits and lies in [2^-10, 2688]); the
 // per-expert fp32 global scale multiplies the fp32 accumulator in the
 // epilogue.  The token rows are x converted to f16 beforehand
-// (launch_to_f16) and h, which the gate/up epilogue writes in f16 on this
+// (by the router) and h, which the gate/up epilogue writes in f16 on this
 // path: exact for activations of magnitude 2^-14 .. 65504, below that
 // rounded to the f16 subnormal grid (absolute error <= 2^-25), above it
 // flagged (kStatusRange).
@@ -629,37 +629,7 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, stream_gemm_kernel<F, NT>, a);
 }
 
-// y = f16(x), eight values per thread; a value that rounds beyond the f16
-// range (or is not finite) sets kStatusRange, once per warp.
-__global__ void __launch_bounds__(256) to_f16_kernel(const uint16_t* __restrict__ x, size_t n8,
-                                                     uint16_t* __restrict__ y, int* status) {
-  bool bad = false;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint16_t lo = f2h(bf16lo(w[j])), hi = f2h(bf16hi(w[j]));
-      bad |= ((lo & 0x7c00u) == 0x7c00u) | ((hi & 0x7c00u) == 0x7c00u);
-      o[j] = (uint32_t)lo | ((uint32_t)hi << 16);
-    }
-    reinterpret_cast<uint4*>(y)[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusRange);
-}
-
 }  // namespace
-
-cudaError_t launch_to_f16(const uint16_t* x, size_t n, uint16_t* y, int* status, cudaStream_t stream,
-                          int* launches) {
-  if (launches) *launches += 1;
-  const size_t n8 = n / 8;
-  if (n8 == 0) return cudaSuccess;
-  const size_t blocks = (n8 + 255) / 256;
-  to_f16_kernel<<<(unsigned)(blocks < 1024 ? blocks : 1024), 256, 0, stream>>>(x, n8, y, status);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_stream_gemm(const StreamGemmArgs& args, cudaStream_t stream, int* launches) {
   if (launches) *launches += 1;
