@@ -39,15 +39,14 @@ struct WsHeader {
   int num_large;          // active experts served by the tensor-core path
   int router_flagged;     // tokens whose ranking needed fp64 logits
   int router_fallback;    // tokens that needed fp64 logits for every expert
-  int tokens_done;        // tokens whose top-k is final (fused grouping)
-  int pad[58];
+  int pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte slot");
 
 // Offsets (bytes) of every workspace region for one shape.
 struct WsLayout {
   size_t hdr, sched, cnt, xnorm, wnorm, logits, logits64, idx, w, counts, offsets, active, tiles, blk_cnt,
-      blk_base, lrank, perm, inv_perm, h, partial, xp, x16, total;
+      blk_base, lrank, perm, inv_perm, h, partial, xp, x16, acnt, total;
   int nblk;               // 512-slot blocks of the grouping kernels
   bool partial_f32;       // fp32 partials (else bf16)
 };
@@ -67,6 +66,7 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
   L.hdr = take(sizeof(WsHeader));
   L.sched = take(sizeof(int) * (E + 1));   // expert-GEMM queue counter, then per-slot counters
   L.cnt = take(sizeof(int) * T);
+  L.acnt = take(sizeof(int) * E);          // per-expert slot counters (ranks by arrival)
   L.xnorm = take(sizeof(float) * T);
   L.wnorm = take(sizeof(float) * E);
   L.logits = take(sizeof(float) * T * E);
@@ -96,8 +96,8 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
 }
 
 // Bytes at the start of the workspace that must be zero when a call starts
-// (header, scheduling counters and per-chunk counters); every entry point
-// clears them on its stream.
+// (header, scheduling counters, per-chunk and per-expert counters); every
+// entry point clears them on its stream.
 inline size_t zeroed_prefix(const WsLayout& L) { return L.xnorm; }
 
 template <typename T>

@@ -12,11 +12,13 @@
 namespace moe {
 
 // Outputs of the grouping when it runs fused into the small-batch router.
+// Grouping fused into the small-batch router: each routed slot f takes its
+// rank within its expert's group, rank[f] = atomicAdd(&acnt[idx[f]], 1)
+// (arrival order; acnt starts at zero).  The expert kernel builds offsets,
+// active list and permutation from acnt, idx and rank (self_group below).
 struct GroupOut {
-  int32_t *counts, *offsets, *perm, *inv_perm, *active, *tiles;
-  int large_threshold, tile_rows;
-  int* zero;     // int region cleared by the grouping CTA (may be null)
-  int nzero;
+  int* acnt;     // [E] slot counts, zero at launch
+  int* rank;     // [S] out
 };
 
 // moe_api.cu -- test-only settings of the bounded device waits (0, 0 in
@@ -83,6 +85,21 @@ struct StreamGemmArgs {
   int* dep;
   int* status;               // workspace status word (kStatusTimeout)
   int num_sms;
+  // self-grouping (small batches: the router leaves arrival ranks instead of
+  // a grouping): every CTA builds the active list, offsets and permutation
+  // from acnt / idx / rank in its prologue, and CTA 0 also writes them to
+  // counts / offsets / active / perm / inv_perm and the header (diagnostics)
+  bool self_group;
+  const int* acnt;           // [E]
+  const int32_t* idx;        // [S] expert of each routed slot
+  const int* rank;           // [S]
+  int32_t* counts_out;
+  int32_t* offsets_out;      // [E + 1]
+  int32_t* active_out;
+  int32_t* perm_out;
+  int32_t* inv_perm_out;
+  int* num_active_out;
+  int* num_large_out;
   // bounded waits: polls before a down unit's wait gives up; with
   // wait_extra > 0 the wait aims at a count that no unit reaches (test-only
   // forced timeout, see moe_debug_force_wait_timeout)

@@ -234,8 +234,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   MOE_TRY_CUDA(launch_zero(workspace, zeroed_prefix(L), s));
   if (launches) *launches += 1;
   if (fuse) {
-    GroupOut go{counts, offsets, perm, inv_perm, ws_ptr<int32_t>(workspace, L.active),
-                ws_ptr<int32_t>(workspace, L.tiles), large_threshold, kTcRows, nullptr, 0};
+    GroupOut go{ws_ptr<int>(workspace, L.acnt), ws_ptr<int>(workspace, L.lrank)};
     MOE_TRY_CUDA(launch_route(x, gate_w, bias, T, H, E, top_k, idx, w, workspace, L, s, launches, &go, x16));
     MOE_TRY_CUDA(mark(1));
     MOE_TRY_CUDA(mark(2));
@@ -273,6 +272,16 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   a.dep = a.queue + 1;
   a.status = &hdr->status;
   a.num_sms = num_sms;
+  if (fuse) {
+    // the expert kernel groups the batch itself from the router's ranks
+    a.self_group = true;
+    a.acnt = ws_ptr<int>(workspace, L.acnt);
+    a.idx = idx;
+    a.rank = ws_ptr<int>(workspace, L.lrank);
+    a.counts_out = counts; a.offsets_out = offsets; a.active_out = ws_ptr<int32_t>(workspace, L.active);
+    a.perm_out = perm; a.inv_perm_out = inv_perm;
+    a.num_active_out = &hdr->num_active; a.num_large_out = &hdr->num_large;
+  }
   TcLaunch tc{};
   tc.T = T; tc.H = H; tc.E = E; tc.I = I; tc.k = top_k;
   tc.counts = counts; tc.offsets = offsets; tc.perm = perm; tc.active = a.active;

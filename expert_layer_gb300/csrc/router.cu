@@ -19,7 +19,6 @@
 #include <limits.h>
 
 #include "common.cuh"
-#include "grouping.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -435,8 +434,10 @@ __device__ void select_end(int E, int k, WarpScratch& sc, const double* l64_row,
 // orders each token's experts: one warp per token extracting in rank order
 // (chunks of 4 or 8 tokens, E <= 128), or all threads ranking every
 // (token, expert) by counting (one-token chunks, or E > 128); then one warp
-// per token selects.  With kGroup, the CTA that selects the batch's last
-// tokens then groups all routed slots (grouping.cuh) in the same launch.
+// per token selects.  With kGroup, each selecting CTA then gives every
+// routed slot of its chunk its rank within its expert's group (an atomic
+// per-expert counter, arrival order); the expert kernel builds the grouping
+// from those ranks (no grouping pass and no hand-off between them).
 constexpr int kSmallWarps = 16;
 constexpr int kXCols = 2048;   // token-row columns staged per block
 
@@ -447,18 +448,14 @@ struct SmallCfg {
   static constexpr bool kStaged = kTT >= 4;                // token rows in shared memory
 };
 
-// Shared memory of the small router: grouping scratch (kGroup); for the
-// selecting CTA, the chunk's sort keys [tt][E], logits [tt][E], ||w_e|| [E]
-// and ||x_t|| [tt]; then (staged chunks) the token rows [tt][kXCols] bf16.
-__host__ __device__ inline size_t router_small_group_ints(int E, int S, bool group) {
-  return group ? grouping::single_block_smem_ints(E, S) : 0;
+// Shared memory of the small router: for the selecting CTA, the chunk's
+// sort keys [tt][E], logits [tt][E], ||w_e|| [E] and ||x_t|| [tt]; then
+// (staged chunks) the token rows [tt][kXCols] bf16.
+__host__ __device__ inline size_t router_small_select_bytes(int E, int tt) {
+  return sizeof(uint64_t) * (size_t)tt * E + sizeof(float) * ((size_t)(tt + 1) * E + tt);
 }
-__host__ __device__ inline size_t router_small_select_bytes(int E, int S, int tt, bool group) {
-  return sizeof(int) * router_small_group_ints(E, S, group) + sizeof(uint64_t) * (size_t)tt * E +
-         sizeof(float) * ((size_t)(tt + 1) * E + tt);
-}
-__host__ __device__ inline size_t router_small_smem(int E, int S, int tt, bool group) {
-  const size_t sel = (router_small_select_bytes(E, S, tt, group) + 15) & ~size_t(15);
+__host__ __device__ inline size_t router_small_smem(int E, int tt) {
+  const size_t sel = (router_small_select_bytes(E, tt) + 15) & ~size_t(15);
   return tt >= 4 ? sel + sizeof(uint16_t) * (size_t)tt * kXCols : sel;
 }
 
@@ -524,8 +521,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
   extern __shared__ __align__(16) int dsm[];
   __shared__ WarpScratch scr[kTT];
   __shared__ DotPart s_part[kSmallWarps];
-  __shared__ int s_last, s_group;
-  __shared__ int4 sw[grouping::kWarps];
+  __shared__ int s_last;
   pdl_wait();      // the workspace counters are cleared
   pdl_trigger();   // the expert kernel may become resident; it waits for this grid
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -536,7 +532,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   uint16_t* xs = reinterpret_cast<uint16_t*>(
       reinterpret_cast<unsigned char*>(dsm) +
-      ((router_small_select_bytes(E, T * k, kTT, kGroup) + 15) & ~size_t(15)));
+      ((router_small_select_bytes(E, kTT) + 15) & ~size_t(15)));
   const bool xn_warp = blockIdx.y == 0 && warp < nt;   // this warp writes ||x_{t0+warp}||
   float acc[kEPW][kTT], sq[kEPW], sqx = 0.f;
 #pragma unroll
@@ -656,9 +652,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
   if (!s_last) return;
 
   // ---- last CTA of the chunk: stage logits, ||w_e||, ||x_t|| (one L2 trip)
-  // (the grouping scratch is an even number of ints: the keys are 8-byte aligned)
   const bool by_warp = kTT >= 4 && E <= 128;   // extraction in rank order, one warp per token
-  uint64_t* skey = reinterpret_cast<uint64_t*>(dsm + router_small_group_ints(E, T * k, kGroup));
+  uint64_t* skey = reinterpret_cast<uint64_t*>(dsm);
   float* sl = reinterpret_cast<float*>(skey + (size_t)kTT * E);
   float* swn = sl + (size_t)kTT * E;
   float* sxn = swn + E;
@@ -729,13 +724,14 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
                  w + (size_t)(t0 + warp) * k);
   }
   if constexpr (kGroup) {
-    __syncthreads();   // the selecting warps' idx / w writes, then one release
-    if (threadIdx.x == 0) s_group = atomic_add_acq_rel(&hdr->tokens_done, nt) + nt == T;
-    __syncthreads();
-    if (!s_group) return;
-    grouping::group_single_block(idx, T * k, E, go.large_threshold, go.tile_rows, go.counts,
-                                 go.offsets, go.perm, go.inv_perm, go.active, go.tiles, ws, dsm,
-                                 sw, go.zero, go.nzero);
+    // each routed slot of the chunk takes its rank in its expert's group
+    // (arrival order); the expert kernel builds the grouping from these
+    __syncthreads();   // the selecting warps' idx writes
+    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+      const int f = t0 * k + i;
+      const int e = idx[f];
+      go.rank[f] = (unsigned)e < (unsigned)E ? atomicAdd(&go.acnt[e], 1) : -1;
+    }
   }
 }
 
@@ -993,7 +989,9 @@ __global__ void __launch_bounds__(256) wnorm_kernel(const uint16_t* __restrict__
 }  // namespace
 
 bool route_can_group(int T, int E, int k) {
-  return !(T >= 2048 && E <= 128) && T * k <= grouping::kSingleMaxSlots;
+  // the expert kernels keep a self-grouped batch's permutation in shared
+  // memory: at most 4096 slots
+  return !(T >= 2048 && E <= 128) && T * k <= 4096;
 }
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float* bias, int T, int H,
@@ -1025,7 +1023,7 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
   const float gamma = gamma_bound(H / 32 + 5);
   const bool grp = group != nullptr;
   const int tt = T <= 16 ? 1 : T <= 128 ? 4 : 8;
-  const size_t smem = router_small_smem(E, T * k, tt, grp);
+  const size_t smem = router_small_smem(E, tt);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   const int per_cta = tt >= 4 ? SmallCfg<4>::kExperts : SmallCfg<1>::kExperts;
   const dim3 grid((unsigned)((T + tt - 1) / tt), (unsigned)((E + per_cta - 1) / per_cta));

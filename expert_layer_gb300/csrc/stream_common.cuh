@@ -102,6 +102,88 @@ __device__ __forceinline__ void task_load(Task& t, const int4* smeta, const Queu
   t.ngroups = (t.nkb + KG - 1) / KG;
 }
 
+// The grouping of a small batch from the router's arrival ranks, built by
+// every CTA of an expert kernel in its prologue (called by all threads; S <=
+// kPermSmem).  Warp 0 turns the per-expert counts into offsets (exclusive
+// prefix in expert order) and the active list smeta[0..nact) = (expert,
+// rows, first grouped row), ascending; then every thread places its slots,
+// sperm[offset[e] + rank[f]] = f.  Slots of one expert are thus in arrival
+// order, not slot order: the output does not depend on it (each grouped row
+// is computed on its own, with the same K order).  CTA 0 also writes the
+// grouping to the workspace (counts, offsets, active list, permutation and
+// its inverse, the header's expert counts) for diagnostics.  Returns nact.
+// s_off ([E] ints) and s_nact may alias memory that the caller uses after
+// the call (the final barrier orders every read of them before).
+__device__ int self_group(const StreamGemmArgs& a, int4* smeta, int* sperm, int* s_off, int* s_nact) {
+  const int E = a.E, S = a.T * a.k;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (E + 31) / 32, e0 = lane * per;
+    int sum = 0, na = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = e0 + i;
+      if (e < E) {
+        const int v = a.acnt[e];
+        sum += v;
+        na += v > 0 ? 1 : 0;
+      }
+    }
+    int ps = sum, pa = na;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int qs = __shfl_up_sync(0xffffffffu, ps, o), qa = __shfl_up_sync(0xffffffffu, pa, o);
+      if (lane >= o) { ps += qs; pa += qa; }
+    }
+    int off = ps - sum, act = pa - na;
+    const int total = __shfl_sync(0xffffffffu, ps, 31), nact = __shfl_sync(0xffffffffu, pa, 31);
+    for (int i = 0; i < per; ++i) {
+      const int e = e0 + i;
+      if (e < E) {
+        const int v = a.acnt[e];
+        s_off[e] = off;
+        if (v > 0) smeta[act++] = make_int4(e, v, off, 0);
+        off += v;
+      }
+    }
+    if (lane == 0) {
+      *s_nact = nact;
+      if (total != S) atomicOr(a.status, kStatusBadExpert);
+    }
+  }
+  __syncthreads();
+  for (int f = threadIdx.x; f < S; f += blockDim.x) {
+    const int e = a.idx[f], r = a.rank[f];
+    if ((unsigned)e < (unsigned)E && r >= 0) {
+      const int pos = s_off[e] + r;
+      if ((unsigned)pos < (unsigned)S) sperm[pos] = f;
+      else atomicOr(a.status, kStatusBadExpert);
+    } else {
+      atomicOr(a.status, kStatusBadExpert);
+    }
+  }
+  __syncthreads();
+  const int nact = *s_nact;
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      a.counts_out[e] = a.acnt[e];
+      a.offsets_out[e] = s_off[e];
+    }
+    for (int i = threadIdx.x; i < nact; i += blockDim.x) a.active_out[i] = smeta[i].x;
+    for (int p = threadIdx.x; p < S; p += blockDim.x) {
+      const int f = sperm[p];
+      a.perm_out[p] = f;
+      if ((unsigned)f < (unsigned)S) a.inv_perm_out[f] = p;
+    }
+    if (threadIdx.x == 0) {
+      a.offsets_out[E] = S;
+      *a.num_active_out = nact;
+      *a.num_large_out = 0;
+    }
+  }
+  __syncthreads();
+  return nact;
+}
+
 }  // namespace
 }  // namespace stream
 }  // namespace moe

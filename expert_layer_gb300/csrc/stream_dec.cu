@@ -174,26 +174,33 @@ __global__ void __launch_bounds__(DecCfg<F, NT>::kThreads, 1)
   // combine may start launching
   pdl_wait();
   pdl_trigger();
+  const int S = a.T * a.k;
+  const bool perm_smem = a.self_group || S <= kPermSmem;
+  int nsmall;
+  if (a.self_group) {
+    // small batch: the grouping from the router's arrival ranks, per CTA
+    // (its scratch lives in the weight ring, unused until the first copy)
+    nsmall = self_group(a, smeta, sperm, reinterpret_cast<int*>(smem), reinterpret_cast<int*>(smem) + a.E);
+  } else {
+    nsmall = *a.num_active - (a.num_large ? *a.num_large : 0);
+    for (int i = threadIdx.x; i < nsmall; i += blockDim.x) {
+      int e = a.active[i];
+      if (!bounds_ok((unsigned)e < (unsigned)a.E, a.status)) e = 0;
+      int m = a.counts[e], off = a.offsets[e];
+      if (!bounds_ok(off >= 0 && m >= 0 && off + m <= S, a.status)) m = 0, off = 0;
+      smeta[i] = make_int4(e, m, off, 0);
+    }
+    if (perm_smem)
+      for (int i = threadIdx.x; i < S; i += blockDim.x) sperm[i] = a.perm[i];
+    __syncthreads();
+  }
   Queue qs;
-  const int nsmall = *a.num_active - (a.num_large ? *a.num_large : 0);
   qs.UPEg = a.I / (8 * FR);
   qs.UPEd = a.H / (16 * FR);
   qs.Ug = nsmall * qs.UPEg;
   qs.Q = qs.Ug + nsmall * qs.UPEd;
   qs.nkb_g = a.H / (kFp4 ? 128 : 64);
   qs.nkb_d = a.I / (kFp4 ? 128 : 64);
-  const int S = a.T * a.k;
-  const bool perm_smem = S <= kPermSmem;
-  for (int i = threadIdx.x; i < nsmall; i += blockDim.x) {
-    int e = a.active[i];
-    if (!bounds_ok((unsigned)e < (unsigned)a.E, a.status)) e = 0;
-    int m = a.counts[e], off = a.offsets[e];
-    if (!bounds_ok(off >= 0 && m >= 0 && off + m <= S, a.status)) m = 0, off = 0;
-    smeta[i] = make_int4(e, m, off, 0);
-  }
-  if (perm_smem)
-    for (int i = threadIdx.x; i < S; i += blockDim.x) sperm[i] = a.perm[i];
-  __syncthreads();
   const int* permp = perm_smem ? sperm : a.perm;
 
   if (warp == NW) {
@@ -564,6 +571,7 @@ cudaError_t launch_dec(const StreamGemmArgs& a, cudaStream_t stream) {
   const long long need = (units + C::NW - 1) / C::NW;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
+  // [rings][barriers][fifo][smeta E][sperm S]
   const int smem = C::NW * C::kRingBytes + 2 * C::NW * C::NS * 8 + C::NW * C::kFifo * 4 + 16 * a.E +
                    (S <= kPermSmem ? 4 * (int)S : 0);
   cudaError_t err =

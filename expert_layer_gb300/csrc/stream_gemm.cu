@@ -147,8 +147,29 @@ __global__ void __launch_bounds__(StreamCfg<F, NT>::kWarps * 32, 1) stream_gemm_
   // combine may start launching
   pdl_wait();
   pdl_trigger();
+  const int S = a.T * a.k;
+  const bool perm_smem = a.self_group || S <= kPermSmem;
+  int nsmall;
+  if (a.self_group) {
+    // small batch: the grouping from the router's arrival ranks, per CTA
+    // (its scratch lives in the weight ring, unused until the first copy)
+    nsmall = self_group(a, smeta, sperm, reinterpret_cast<int*>(smem), reinterpret_cast<int*>(smem) + a.E);
+  } else {
+    // the small groups' metadata, and the slot permutation when it is
+    // short, once per CTA: no dependent global loads when a warp changes unit
+    nsmall = *a.num_active - (a.num_large ? *a.num_large : 0);
+    for (int i = threadIdx.x; i < nsmall; i += blockDim.x) {
+      int e = a.active[i];
+      if (!bounds_ok((unsigned)e < (unsigned)a.E, a.status)) e = 0;
+      int m = a.counts[e], off = a.offsets[e];
+      if (!bounds_ok(off >= 0 && m >= 0 && off + m <= a.T * a.k, a.status)) m = 0, off = 0;
+      smeta[i] = make_int4(e, m, off, 0);
+    }
+    if (perm_smem)
+      for (int i = threadIdx.x; i < S; i += blockDim.x) sperm[i] = a.perm[i];
+    __syncthreads();
+  }
   Queue qs;
-  const int nsmall = *a.num_active - (a.num_large ? *a.num_large : 0);
   constexpr int FR = C::FR;
   qs.UPEg = a.I / (8 * FR);
   qs.UPEd = a.H / (16 * FR);
@@ -157,20 +178,6 @@ __global__ void __launch_bounds__(StreamCfg<F, NT>::kWarps * 32, 1) stream_gemm_
   qs.nkb_g = a.H / KB;
   qs.nkb_d = a.I / KB;
   const int nwarps = (int)gridDim.x * NW;
-  // the small groups' metadata, and the slot permutation when it is short,
-  // once per CTA: no dependent global loads when a warp changes unit
-  const int S = a.T * a.k;
-  const bool perm_smem = S <= kPermSmem;
-  for (int i = threadIdx.x; i < nsmall; i += blockDim.x) {
-    int e = a.active[i];
-    if (!bounds_ok((unsigned)e < (unsigned)a.E, a.status)) e = 0;
-    int m = a.counts[e], off = a.offsets[e];
-    if (!bounds_ok(off >= 0 && m >= 0 && off + m <= a.T * a.k, a.status)) m = 0, off = 0;
-    smeta[i] = make_int4(e, m, off, 0);
-  }
-  if (perm_smem)
-    for (int i = threadIdx.x; i < S; i += blockDim.x) sperm[i] = a.perm[i];
-  __syncthreads();
   const int* permp = perm_smem ? sperm : a.perm;
 
   // unit ids: the first by global warp index, later ones nwarps + ticket
@@ -611,6 +618,7 @@ cudaError_t launch_variant(const StreamGemmArgs& a, cudaStream_t stream) {
   const long long need = (units + C::kWarps - 1) / C::kWarps;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
+  // [rings][smeta E][sperm S]
   const int smem = C::kWarpBytes * C::kWarps + C::kLutBytes + 16 * a.E +
                    (S <= kPermSmem ? 4 * (int)S : 0);
   cudaError_t err = cudaFuncSetAttribute(stream_gemm_kernel<F, NT>,
