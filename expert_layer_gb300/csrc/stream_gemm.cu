@@ -80,7 +80,10 @@ struct StreamCfg {
   static constexpr int KB = kFp4 ? 128 : kQ8 ? 64 : 32;   // K elements per block
   static constexpr int KG = kDec ? 1 : 4;         // blocks per pipelined group
   static constexpr int FR = kDec ? (NT >= 4 ? 2 : 4) : 1;   // 16-row fragments per unit
-  static constexpr int NS = kDec ? (NT >= 4 ? 5 : 3) : 4;   // groups in the ring (NS-1 in flight)
+  // groups in the ring (NS-1 in flight).  bf16: three, which leaves more of
+  // the SM's unified L1 / shared memory to the token rows the warps share in
+  // L1 (decode64 streaming stage 188 -> 179 us against four)
+  static constexpr int NS = kDec ? (NT >= 4 ? 5 : 3) : 3;
   static constexpr int kWarps = kDec ? 8 : 12;
   // per-warp ring: [NS][KG][FR][2 rows][32 lanes] x 16 B of weights (codes),
   // plus the block scales of the decoded formats
