@@ -113,7 +113,9 @@ __device__ __forceinline__ TileInfo decode_tile(const TileMeta& md, const int* p
 //               warp; one arrive per warp on CTA 0's accumulator-empty
 //               barrier (16 per tile)
 constexpr int NS2 = 3;
-constexpr int kEpiWarps = 8;                             // epilogue warps 2 .. 9
+constexpr int kEpiWarps = 8;                             // epilogue warps 2 .. 2 + kEpiWarps - 1
+constexpr int kEpiSets = kEpiWarps / 4;                  // warps per TMEM lane quadrant
+constexpr int kEpiChunks = (BN / 32) / kEpiSets;          // 32-column chunks per warp and tile
 constexpr int kThreadsPair = (2 + kEpiWarps) * 32;
 constexpr int kPairRows = 128;                          // weight rows, token rows per CTA
 // A stage is 128 K wide, two 64-wide halves of each operand: one barrier
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   } else {
     // ------------------------------------------------------------ epilogue (each CTA)
     // warp w reads TMEM lanes 32(w % 4) .. +31 and the 32-column chunks
-    // v = 2i + hc of the tile (hc = 0 for warps 2-5, 1 for warps 6-9)
+    // v = kEpiSets * i + hc of the tile (hc = (warp - 2) / 4)
     const int q = warp & 3;
     const int hc = (warp - 2) >> 2;
     const uint32_t tempty0[2] = {map_to_rank(&tempty[0], 0), map_to_rank(&tempty[1], 0)};
@@ -299,13 +301,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       const int n = pair_n(rem);
       const int ncols = rem < n ? rem : n;           // token columns to store
       // down: slots and routing weights of this warp's columns (lane c of
-      // chunk i: token 32(2i + hc) + c), fetched before the accumulator wait
-      int fl[4];
-      float wl[4];
+      // chunk i: token 32(kEpiSets i + hc) + c), fetched before the accumulator wait
+      int fl[kEpiChunks];
+      float wl[kEpiChunks];
       if (kDown) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = 32 * (2 * i + hc) + lane;
+        for (int i = 0; i < kEpiChunks; ++i) {
+          const int c = 32 * (kEpiSets * i + hc) + lane;
           fl[i] = c < ncols ? __ldg(&a.perm[ti.off + tok0 + c]) : 0;
           if (!bounds_ok((unsigned)fl[i] < (unsigned)(a.T * a.k), a.status)) fl[i] = 0;
           wl[i] = c < ncols ? __ldg(&a.topk_w[fl[i]]) : 0.f;
@@ -317,8 +319,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       // rolled: inlined copies of the 32-column body would crowd the
       // instruction cache that the producer and MMA threads share
 #pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
-        const int c0 = 32 * (2 * i + hc);
+      for (int i = 0; i < kEpiChunks; ++i) {
+        const int c0 = 32 * (kEpiSets * i + hc);
         if (c0 >= ncols) break;   // uniform over the warp
         uint32_t y[32];
         tmem_ld32(tb + c0, y);
