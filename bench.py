@@ -113,11 +113,15 @@ def workload_name(workload: str, tokens) -> str:
 
 
 STAGE_SOURCES = {
-    "stream": ["expert_layer_gb300/csrc/stream_gemm.cu", "expert_layer_gb300/csrc/common.cuh",
-               "expert_layer_gb300/csrc/kernels.h"],
+    # the weight-streaming kernels (bf16: stream_gemm.cu; NVFP4 / int8: stream_dec.cu)
+    "stream": ["expert_layer_gb300/csrc/stream_gemm.cu", "expert_layer_gb300/csrc/stream_dec.cu",
+               "expert_layer_gb300/csrc/stream_common.cuh", "expert_layer_gb300/csrc/nvfp4.cuh",
+               "expert_layer_gb300/csrc/common.cuh", "expert_layer_gb300/csrc/kernels.h"],
     # the tensor-core stage: token-row gather + gate/up + down kernels
-    "tc": ["expert_layer_gb300/csrc/tc_gemm.cu", "expert_layer_gb300/csrc/tc_ptx.cuh",
-           "expert_layer_gb300/csrc/common.cuh", "expert_layer_gb300/csrc/kernels.h"],
+    # (W4A4: activation quantiser + block-scaled FP4 GEMMs, tc_fp4.cu)
+    "tc": ["expert_layer_gb300/csrc/tc_gemm.cu", "expert_layer_gb300/csrc/tc_fp4.cu",
+           "expert_layer_gb300/csrc/tc_ptx.cuh", "expert_layer_gb300/csrc/common.cuh",
+           "expert_layer_gb300/csrc/kernels.h"],
 }
 
 
