@@ -56,10 +56,13 @@ struct DecCfg {
   static constexpr int kStageBytes = kCodeBytes + kScaleBytes;
   // consumer warps, and stages per consumer ring: with the producer warp
   // three warps per SM sub-partition (168 registers each) for one or two
-  // token tiles per pass; two (255 registers) for four tiles, which spill at
-  // 168.  Measured at nvfp4_256 / int8_256: 11 consumers with 3 stages 153 /
-  // 205 us, 7 consumers with 4 stages 160 / 219 us.
-  static constexpr int NW = NT >= 4 ? 7 : 11;
+  // token tiles per pass; two (255 registers) for three or four tiles, which
+  // spill at 168.  Measured at nvfp4_256 / int8_256 (16 rows per expert on
+  // average): two tiles with 11 consumers and 3 stages 153 / 205 us, with 7
+  // consumers and 4 stages 160 / 219 us; three tiles (24-row passes, so that
+  // 97% of the experts decode their weights once) with 7 consumers 146 /
+  // 189 us.
+  static constexpr int NW = NT >= 3 ? 7 : 11;
   static constexpr int NS = FR == 4 ? 3 : 8;
   static constexpr int kThreads = (NW + 1) * 32;
   static constexpr int kRingBytes = NS * kStageBytes;
@@ -600,12 +603,17 @@ cudaError_t launch_stream_dec(const StreamGemmArgs& a, cudaStream_t stream) {
   const bool two = a.T > 8;
   const long long S = (long long)a.T * a.k;
   const long long avg = S / (S < a.E ? S : a.E);
+  // token tiles per pass: 32-row passes once the experts average 24 rows,
+  // 24-row passes from 12, else 16 (T > 8) or 8
   const bool four = a.T > 16 && avg >= 24;
+  const bool three = a.T > 16 && avg >= 12 && !four;
   if (a.gu_codes != nullptr) {
     if (four) return launch_dec<kFmtFp4, 4>(a, stream);
+    if (three) return launch_dec<kFmtFp4, 3>(a, stream);
     return two ? launch_dec<kFmtFp4, 2>(a, stream) : launch_dec<kFmtFp4, 1>(a, stream);
   }
   if (four) return launch_dec<kFmtQ8, 4>(a, stream);
+  if (three) return launch_dec<kFmtQ8, 3>(a, stream);
   return two ? launch_dec<kFmtQ8, 2>(a, stream) : launch_dec<kFmtQ8, 1>(a, stream);
 }
 

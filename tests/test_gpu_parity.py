@@ -70,6 +70,9 @@ SMALL_CASES = {
     "int8_tma_t4": dict(T=4, H=512, E=8, k=2, I=256, q8=True),
     "int8_tma_t40": dict(T=40, H=256, E=8, k=2, I=512, q8=True),
     "int8_tma_global_perm": dict(T=640, H=256, E=16, k=8, I=256, q8=True),
+    # 16 rows per expert on average: 24-row passes (three token tiles)
+    "nvfp4_tma_t3": dict(T=64, H=512, E=8, k=2, I=256, nvfp4=True, bias="zipf"),
+    "int8_tma_t3": dict(T=64, H=256, E=8, k=2, I=512, q8=True),
     # groups of >= 64 rows run on the tcgen05 kernels
     "tc_all": dict(T=512, H=256, E=8, k=2, I=128),
     "tc_mixed": dict(T=300, H=512, E=16, k=2, I=256, bias="zipf"),
