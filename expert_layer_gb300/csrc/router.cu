@@ -76,7 +76,7 @@ __device__ DotPart warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* 
      va4[it] = h < h1 ? *reinterpret_cast<const uint4*>(a + h) : make_uint4(0, 0, 0, 0);
      vb4[it] = h < h1 ? *reinterpret_cast<const uint4*>(b + h) : make_uint4(0, 0, 0, 0);
    }
-#pragma unroll
+#pragma unroll 1
    for (int it = 0; it < kB; ++it) {
     if (hb + 256 * it >= h1) break;   // whole warp: past the range
     const uint4 va = va4[it], vb = vb4[it];
@@ -84,9 +84,12 @@ __device__ DotPart warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* 
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
     uint32_t pu[8];
     bool outside = false;
-#pragma unroll
+    // rolled loops throughout: this code runs rarely, from a cold
+    // instruction cache, and its fetch time exceeded its execution time
+    // (a traced copy: 9-12 us per dot unrolled, 6-7 us rolled)
+#pragma unroll 1
     for (int i = 0; i < 4; ++i) {
-#pragma unroll
+#pragma unroll 1
       for (int j = 0; j < 2; ++j) {
         const float fa = j ? bf16hi(wa[i]) : bf16lo(wa[i]);
         const float fb = j ? bf16hi(wb[i]) : bf16lo(wb[i]);
@@ -100,13 +103,13 @@ __device__ DotPart warp_dot_f64(const uint16_t* __restrict__ a, const uint16_t* 
     }
     if (__any_sync(0xffffffffu, outside || !fixed_ok)) {
       used64 = true;
-#pragma unroll
+#pragma unroll 1
       for (int i = 0; i < 4; ++i) {
         s[i] = fma((double)bf16lo(wa[i]), (double)bf16lo(wb[i]), s[i]);
         s[i] = fma((double)bf16hi(wa[i]), (double)bf16hi(wb[i]), s[i]);
       }
     } else {
-#pragma unroll
+#pragma unroll 1
       for (int i = 0; i < 8; ++i) acc += fixed_of_product(pu[i]);
     }
    }
