@@ -15,7 +15,7 @@ import torch
 
 __all__ = ["MoEError", "lib", "workspace_size", "alloc_workspace", "route", "permute", "forward",
            "read_status", "read_diagnostics", "LIB_PATH", "nvfp4_tc_scales", "nvfp4_quantize",
-           "W4A4Weights", "w4a4_weights", "forward_w4a4"]
+           "W4A4Weights", "w4a4_weights", "forward_w4a4", "forward_int8", "int8_struct"]
 
 # MOE_GB300_LIB selects another build of the library (e.g. the index-checking
 # MOE_DEBUG_BOUNDS build); the default is the in-tree libmoe_gb300.so.
