@@ -251,10 +251,15 @@ def algorithmic_bytes(inp, split):
     pb = 4 if S * H * 4 <= (32 << 20) else 2                        # bytes per partial
     per_row = H * 2 + 2 * I * 2 + H * pb   # token row in, h out and back in, partial out
     A = split["A_s"] + split["A_l"]
+    # without tensor-core groups and with a small combine, the streaming
+    # kernel also does the combine (the library's rule; 152 SMs)
+    fused = (split["A_l"] == 0 and getattr(inp, "x_global", None) is None
+             and T * H // (4 if pb == 4 else 8) <= 224 * 152)
     return {
         "route": E * H * 2 + T * H * 2 + S * 8,
         "permute": S * 4 * 4 + E * 12,
-        "stream": split["A_s"] * 3 * I * H * wb + split["S_s"] * per_row,
+        "stream": split["A_s"] * 3 * I * H * wb + split["S_s"] * per_row
+        + (S * H * pb + T * H * 2 if fused else 0),
         "tc": split["A_l"] * 3 * I * H * wb + split["S_l"] * per_row,
         "quant_x": S * H * 2 + S * H * (0.5 + 1.0 / 16),
         "combine": S * H * pb + T * H * 2,

@@ -64,7 +64,8 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
   L.nblk = (int)((S + kPermBlock - 1) / kPermBlock);
   L.partial_f32 = (size_t)S * (size_t)H * 4 <= kPartialF32Limit;
   L.hdr = take(sizeof(WsHeader));
-  L.sched = take(sizeof(int) * (E + 1));   // expert-GEMM queue counter, then per-slot counters
+  // expert-GEMM queue counter, per-slot counters, the fused combine's counter
+  L.sched = take(sizeof(int) * (E + 2));
   L.cnt = take(sizeof(int) * T);
   L.acnt = take(sizeof(int) * E);          // per-expert slot counters (ranks by arrival)
   L.xnorm = take(sizeof(float) * T);

@@ -100,6 +100,12 @@ struct StreamGemmArgs {
   int32_t* inv_perm_out;
   int* num_active_out;
   int* num_large_out;
+  // fused combine (every group on this kernel): after its units each CTA
+  // arrives on *done and waits for all CTAs (all are resident), then sums its
+  // slice of out[t] = sum_s partial[t*k + s] in slot order
+  bool fused_combine;
+  int* done;                 // zero at launch
+  uint16_t* out;             // [T, H] bf16
   // bounded waits: polls before a down unit's wait gives up; with
   // wait_extra > 0 the wait aims at a count that no unit reaches (test-only
   // forced timeout, see moe_debug_force_wait_timeout)

@@ -270,6 +270,15 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
   a.partial_f32 = L.partial_f32;
   a.queue = ws_ptr<int>(workspace, L.sched);
   a.dep = a.queue + 1;
+  // with every group on the streaming kernel, and a combine small enough
+  // that each of its threads (at least 224 per SM) sums about one 16-byte
+  // vector, the streaming kernel also does the combine (measured: decode8
+  // 94.9 -> 93.2-94.0 us per step; at T = 256 the separate, wider combine
+  // kernel is 2-3 us faster)
+  const long long comb_vecs = (long long)T * (H / (L.partial_f32 ? 4 : 8));
+  a.fused_combine = !use_tc && comb_vecs <= 224ll * num_sms;
+  a.done = a.queue + 1 + E;
+  a.out = out;
   a.status = &hdr->status;
   a.num_sms = num_sms;
   if (fuse) {
@@ -299,7 +308,8 @@ static int forward_impl(const uint16_t* x, const uint16_t* gate_w, const float* 
     MOE_TRY_CUDA(launch_tc_gemm(tc, true, s, launches));
   }
   MOE_TRY_CUDA(mark(4));
-  MOE_TRY_CUDA(launch_combine(a.partial, L.partial_f32, T, H, top_k, out, num_sms, s, launches));
+  if (!a.fused_combine)
+    MOE_TRY_CUDA(launch_combine(a.partial, L.partial_f32, T, H, top_k, out, num_sms, s, launches));
   MOE_TRY_CUDA(mark(5));
   return MOE_OK;
 }

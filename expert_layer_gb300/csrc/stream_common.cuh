@@ -184,6 +184,74 @@ __device__ int self_group(const StreamGemmArgs& a, int4* smeta, int* sperm, int*
   return nact;
 }
 
+// Grid-wide arrive and wait of one thread per CTA (every CTA of the launch
+// is resident: persistent grids of at most one CTA per SM).  The caller has
+// passed a CTA barrier after its CTA's last writes; the fence makes them
+// visible device-wide before the arrive.  Bounded: false (and
+// kStatusTimeout) after kSpinLimit polls.
+__device__ bool grid_sync(int* ctr, int n, int* status) {
+  __threadfence();
+  atomicAdd(ctr, 1);
+  int it = 0;
+  while (ld_acquire(ctr) < n) {
+    if (++it > kSpinLimit) {
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// The combine after a grid_sync: vectors i = first, first + stride, ... of
+// out viewed as [T][H / V] (V = 4 fp32 or 8 bf16 partials per 16 bytes);
+// each sums the k partial vectors of its token in slot order from zero in
+// fp32 and rounds to bf16 once -- the same arithmetic and order as the
+// combine kernel.  The partials come from other CTAs: loads through L2.
+__device__ void combine_slice(const StreamGemmArgs& a, long long first, long long stride) {
+  const int H = a.H, k = a.k, V = a.partial_f32 ? 4 : 8;
+  const long long nvec = (long long)a.T * (H / V);
+  for (long long i = first; i < nvec; i += stride) {
+    const long long t = i / (H / V);
+    const int d = (int)(i % (H / V)) * V;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // the slots' vectors in batches of 8, all loads of a batch issued first
+    for (int s0 = 0; s0 < k; s0 += 8) {
+      uint4 q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        q[j] = make_uint4(0, 0, 0, 0);
+        if (s0 + j < k) {
+          const size_t row = (size_t)(t * k + s0 + j) * H + d;
+          q[j] = a.partial_f32
+                     ? __ldcg(reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(a.partial) + row))
+                     : __ldcg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.partial) + row));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j >= k) break;
+        const uint32_t w4[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+        if (a.partial_f32) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] += __uint_as_float(w4[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) { acc[2 * i] += bf16lo(w4[i]); acc[2 * i + 1] += bf16hi(w4[i]); }
+        }
+      }
+    }
+    if (a.partial_f32) {
+      *reinterpret_cast<uint2*>(a.out + (size_t)t * H + d) =
+          make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+    } else {
+      *reinterpret_cast<uint4*>(a.out + (size_t)t * H + d) =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                     pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
 }  // namespace
 }  // namespace stream
 }  // namespace moe

@@ -522,6 +522,17 @@ __global__ void __launch_bounds__(DecCfg<F, NT>::kThreads, 1)
     }
   }
   if (dead) atomicOr(a.status, kStatusTimeout);
+  if (a.fused_combine) {
+    // every group was on this launch: once all CTAs' partials are written,
+    // the consumer warps combine (named barrier 1 over the consumers; the
+    // producer warp may have left; the ring's first word, idle now, carries
+    // the verdict)
+    asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+    int* flag = reinterpret_cast<int*>(smem);
+    if (threadIdx.x == 0) *flag = grid_sync(a.done, (int)gridDim.x, a.status) ? 1 : 0;
+    asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+    if (*flag) combine_slice(a, (long long)blockIdx.x * (NW * 32) + threadIdx.x, (long long)gridDim.x * (NW * 32));
+  }
 }
 
 // Byte tensor map (uint8, no swizzle) of the given rank; strides in bytes

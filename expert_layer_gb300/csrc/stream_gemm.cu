@@ -609,6 +609,15 @@ __global__ void __launch_bounds__(StreamCfg<F, NT>::kWarps * 32, 1) stream_gemm_
     pop();
   }
   cp_async_wait<0>();
+  if (a.fused_combine) {
+    // every group was on this launch: once all CTAs' partials are written,
+    // the combine runs here (the ring's first word carries the verdict)
+    __syncthreads();
+    int* flag = reinterpret_cast<int*>(smem);
+    if (threadIdx.x == 0) *flag = grid_sync(a.done, (int)gridDim.x, a.status) ? 1 : 0;
+    __syncthreads();
+    if (*flag) combine_slice(a, (long long)blockIdx.x * blockDim.x + threadIdx.x, (long long)gridDim.x * blockDim.x);
+  }
 }
 
 template <int F, int NT>

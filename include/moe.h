@@ -155,7 +155,8 @@ int moe_forward(const uint16_t *x, const uint16_t *gate_w, const float *bias,
  * created by the caller) on `stream` at the stage boundaries
  *   [0] start  [1] after routing  [2] after grouping
  *   [3] after the weight-streaming expert kernel (gate/up, SwiGLU and down of
- *       the experts with few rows, one launch)
+ *       the experts with few rows, one launch; when no expert goes to the
+ *       tensor-core kernels it also does the combine)
  *   [4] after the tensor-core expert kernels (gate/up+SwiGLU, then down, of
  *       the experts with many rows; none for small batches)  [5] after combine
  * and stores in *kernels_launched (HOST pointer, may be NULL) the number of
