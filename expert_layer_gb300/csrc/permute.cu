@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kThreads) permute_single_kernel(
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv_perm, int32_t* __restrict__ active, int32_t* __restrict__ tiles,
     void* ws) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   __shared__ int4 sw[kWarps];
   grouping::group_single_block(idx, S, E, large_threshold, tile_rows, counts, offsets, perm,
@@ -41,6 +43,7 @@ constexpr size_t kScanSmemMax = 160 * 1024;
 __global__ void __launch_bounds__(kThreads) permute_block_rank_kernel(
     const int32_t* __restrict__ idx, int S, int E, int32_t* __restrict__ blk_cnt,
     int32_t* __restrict__ lrank, void* ws) {
+  pdl_wait();
   extern __shared__ int tab[];  // [kWarps][E]
   const int f = blockIdx.x * kThreads + threadIdx.x;
   int e = -1;
@@ -62,6 +65,8 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
     int tile_rows, int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ active, int32_t* __restrict__ tiles,
     void* ws, int staged) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   int* s_cnt = smem;       // [E]
   int* s_off = s_cnt + E;  // [E]
@@ -149,6 +154,7 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
 __global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
     const int32_t* __restrict__ idx, int S, int E, const int32_t* __restrict__ blk_base,
     const int32_t* __restrict__ lrank, int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm) {
+  pdl_wait();
   const int f = blockIdx.x * kThreads + threadIdx.x;
   if (f >= S) return;
   const int e = idx[f];
@@ -173,10 +179,8 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* cou
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     if (launches) *launches += 1;
-    permute_single_kernel<<<1, kThreads, smem, stream>>>(idx, S, E, large_threshold, tile_rows,
-                                                         counts, offsets, perm, inv_perm, active,
-                                                         tiles, ws);
-    return cudaGetLastError();
+    return launch_pdl(permute_single_kernel, dim3(1), dim3(kThreads), smem, stream, idx, S, E, large_threshold,
+                      tile_rows, counts, offsets, perm, inv_perm, active, tiles, ws);
   }
   int32_t* blk_cnt = ws_ptr<int32_t>(ws, L.blk_cnt);
   int32_t* blk_base = ws_ptr<int32_t>(ws, L.blk_base);
@@ -186,19 +190,20 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* cou
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tab);
   if (err != cudaSuccess) return err;
   if (launches) *launches += 3;
-  permute_block_rank_kernel<<<L.nblk, kThreads, smem_tab, stream>>>(idx, S, E, blk_cnt, lrank, ws);
+  err = launch_pdl(permute_block_rank_kernel, dim3(L.nblk), dim3(kThreads), smem_tab, stream, idx, S, E, blk_cnt,
+                   lrank, ws);
+  if (err != cudaSuccess) return err;
   const size_t scan_smem_staged = sizeof(int) * (2 * (size_t)E + (size_t)L.nblk * E);
   const int staged = scan_smem_staged <= kScanSmemMax ? 1 : 0;
   const size_t scan_smem = staged ? scan_smem_staged : sizeof(int) * 2 * (size_t)E;
   err = cudaFuncSetAttribute(permute_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)scan_smem);
   if (err != cudaSuccess) return err;
-  permute_scan_kernel<<<1, kThreads, scan_smem, stream>>>(
-      blk_cnt, L.nblk, S, E, large_threshold, tile_rows, blk_base, counts, offsets, active, tiles,
-      ws, staged);
-  permute_scatter_kernel<<<L.nblk, kThreads, 0, stream>>>(idx, S, E, blk_base, lrank, perm,
-                                                          inv_perm);
-  return cudaGetLastError();
+  err = launch_pdl(permute_scan_kernel, dim3(1), dim3(kThreads), scan_smem, stream, (const int32_t*)blk_cnt,
+                   L.nblk, S, E, large_threshold, tile_rows, blk_base, counts, offsets, active, tiles, ws, staged);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(permute_scatter_kernel, dim3(L.nblk), dim3(kThreads), 0, stream, idx, S, E,
+                    (const int32_t*)blk_base, (const int32_t*)lrank, perm, inv_perm);
 }
 
 }  // namespace moe

@@ -763,6 +763,7 @@ __global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
     int T, int H, int E, float* __restrict__ logits, float* __restrict__ xnorm, uint16_t* __restrict__ x16,
     int* status) {
+  pdl_wait();   // programmatic dependent launch: the workspace is ready
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // [pair][buf]: x tile [kTileK][kTileT] then w tile [kTileK][kTileE], fp32
   float* tiles = reinterpret_cast<float*>(smem_raw);
@@ -929,6 +930,7 @@ __global__ void __launch_bounds__(256, 3) router_select_kernel(
     int T, int H, int E, int k, float gamma, const float* __restrict__ logits,
     const float* __restrict__ xnorm, const float* __restrict__ wnorm, double* __restrict__ l64,
     int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
+  pdl_wait();   // the logits and norms are complete
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ DotPart s_part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -974,6 +976,8 @@ __global__ void __launch_bounds__(256, 3) router_select_kernel(
 // ||w_e|| for every expert, one warp per expert.
 __global__ void __launch_bounds__(256) wnorm_kernel(const uint16_t* __restrict__ gw, int H, int E,
                                                     float* __restrict__ wnorm) {
+  pdl_wait();
+  pdl_trigger();   // the logits kernel does not read ||w_e||; it may launch at once
   const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (e >= E) return;
   float sq = 0.f;
@@ -1009,21 +1013,23 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
   if (tiled) {
     float* logits = ws_ptr<float>(ws, L.logits);
     float* xnorm = ws_ptr<float>(ws, L.xnorm);
-    wnorm_kernel<<<(E + 7) / 8, 256, 0, stream>>>(gate_w, H, E, wnorm);
+    cudaError_t err = launch_pdl(wnorm_kernel, dim3((E + 7) / 8), dim3(256), 0, stream, gate_w, H, E, wnorm);
+    if (err != cudaSuccess) return err;
     const size_t smem = sizeof(float) * 4 * kTileBuf;
-    cudaError_t err = cudaFuncSetAttribute(router_tile_kernel,
+    err = cudaFuncSetAttribute(router_tile_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    router_tile_kernel<<<(T + kTileT - 1) / kTileT, kTileThreads, smem, stream>>>(
-        x, gate_w, bias, T, H, E, logits, xnorm, x16, &reinterpret_cast<WsHeader*>(ws)->status);
+    err = launch_pdl(router_tile_kernel, dim3((T + kTileT - 1) / kTileT), dim3(kTileThreads), smem, stream, x,
+                     gate_w, bias, T, H, E, logits, xnorm, x16, &reinterpret_cast<WsHeader*>(ws)->status);
+    if (err != cudaSuccess) return err;
     const size_t smem2 = sizeof(WarpScratch) * 8;
     err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem2);
     if (err != cudaSuccess) return err;
     const float gamma = gamma_bound(kTileK + H / kTileK + 1);
-    router_select_kernel<<<(T + 7) / 8, 256, smem2, stream>>>(x, gate_w, bias, T, H, E, k, gamma,
-                                                              logits, xnorm, wnorm, l64, idx, w, ws);
-    return cudaGetLastError();
+    return launch_pdl(router_select_kernel, dim3((T + 7) / 8), dim3(256), smem2, stream, x, gate_w, bias, T, H,
+                      E, k, gamma, (const float*)logits, (const float*)xnorm, (const float*)wnorm, l64, idx, w,
+                      ws);
   }
   const float gamma = gamma_bound(H / 32 + 5);
   const bool grp = group != nullptr;

@@ -136,6 +136,7 @@ template <bool kDown>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
+  pdl_wait();   // programmatic dependent launch: the grouping and token rows are complete
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ perm, int S,
                                                           int H, int k, uint16_t* __restrict__ xp,
                                                           int* status) {
+  pdl_wait();   // programmatic dependent launch: the permutation is complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (long long r = (long long)blockIdx.x * 8 + warp; r < S; r += (long long)gridDim.x * 8) {
     int f = perm[r];
@@ -399,10 +401,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int S, int H, int k,
                                uint16_t* xp, int* status, cudaStream_t stream, int* launches) {
   const long long blocks = ((long long)S + 7) / 8;
-  gather_rows_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(x, perm, S, H, k, xp,
-                                                                                     status);
   if (launches) *launches += 1;
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(256), 0, stream, x,
+                    perm, S, H, k, xp, status);
 }
 
 cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, int* launches) {
@@ -460,13 +461,15 @@ cudaError_t launch_tc_gemm(const TcLaunch& p, bool down, cudaStream_t stream, in
   cfg.blockDim = dim3(kThreadsPair);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
 }
 
