@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
                                                          int E, const float* __restrict__ glob,
                                                          uint8_t* __restrict__ codes,
                                                          uint8_t* __restrict__ sf, int* status) {
+  pdl_wait();   // programmatic dependent launch: the grouping (or h) is complete
   __shared__ int tpre[kMaxE + 1];
   // 128-row blocks before each expert: every thread loads counts, one warp
   // scans (lane l owns experts [32l .. 32l + 31] of at most 1024)
@@ -357,6 +358,7 @@ template <bool kDown>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const Fp4Args a) {
+  pdl_wait();   // programmatic dependent launch: the quantised token rows are complete
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -666,12 +668,10 @@ cudaError_t launch_quant_rows(bool gather, const uint16_t* src, const int32_t* p
   const long long cap = 3ll * nsm;   // grid-stride rows: the CTAs that are resident at once
   const unsigned grid = (unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
   if (gather)
-    quant_rows_kernel<true><<<grid, 256, 0, stream>>>(src, perm, idx, k, counts, offsets, S, K, E, glob, codes,
-                                                      sf, status);
-  else
-    quant_rows_kernel<false><<<grid, 256, 0, stream>>>(src, perm, idx, k, counts, offsets, S, K, E, glob, codes,
-                                                       sf, status);
-  return cudaGetLastError();
+    return launch_pdl(quant_rows_kernel<true>, dim3(grid), dim3(256), 0, stream, src, perm, idx, k, counts, offsets,
+                      S, K, E, glob, codes, sf, status);
+  return launch_pdl(quant_rows_kernel<false>, dim3(grid), dim3(256), 0, stream, src, perm, idx, k, counts, offsets,
+                    S, K, E, glob, codes, sf, status);
 }
 
 cudaError_t launch_quant_plain(const uint16_t* src, int R, int K, float g, uint8_t* codes, uint8_t* scales,
@@ -716,8 +716,7 @@ cudaError_t launch_tc_fp4(const Fp4Launch& p, bool down, cudaStream_t stream, in
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
   if (launches) *launches += 1;
-  kern<<<p.num_sms, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p.num_sms), dim3(kThreads), kSmemBytes, stream, tmA, tmB, a);
 }
 
 }  // namespace moe
