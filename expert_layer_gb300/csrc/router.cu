@@ -18,6 +18,8 @@
 #include <float.h>
 #include <limits.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -428,8 +430,11 @@ __device__ void select_end(int E, int k, WarpScratch& sc, const double* l64_row,
 // computes the logits of kEPW experts (16y + w for kTT = 1; 32y + 2w, +1 for
 // chunks of 4 or 8 tokens) for the kTT tokens of chunk c, holding its gate
 // rows in registers.  Lane l sums the products at h = 8l + 256j + (0..7)
-// sequentially (H/32 terms), then a 5-level xor tree: at most H/32 + 4
-// roundings per product.  With kTT = 1 the warp reads the token row from
+// in kChains sequential chains (vector j goes to chain j mod kChains: 8
+// chains for one-token chunks, 2 for four-token chunks, 1 for eight, as the
+// registers allow), adds the chains pairwise, then a 5-level xor tree: at
+// most min(H/32, 64 ceil(H/2048) / kChains) + log2(kChains) + 5 roundings
+// per product (16 at H = 2048 for one-token chunks, against 69 in one chain).  With kTT = 1 the warp reads the token row from
 // global memory; larger chunks first stage the chunk's token rows (2048
 // columns at a time) in shared memory, so each warp's token loads are
 // shared-memory reads.  Warps w < #tokens of the y = 0 CTAs also write
@@ -447,6 +452,10 @@ constexpr int kXCols = 2048;   // token-row columns staged per block
 template <int kTT>
 struct SmallCfg {
   static constexpr int kEPW = kTT >= 4 ? 2 : 1;            // experts per warp
+  // independent accumulation chains per (expert, token) in a lane: chain
+  // v % kChains takes the products of 16-byte vector v (fewer roundings per
+  // product, so a tighter certified bound and fewer exact re-rankings)
+  static constexpr int kChains = kTT == 1 ? 8 : kTT == 4 ? 2 : 1;
   static constexpr int kExperts = kSmallWarps * kEPW;     // experts per CTA
   static constexpr bool kStaged = kTT >= 4;                // token rows in shared memory
 };
@@ -537,12 +546,15 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
       reinterpret_cast<unsigned char*>(dsm) +
       ((router_small_select_bytes(E, kTT) + 15) & ~size_t(15)));
   const bool xn_warp = blockIdx.y == 0 && warp < nt;   // this warp writes ||x_{t0+warp}||
-  float acc[kEPW][kTT], sq[kEPW], sqx = 0.f;
+  constexpr int NC = Cfg::kChains;
+  float acc[kEPW][kTT][NC], sq[kEPW], sqx = 0.f;
 #pragma unroll
   for (int ep = 0; ep < kEPW; ++ep) {
     sq[ep] = 0.f;
 #pragma unroll
-    for (int tt = 0; tt < kTT; ++tt) acc[ep][tt] = 0.f;
+    for (int tt = 0; tt < kTT; ++tt)
+#pragma unroll
+      for (int c = 0; c < NC; ++c) acc[ep][tt][c] = 0.f;
   }
   for (int hb = 0; hb < H; hb += 2048) {
     uint4 wv[kEPW][8];
@@ -583,7 +595,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
           for (int ep = 0; ep < kEPW; ++ep) {
             const uint32_t ww[4] = {wv[ep][v].x, wv[ep][v].y, wv[ep][v].z, wv[ep][v].w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[ep][tt] = fma_bf16x2(xw[i], ww[i], acc[ep][tt]);
+            for (int i = 0; i < 4; ++i) acc[ep][tt][v % NC] = fma_bf16x2(xw[i], ww[i], acc[ep][tt][v % NC]);
           }
         }
       }
@@ -620,12 +632,24 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
         const uint32_t ww[4] = {wv[0][v].x, wv[0][v].y, wv[0][v].z, wv[0][v].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          acc[0][0] = fma_bf16x2(xw[i], ww[i], acc[0][0]);
+          acc[0][0][v % NC] = fma_bf16x2(xw[i], ww[i], acc[0][0][v % NC]);
           if (xn_warp) sqx = fma_bf16x2(xw[i], xw[i], sqx);
         }
       }
     }
   }
+  // the chains pairwise (log2 NC levels), then the lanes (5 levels)
+  float dot[kEPW][kTT];
+#pragma unroll
+  for (int ep = 0; ep < kEPW; ++ep)
+#pragma unroll
+    for (int tt = 0; tt < kTT; ++tt) {
+#pragma unroll
+      for (int w = NC / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) acc[ep][tt][c] += acc[ep][tt][c + w];
+      dot[ep][tt] = acc[ep][tt][0];
+    }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     sqx += __shfl_xor_sync(0xffffffffu, sqx, o);
@@ -633,16 +657,16 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
     for (int ep = 0; ep < kEPW; ++ep) {
       sq[ep] += __shfl_xor_sync(0xffffffffu, sq[ep], o);
 #pragma unroll
-      for (int tt = 0; tt < kTT; ++tt) acc[ep][tt] += __shfl_xor_sync(0xffffffffu, acc[ep][tt], o);
+      for (int tt = 0; tt < kTT; ++tt) dot[ep][tt] += __shfl_xor_sync(0xffffffffu, dot[ep][tt], o);
     }
   }
 #pragma unroll
   for (int ep = 0; ep < kEPW; ++ep) {
     const int e = e0 + ep;
     if (e >= E) continue;
-    float mine = acc[ep][0];
+    float mine = dot[ep][0];
 #pragma unroll
-    for (int tt = 1; tt < kTT; ++tt) if (lane == tt) mine = acc[ep][tt];
+    for (int tt = 1; tt < kTT; ++tt) if (lane == tt) mine = dot[ep][tt];
     if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = bias ? mine + bias[e] : mine;
     if (lane == 31) wnorm[e] = sqrtf(sq[ep]);   // the same value from every chunk's CTA
   }
@@ -1031,9 +1055,14 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
                       E, k, gamma, (const float*)logits, (const float*)xnorm, (const float*)wnorm, l64, idx, w,
                       ws);
   }
-  const float gamma = gamma_bound(H / 32 + 5);
-  const bool grp = group != nullptr;
   const int tt = T <= 16 ? 1 : T <= 128 ? 4 : 8;
+  // roundings per product: the lane's chain (at most 64 per 2048 columns
+  // over the chains, and never more than the lane's H/32 products), the
+  // chain tree, the 5-level lane tree
+  const int nc = tt == 1 ? SmallCfg<1>::kChains : tt == 4 ? SmallCfg<4>::kChains : SmallCfg<8>::kChains;
+  const int per_chain = std::min(H / 32, 64 * ((H + 2047) / 2048) / nc);
+  const float gamma = gamma_bound(per_chain + (nc == 8 ? 3 : nc == 2 ? 1 : 0) + 5);
+  const bool grp = group != nullptr;
   const size_t smem = router_small_smem(E, tt);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   const int per_cta = tt >= 4 ? SmallCfg<4>::kExperts : SmallCfg<1>::kExperts;
