@@ -45,13 +45,20 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte slot");
 
 // Offsets (bytes) of every workspace region for one shape.
 struct WsLayout {
-  size_t hdr, sched, cnt, xnorm, wnorm, logits, logits64, idx, w, counts, offsets, active, tiles, blk_cnt,
+  size_t hdr, sched, cnt, xnorm, wnorm, logits, logits64, lpart, xsq, idx, w, counts, offsets, active, tiles, blk_cnt,
       blk_base, lrank, perm, inv_perm, h, partial, xp, x16, acnt, total;
   int nblk;               // 512-slot blocks of the grouping kernels
   bool partial_f32;       // fp32 partials (else bf16)
 };
 
 constexpr int kPermBlock = 512;            // slots per grouping block
+
+// Large batches route through the tiled logits kernel (stream-K over token
+// blocks and K chunks; a block's partial logits come in at most
+// kRouteTilePieces pieces, each with its partial ||x_t||^2).
+constexpr int kRouteTilePieces = 4;
+constexpr long long kRouteTileMaxE = 128;
+inline bool route_tiled(long long T, long long E) { return T >= 2048 && E <= kRouteTileMaxE; }
 constexpr size_t kPartialF32Limit = 32ull << 20;
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -72,6 +79,9 @@ inline WsLayout make_layout(long long T, long long H, long long E, long long I, 
   L.wnorm = take(sizeof(float) * E);
   L.logits = take(sizeof(float) * T * E);
   L.logits64 = take(sizeof(double) * T * E);
+  const bool tiled = route_tiled(T, E);   // the tiled router's pieces
+  L.lpart = take(tiled ? sizeof(float) * kRouteTilePieces * T * E : 0);
+  L.xsq = take(tiled ? sizeof(float) * kRouteTilePieces * T : 0);
   L.idx = take(sizeof(int) * S);
   L.w = take(sizeof(float) * S);
   L.counts = take(sizeof(int) * E);

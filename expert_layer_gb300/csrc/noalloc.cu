@@ -35,11 +35,13 @@ namespace {
 // Largest T*E the array serves; T itself is also bounded (xnorm holds T floats).
 constexpr long long kNoAllocMaxTE = 65536;
 constexpr long long kNoAllocMaxT = 8192;
-// header + scheduling counters[E+1] + counters[T] + xnorm[T] + wnorm[E] +
-// fp32 logits[T*E] + fp64 logits[T*E], each region 256-byte aligned (the
-// router's part of the workspace layout)
-constexpr size_t kNoAllocScratchBytes = 256 + 1025 * 4 + 2 * kNoAllocMaxT * 4 + 1024 * 4 +
-                                        kNoAllocMaxTE * 4 + kNoAllocMaxTE * 8 + 6 * 256;
+// header + scheduling counters[E+2] + counters[T] + per-expert counters[E] +
+// xnorm[T] + wnorm[E] + fp32 logits[T*E] + fp64 logits[T*E] + the tiled
+// router's pieces (partial logits[pieces*T*E], partial squares[pieces*T]),
+// each region 256-byte aligned (the router's part of the workspace layout)
+constexpr size_t kNoAllocScratchBytes =
+    256 + 1026 * 4 + 2 * kNoAllocMaxT * 4 + 2 * 1024 * 4 + kNoAllocMaxTE * 4 + kNoAllocMaxTE * 8 +
+    moe::kRouteTilePieces * (kNoAllocMaxTE + kNoAllocMaxT) * 4 + 9 * 256;
 
 __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratchBytes];
 

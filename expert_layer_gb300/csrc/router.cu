@@ -765,48 +765,89 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_small_kernel(
 }
 
 // ------------------------------------------------------------ large batches
-// Logits: one CTA = 32 tokens x all E (<= 128) experts, 4 warps.  K runs in
-// chunks of 32; the even chunks go to warps 0-1 and the odd chunks to warps
-// 2-3 (each pair has its own double-buffered tiles and named barrier).  In a
-// pair, warp w covers tokens 16(w mod 2) .. +15: lane l owns the 8 tokens
-// 8(l / 16) .. +7 of them and the 8 experts 4(l mod 16) .. +3 and
-// 64 + 4(l mod 16) .. +3, so a step is 64 FMAs from four 16-byte shared loads
-// (the token loads are broadcasts) -- register blocking that keeps the FMA
-// pipe, not shared memory, the limit.  A chunk's 32 products are summed
-// sequentially from zero (31 roundings); each pair adds its chunk sums in
-// order (H/64 additions) and the two pairs' totals are added once: at most
-// 32 + H/32 roundings per product.  Selection then runs one warp per token.
-constexpr int kTileT = 32, kTileE = 128, kTileK = 32, kTileThreads = 128;
-constexpr int kTileBuf = kTileK * (kTileT + kTileE);   // floats of one chunk's tiles
+// Logits, stream-K over a persistent grid.  A work item is (32-token block b,
+// 32-wide K chunk c); the Q = nblocks * nchunks items, block-major, are split
+// evenly over the G CTAs of the launch (CTA i: items [iQ/G, (i+1)Q/G)), so
+// every SM gets the same number of chunk products whatever T is.  A CTA's
+// range may cross block boundaries: for every block it touches it stores one
+// piece, the block's partial logits over the chunks it covered, in slot
+// p = i - (first CTA of the block); the select kernel adds a block's pieces
+// in slot order.  The host sizes G so that a block has at most kTilePieces
+// pieces.
+//
+// Inside a CTA: 4 warps, the even chunks of a segment to warps 0-1 and the
+// odd chunks to warps 2-3 (each pair with its own double-buffered tiles and
+// named barrier).  In a pair, warp w covers tokens 16(w mod 2) .. +15: lane
+// l owns the 8 tokens 8(l / 16) .. +7 of them and the experts 4(l mod 16)
+// .. +3 and 64 + 4(l mod 16) .. +3.  The products run on paired fp32 FMAs
+// (fma.rn.f32x2: two independent fp32 fmas, each rounded as fmaf): the x
+// tile holds every value twice, (x, x), so one 16-byte shared load gives two
+// tokens' pairs and one f32x2 fma updates two experts of a token; a step is
+// 32 paired fmas from six 16-byte shared loads.  (Four experts a lane, 16
+// warps per SM at 128 registers, was slower: 10 more shared loads per 32
+// paired fmas.)
+//
+// Roundings per product: a chunk's 32 products are summed sequentially from
+// zero (31), a pair adds its chunk sums in order (at most nchunks/2), the two
+// pairs' totals are added once, and the select kernel adds at most
+// kTilePieces pieces: 31 + nchunks/2 + 1 + (kTilePieces - 1).
+constexpr int kTileT = 32, kTileE = 128, kTileK = 32, kTileThreads = 128, kTilePieces = 4;
+// floats of one chunk's tiles: x [kTileK][kTileT] as (x, x) pairs, then w [kTileK][kTileE]
+constexpr int kTileXF = 2 * kTileK * kTileT;
+constexpr int kTileBuf = kTileXF + kTileK * kTileE;
+
+// The CTA whose item range holds item q (CTA i starts at floor(iQ/G)).
+__host__ __device__ inline long long tile_cta_of(long long q, long long Q, long long G) {
+  return ((q + 1) * G - 1) / Q;
+}
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-__global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
-    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
-    int T, int H, int E, float* __restrict__ logits, float* __restrict__ xnorm, uint16_t* __restrict__ x16,
-    int* status) {
+// c + a * b and c + a, elementwise on fp32 pairs (each half rounded as the
+// scalar fmaf / fadd)
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%0, %1};\n fma.rn.f32x2 rc, ra, rb, rc;\n mov.b64 {%0, %1}, rc;\n}"
+      : "+f"(c.x), "+f"(c.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return c;
+}
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n"
+      " add.rn.f32x2 ra, ra, rb;\n mov.b64 {%0, %1}, ra;\n}"
+      : "+f"(a.x), "+f"(a.y)
+      : "f"(b.x), "f"(b.y));
+  return a;
+}
+
+__global__ void __launch_bounds__(kTileThreads, 2) router_tile_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, int T, int H, int E, int G,
+    float* __restrict__ lpart, float* __restrict__ xsq, uint16_t* __restrict__ x16, int* status) {
   pdl_wait();   // programmatic dependent launch: the workspace is ready
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // [pair][buf]: x tile [kTileK][kTileT] then w tile [kTileK][kTileE], fp32
+  // [pair][buf]: x tile then w tile, fp32
   float* tiles = reinterpret_cast<float*>(smem_raw);
   __shared__ float s_sq[2][kTileT * 4];   // ||x_t||^2 partials of each pair
   const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * kTileT;
   const int warp = tid >> 5, lane = tid & 31;
-  const int pair = warp >> 1;             // chunks kc with kc % 2 == pair
+  const int pair = warp >> 1;             // the segment's chunks c0 + pair, c0 + pair + 2, ...
   const int ptid = tid & 63;              // thread index within the pair
   const int tw = (warp & 1) * 16 + (lane >> 4) * 8;   // this lane's first token
   const int ew = 4 * (lane & 15);                     // this lane's first expert (+64)
+  const int nchunks = H / kTileK;
+  const long long Q = (long long)((T + kTileT - 1) / kTileT) * nchunks;
+  long long q = (long long)blockIdx.x * Q / G;
+  const long long q_end = (long long)(blockIdx.x + 1) * Q / G;
 
   // staging of one chunk by the 64 threads of a pair: x 32x32 (128 vectors,
   // 2 per thread), w 128x32 (512 vectors, 8 per thread); vector v covers row
   // v % rows and columns 8*(v / rows) .. +7 (consecutive lanes -> consecutive
-  // rows: the transposed stores hit 32 distinct banks)
+  // rows: the transposed stores hit distinct banks)
   uint4 rx[2], rw[8];
-  float sqacc[2] = {0.f, 0.f};   // squares of the staged x values, per vector slot
-  auto load_chunk = [&](int kc) {
+  float sqacc[2];   // squares of the staged x values, per vector slot
+  auto load_chunk = [&](int t0, int kc) {
     const int k0 = kc * kTileK;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -815,7 +856,7 @@ __global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
       const int t = t0 + row;
       rx[i] = (t < T) ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + col) : make_uint4(0, 0, 0, 0);
     }
-    if (x16) {   // the f16 copy of the token rows (each vector is loaded once per CTA)
+    if (x16) {   // the f16 copy of the token rows (each vector is loaded once in the launch)
       bool bad = false;
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -836,17 +877,17 @@ __global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
   };
   auto store_chunk = [&](int buf) {
     float* xb = tiles + (size_t)(pair * 2 + buf) * kTileBuf;
-    float* wb = xb + kTileK * kTileT;
+    float* wb = xb + kTileXF;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int v = ptid + 64 * i;
       const int row = v % kTileT, col = (v / kTileT) * 8;
       const uint32_t u[4] = {rx[i].x, rx[i].y, rx[i].z, rx[i].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float lo = bf16lo(u[q]), hi = bf16hi(u[q]);
-        xb[(col + 2 * q) * kTileT + row] = lo;
-        xb[(col + 2 * q + 1) * kTileT + row] = hi;
+      for (int m = 0; m < 4; ++m) {
+        const float lo = bf16lo(u[m]), hi = bf16hi(u[m]);
+        *reinterpret_cast<float2*>(xb + 2 * ((col + 2 * m) * kTileT + row)) = make_float2(lo, lo);
+        *reinterpret_cast<float2*>(xb + 2 * ((col + 2 * m + 1) * kTileT + row)) = make_float2(hi, hi);
         sqacc[i] = fmaf(lo, lo, sqacc[i]);
         sqacc[i] = fmaf(hi, hi, sqacc[i]);
       }
@@ -857,92 +898,109 @@ __global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
       const int row = v % kTileE, col = (v / kTileE) * 8;
       const uint32_t u[4] = {rw[i].x, rw[i].y, rw[i].z, rw[i].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        wb[(col + 2 * q) * kTileE + row] = bf16lo(u[q]);
-        wb[(col + 2 * q + 1) * kTileE + row] = bf16hi(u[q]);
+      for (int m = 0; m < 4; ++m) {
+        wb[(col + 2 * m) * kTileE + row] = bf16lo(u[m]);
+        wb[(col + 2 * m + 1) * kTileE + row] = bf16hi(u[m]);
       }
     }
   };
 
-  float tot[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) tot[i][j] = 0.f;
+  while (q < q_end) {
+    const long long b = q / nchunks;
+    const int c0 = (int)(q - b * nchunks);
+    const int c1 = (int)min((long long)nchunks, c0 + (q_end - q));
+    const int t0 = (int)(b * kTileT);
+    const int piece = (int)(blockIdx.x - tile_cta_of(b * nchunks, Q, G));
+    __syncthreads();   // the previous segment is done with the tiles
 
-  const int nchunks = H / kTileK;
-  int buf = 0;
-  if (pair < nchunks) {
-    load_chunk(pair);
-    store_chunk(0);
-  }
-  named_sync(1 + pair, 64);
-  for (int kc = pair; kc < nchunks; kc += 2) {
-    const bool more = kc + 2 < nchunks;
-    if (more) load_chunk(kc + 2);
-    const float* xb = tiles + (size_t)(pair * 2 + buf) * kTileBuf + tw;
-    const float* wb = tiles + (size_t)(pair * 2 + buf) * kTileBuf + kTileK * kTileT + ew;
-    float part[8][8];
+    float2 tot[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) part[i][j] = 0.f;
-#pragma unroll 4
-    for (int kk = 0; kk < kTileK; ++kk) {
-      const float4 xa = *reinterpret_cast<const float4*>(xb + kk * kTileT);
-      const float4 xc = *reinterpret_cast<const float4*>(xb + kk * kTileT + 4);
-      const float4 wa = *reinterpret_cast<const float4*>(wb + kk * kTileE);
-      const float4 wc = *reinterpret_cast<const float4*>(wb + kk * kTileE + 64);
-      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
-      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wc.x, wc.y, wc.z, wc.w};
+      for (int j = 0; j < 4; ++j) tot[i][j] = make_float2(0.f, 0.f);
+    sqacc[0] = sqacc[1] = 0.f;
+    int buf = 0;
+    if (c0 + pair < c1) {
+      load_chunk(t0, c0 + pair);
+      store_chunk(0);
+    }
+    named_sync(1 + pair, 64);
+    for (int kc = c0 + pair; kc < c1; kc += 2) {
+      const bool more = kc + 2 < c1;
+      if (more) load_chunk(t0, kc + 2);
+      const float* xb = tiles + (size_t)(pair * 2 + buf) * kTileBuf + 2 * tw;
+      const float* wb = tiles + (size_t)(pair * 2 + buf) * kTileBuf + kTileXF + ew;
+      float2 part[8][4];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
+        for (int j = 0; j < 4; ++j) part[i][j] = make_float2(0.f, 0.f);
+#pragma unroll 4
+      for (int kk = 0; kk < kTileK; ++kk) {
+        float4 xv[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) xv[m] = *reinterpret_cast<const float4*>(xb + 2 * kk * kTileT + 4 * m);
+        const float4 wa = *reinterpret_cast<const float4*>(wb + kk * kTileE);
+        const float4 wc = *reinterpret_cast<const float4*>(wb + kk * kTileE + 64);
+        const float2 wp[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w), make_float2(wc.x, wc.y),
+                              make_float2(wc.z, wc.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 xi = (i & 1) ? make_float2(xv[i / 2].z, xv[i / 2].w) : make_float2(xv[i / 2].x, xv[i / 2].y);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) part[i][j] = fma_f32x2(xi, wp[j], part[i][j]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tot[i][j] = add_f32x2(tot[i][j], part[i][j]);
+      if (more) store_chunk(buf ^ 1);
+      named_sync(1 + pair, 64);
+      buf ^= 1;
+    }
+    __syncthreads();   // both pairs are done with their tiles
+    // pair 1 hands its totals to pair 0 (through the tile memory), which adds
+    // them once and stores the piece
+    float* xfer = tiles;   // [64 threads][64]
+    if (pair == 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xfer[(i * 8 + 2 * j) * 64 + ptid] = tot[i][j].x;
+          xfer[(i * 8 + 2 * j + 1) * 64 + ptid] = tot[i][j].y;
+        }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 2; ++i) s_sq[pair][ptid + 64 * i] = sqacc[i];
+    __syncthreads();
+    if (pair == 0) {
+      float* dst = lpart + (size_t)piece * T * E;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) tot[i][j] += part[i][j];
-    if (more) store_chunk(buf ^ 1);
-    named_sync(1 + pair, 64);
-    buf ^= 1;
-  }
-  __syncthreads();   // both pairs are done with their tiles
-  // pair 1 hands its totals to pair 0 (through the tile memory), which adds
-  // them once and writes the logits
-  float* xfer = tiles;   // [64 threads][64]
-  if (pair == 1) {
+      for (int i = 0; i < 8; ++i) {
+        const int t = t0 + tw + i;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) xfer[(i * 8 + j) * 64 + ptid] = tot[i][j];
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) s_sq[pair][ptid + 64 * i] = sqacc[i];
-  __syncthreads();
-  if (pair == 0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = t0 + tw + i;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float v = tot[i][j] + xfer[(i * 8 + j) * 64 + ptid];
-        const int e = (j < 4 ? 0 : 64) + ew + (j & 3);
-        if (t < T && e < E) logits[(size_t)t * E + e] = bias ? v + bias[e] : v;
+        for (int j = 0; j < 4; ++j) {
+          const int e = (j < 2 ? 0 : 64) + ew + 2 * (j & 1);
+          const float v0 = tot[i][j].x + xfer[(i * 8 + 2 * j) * 64 + ptid];
+          const float v1 = tot[i][j].y + xfer[(i * 8 + 2 * j + 1) * 64 + ptid];
+          if (t < T && e < E) dst[(size_t)t * E + e] = v0;
+          if (t < T && e + 1 < E) dst[(size_t)t * E + e + 1] = v1;
+        }
       }
     }
-  }
-  // ||x_t||: row t's partials are the vector slots v = t + 32c (c = 0..3) of
-  // both pairs, added in a fixed order (any order serves the error bound,
-  // which allows for the norm's own rounding)
-  if (tid < kTileT && t0 + tid < T) {
-    float sq = 0.f;
+    // ||x_t||^2 over the segment: row t's partials are the vector slots
+    // v = t + 32c (c = 0..3) of both pairs
+    if (tid < kTileT && t0 + tid < T) {
+      float sq = 0.f;
 #pragma unroll
-    for (int p2 = 0; p2 < 2; ++p2)
+      for (int p2 = 0; p2 < 2; ++p2)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) sq += s_sq[p2][tid + kTileT * c];
-    xnorm[t0 + tid] = sqrtf(sq);
+        for (int c = 0; c < 4; ++c) sq += s_sq[p2][tid + kTileT * c];
+      xsq[(size_t)piece * T + t0 + tid] = sq;
+    }
+    q += c1 - c0;
   }
 }
 
@@ -951,8 +1009,8 @@ __global__ void __launch_bounds__(kTileThreads) router_tile_kernel(
 // and ranked from registers.
 __global__ void __launch_bounds__(256, 3) router_select_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
-    int T, int H, int E, int k, float gamma, const float* __restrict__ logits,
-    const float* __restrict__ xnorm, const float* __restrict__ wnorm, double* __restrict__ l64,
+    int T, int H, int E, int k, float gamma, const float* __restrict__ lpart,
+    const float* __restrict__ xsq, int G, const float* __restrict__ wnorm, double* __restrict__ l64,
     int32_t* __restrict__ idx, float* __restrict__ w, void* ws) {
   pdl_wait();   // the logits and norms are complete
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -963,14 +1021,35 @@ __global__ void __launch_bounds__(256, 3) router_select_kernel(
   const int nt = min(8, T - t0);
   const int t = t0 + warp;
   if (warp < nt) {
+    // the token block's pieces (slot order), then the bias
+    const int nchunks = H / kTileK;
+    const long long Q = (long long)((T + kTileT - 1) / kTileT) * nchunks;
+    const long long qb = (long long)(t / kTileT) * nchunks;
+    const int np = (int)(tile_cta_of(qb + nchunks - 1, Q, G) - tile_cta_of(qb, Q, G)) + 1;
     float v[4], wn[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int e = lane + 32 * i;
-      v[i] = e < E ? logits[(size_t)t * E + e] : 0.0f;
+      v[i] = e < E ? lpart[(size_t)t * E + e] : 0.0f;
       wn[i] = e < E ? wnorm[e] : 0.0f;
     }
-    const float xn = xnorm[t];
+    float xs = xsq[t];
+    for (int p = 1; p < np; ++p) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) v[i] += lpart[((size_t)p * T + t) * E + e];
+      }
+      xs += xsq[(size_t)p * T + t];
+    }
+    if (bias) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) v[i] += bias[e];
+      }
+    }
+    const float xn = sqrtf(xs);
     float wmax = 0.f, lmax = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -1032,27 +1111,41 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* gate_w, const float*
                          cudaStream_t stream, int* launches, const GroupOut* group, uint16_t* x16) {
   float* wnorm = ws_ptr<float>(ws, L.wnorm);
   double* l64 = ws_ptr<double>(ws, L.logits64);
-  const bool tiled = T >= 2048 && E <= kTileE;
+  const bool tiled = route_tiled(T, E);
   if (launches) *launches += tiled ? 3 : 1;
   if (tiled) {
-    float* logits = ws_ptr<float>(ws, L.logits);
-    float* xnorm = ws_ptr<float>(ws, L.xnorm);
+    static_assert(kTilePieces == kRouteTilePieces && kTileE == kRouteTileMaxE, "workspace pieces");
+    float* lpart = ws_ptr<float>(ws, L.lpart);
+    float* xsq = ws_ptr<float>(ws, L.xsq);
     cudaError_t err = launch_pdl(wnorm_kernel, dim3((E + 7) / 8), dim3(256), 0, stream, gate_w, H, E, wnorm);
     if (err != cudaSuccess) return err;
-    const size_t smem = sizeof(float) * 4 * kTileBuf;
-    err = cudaFuncSetAttribute(router_tile_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int dev = 0, sms = 0;
+    err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(router_tile_kernel, dim3((T + kTileT - 1) / kTileT), dim3(kTileThreads), smem, stream, x,
-                     gate_w, bias, T, H, E, logits, xnorm, x16, &reinterpret_cast<WsHeader*>(ws)->status);
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    // two CTAs per SM; at least ceil((nchunks - 1) / (kTilePieces - 1)) items
+    // per CTA, so that no block has more than kTilePieces pieces
+    const int nchunks = H / kTileK;
+    const long long Q = (long long)((T + kTileT - 1) / kTileT) * nchunks;
+    const long long per_min = std::max(1, (nchunks - 1 + kTilePieces - 2) / (kTilePieces - 1));
+    long long G = std::max(1LL, std::min(2LL * sms, Q / per_min));
+    if (G > sms && G < 2LL * sms) G = sms;   // whole CTAs per SM: one each rather than one or two
+    const size_t smem = sizeof(float) * 4 * kTileBuf;
+    err = cudaFuncSetAttribute(router_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(router_tile_kernel, dim3((unsigned)G), dim3(kTileThreads), smem, stream, x, gate_w, T, H, E, (int)G,
+                     lpart, xsq, x16, &reinterpret_cast<WsHeader*>(ws)->status);
     if (err != cudaSuccess) return err;
     const size_t smem2 = sizeof(WarpScratch) * 8;
     err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem2);
     if (err != cudaSuccess) return err;
-    const float gamma = gamma_bound(kTileK + H / kTileK + 1);
+    // roundings per product: chunk sum, a pair's chunk sums, the pair
+    // totals, the pieces
+    const float gamma = gamma_bound(kTileK - 1 + (nchunks + 1) / 2 + 1 + (kTilePieces - 1));
     return launch_pdl(router_select_kernel, dim3((T + 7) / 8), dim3(256), smem2, stream, x, gate_w, bias, T, H,
-                      E, k, gamma, (const float*)logits, (const float*)xnorm, (const float*)wnorm, l64, idx, w,
+                      E, k, gamma, (const float*)lpart, (const float*)xsq, (int)G, (const float*)wnorm, l64, idx, w,
                       ws);
   }
   const int tt = T <= 16 ? 1 : T <= 128 ? 4 : 8;
