@@ -147,8 +147,12 @@ __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster)
       : "memory");
 }
+// Relaxed: the arrive orders nothing but the caller's completed tensor-memory
+// loads (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync), so it need
+// not wait for the caller's earlier global stores to become visible in the
+// cluster (which a release arrive does, stalling the epilogue on every tile).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
 }
 // arrive (once the issuing thread's earlier MMAs complete) on the mbarrier at
