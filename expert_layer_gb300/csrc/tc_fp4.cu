@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[b]);
+      if (lane == 0) mbar_arrive_relaxed(&tempty[b]);   // the accumulator reads are complete
       if (*(volatile int*)abort_flag) break;
     }
   }

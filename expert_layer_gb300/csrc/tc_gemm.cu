@@ -292,6 +292,42 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const int q = warp & 3;
     const int hc = (warp - 2) >> 2;
     const uint32_t tempty0[2] = {map_to_rank(&tempty[0], 0), map_to_rank(&tempty[1], 0)};
+    // down: slots and routing weights of this warp's columns (lane c of chunk
+    // i: token 32(kEpiSets i + hc) + c), one tile ahead: the next tile's slot
+    // ids are requested before this tile's accumulator wait and its routing
+    // weights after this tile's stores, so neither load waits on the tile
+    auto tile_cols = [&](int p, int& off0, int& nc) {
+      const TileInfo t2 = decode_tile(md, md.tiles, nlarge, NW, p);
+      const int r0 = t2.mtile * 2 * kPairRows;
+      const int rem2 = t2.m - r0;
+      const int n2 = pair_n(rem2);
+      off0 = t2.off + r0;
+      nc = rem2 < n2 ? rem2 : n2;
+    };
+    int nc_next = 0;   // token columns of the next tile
+    auto load_slots = [&](int p, int (&f)[kEpiChunks]) {
+      int off0;
+      tile_cols(p, off0, nc_next);
+#pragma unroll
+      for (int i = 0; i < kEpiChunks; ++i) {
+        const int c = 32 * (kEpiSets * i + hc) + lane;
+        f[i] = c < nc_next ? __ldg(&a.perm[off0 + c]) : 0;
+      }
+    };
+    auto load_weights = [&](int (&f)[kEpiChunks], float (&w)[kEpiChunks]) {
+#pragma unroll
+      for (int i = 0; i < kEpiChunks; ++i) {
+        const int c = 32 * (kEpiSets * i + hc) + lane;
+        if (!bounds_ok((unsigned)f[i] < (unsigned)(a.T * a.k), a.status)) f[i] = 0;
+        w[i] = c < nc_next ? __ldg(&a.topk_w[f[i]]) : 0.f;
+      }
+    };
+    int fl_next[kEpiChunks];
+    float wl_next[kEpiChunks];
+    if (kDown && cid < total) {
+      load_slots(cid, fl_next);
+      load_weights(fl_next, wl_next);
+    }
     uint32_t lt = 0;
     for (int p = cid; p < total; p += ncl, ++lt) {
       const uint32_t b = lt & 1;
@@ -301,18 +337,15 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       const int rem = ti.m - tok0;                   // token rows left in the group (> 0)
       const int n = pair_n(rem);
       const int ncols = rem < n ? rem : n;           // token columns to store
-      // down: slots and routing weights of this warp's columns (lane c of
-      // chunk i: token 32(kEpiSets i + hc) + c), fetched before the accumulator wait
       int fl[kEpiChunks];
       float wl[kEpiChunks];
       if (kDown) {
 #pragma unroll
         for (int i = 0; i < kEpiChunks; ++i) {
-          const int c = 32 * (kEpiSets * i + hc) + lane;
-          fl[i] = c < ncols ? __ldg(&a.perm[ti.off + tok0 + c]) : 0;
-          if (!bounds_ok((unsigned)fl[i] < (unsigned)(a.T * a.k), a.status)) fl[i] = 0;
-          wl[i] = c < ncols ? __ldg(&a.topk_w[fl[i]]) : 0.f;
+          fl[i] = fl_next[i];
+          wl[i] = wl_next[i];
         }
+        if (p + ncl < total) load_slots(p + ncl, fl_next);
       }
       if (!warp_wait(&tfull[b], tph)) { atomicOr(abort_flag, 1); break; }
       tc_fence_after();
@@ -343,10 +376,16 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           }
         } else {
           const int d = ti.ntile * 2 * kPairRows + (int)rank * kPairRows + 32 * q + lane;
+          // this chunk's slot and weight (selected, not indexed: no local memory)
+          int fi = fl[0];
+          float wi = wl[0];
+#pragma unroll
+          for (int j = 1; j < kEpiChunks; ++j)
+            if (i == j) fi = fl[j], wi = wl[j];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int f = __shfl_sync(0xffffffffu, fl[i], c);
-            const float w = __shfl_sync(0xffffffffu, wl[i], c);
+            const int f = __shfl_sync(0xffffffffu, fi, c);
+            const float w = __shfl_sync(0xffffffffu, wi, c);
             if (c0 + c < ncols) {
               const float val = w * __uint_as_float(y[c]);
               const size_t o = (size_t)f * a.H + d;
@@ -356,6 +395,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           }
         }
       }
+      if (kDown && p + ncl < total) load_weights(fl_next, wl_next);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty0[b]);
