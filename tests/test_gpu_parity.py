@@ -202,12 +202,16 @@ def test_all_tokens_one_expert():
     gh.check_output(inp, out, orc)
 
 
-@pytest.mark.parametrize("T", [2304, 5000])
-def test_large_router_path(T):
-    """T >= 2048 uses the token-tiled router and the multi-block grouping
-    (T = 5000 spreads the tokens over CTAs of fewer than 32, with a ragged
-    last CTA)."""
-    inp = _small(T, 256, 64, 4, 128, bias="zipf")
+@pytest.mark.parametrize("T,H,E", [(2304, 256, 64), (5000, 256, 64), (2085, 1280, 100), (4100, 2048, 128)])
+def test_large_router_path(T, H, E):
+    """T >= 2048 uses the token-tiled router (stream-K over (32-token block,
+    K chunk) items: a block's logits arrive in up to four pieces that the
+    select kernel adds) and the multi-block grouping.  The cases cover ragged
+    last token blocks (5000, 2085, 4100), blocks of two, three and four
+    pieces on a 152-SM device (H = 1280 and 2048 reach four), pieces that
+    split a block mid-way at the layer's own H, and an expert count that ends
+    inside a lane's group of four (E = 100)."""
+    inp = _small(T, H, E, 4, 128, bias="zipf")
     idx, w = moe.route(inp.x, inp.gate_w, inp.bias, inp.top_k)
     counts, offsets, perm, inv = moe.permute(idx, inp.E)
     torch.cuda.synchronize()
