@@ -146,6 +146,58 @@ def measured_traffic(workload: str, stage: str):
     return None
 
 
+class Cudart:
+    """The few CUDA runtime calls of the end-to-end loop (async copies, event
+    record / wait), called through ctypes: per step they cost a few
+    microseconds of host time, where the same calls through torch's stream
+    and event wrappers cost ~40 us, more than a small workload's step."""
+
+    H2D, D2H = 1, 2
+
+    def __init__(self):
+        import ctypes
+        import ctypes.util
+        names = [ctypes.util.find_library("cudart"), "libcudart.so.13", "libcudart.so",
+                 "/usr/local/cuda/lib64/libcudart.so"]
+        self.lib = None
+        for n in names:
+            if not n:
+                continue
+            try:
+                self.lib = ctypes.CDLL(n)
+                break
+            except OSError:
+                continue
+        if self.lib is None:
+            raise OSError("CUDA runtime library not found")
+        c = ctypes
+        L = self.lib
+        L.cudaMemcpyAsync.argtypes = [c.c_void_p, c.c_void_p, c.c_size_t, c.c_int, c.c_void_p]
+        L.cudaEventCreateWithFlags.argtypes = [c.POINTER(c.c_void_p), c.c_uint]
+        L.cudaEventRecord.argtypes = [c.c_void_p, c.c_void_p]
+        L.cudaStreamWaitEvent.argtypes = [c.c_void_p, c.c_void_p, c.c_uint]
+        L.cudaEventDestroy.argtypes = [c.c_void_p]
+        self.c = c
+
+    def check(self, rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} failed with CUDA error {rc}")
+
+    def event(self):
+        ev = self.c.c_void_p()
+        self.check(self.lib.cudaEventCreateWithFlags(self.c.byref(ev), 2), "cudaEventCreateWithFlags")  # no timing
+        return ev
+
+    def copy(self, dst, src, nbytes, kind, stream):
+        self.check(self.lib.cudaMemcpyAsync(dst, src, nbytes, kind, stream), "cudaMemcpyAsync")
+
+    def record(self, ev, stream):
+        self.check(self.lib.cudaEventRecord(ev, stream), "cudaEventRecord")
+
+    def wait(self, stream, ev):
+        self.check(self.lib.cudaStreamWaitEvent(stream, ev, 0), "cudaStreamWaitEvent")
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -675,31 +727,61 @@ def measure(name, args, ctx, headline):
         ctx["dist"].barrier()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
+    try:
+        rt = Cudart()
+    except OSError:
+        rt = None
     f0.record(stream)
     h2d_s.wait_stream(stream)
     d2h_s.wait_stream(stream)
-    for i in range(K):
-        b = i % 2
-        with torch.cuda.stream(h2d_s):
+    if rt is not None:
+        # the same loop on raw handles (torch's streams, runtime events)
+        cs, hs, ds = P(stream.cuda_stream), P(h2d_s.cuda_stream), P(d2h_s.cuda_stream)
+        ev_ready = [rt.event() for _ in range(2)]
+        ev_used = [rt.event() for _ in range(2)]
+        ev_read = [rt.event() for _ in range(2)]
+        xh_p, oh_p = P(x_h.data_ptr()), [P(t.data_ptr()) for t in out_h]
+        xb, ob = x_h.numel() * x_h.element_size(), o_d[0].numel() * o_d[0].element_size()
+        for i in range(K):
+            b = i % 2
             if i >= 2:
-                h2d_s.wait_event(used[b])   # step i-2 has read x_d[b]
-            x_d[b].copy_(x_h, non_blocking=True)
-            ready[b].record(h2d_s)
-        stream.wait_event(ready[b])
-        if i >= 2:
-            stream.wait_event(read[b])      # step i-2's result has left o_d[b]
-        step(i, xp=xd_p[b], op=od_p[b])
-        used[b].record(stream)
-        with torch.cuda.stream(d2h_s):
-            d2h_s.wait_event(used[b])
-            out_h[b].copy_(o_d[b], non_blocking=True)
-            read[b].record(d2h_s)
+                rt.wait(hs, ev_used[b])     # step i-2 has read x_d[b]
+            rt.copy(xd_p[b], xh_p, xb, Cudart.H2D, hs)
+            rt.record(ev_ready[b], hs)
+            rt.wait(cs, ev_ready[b])
+            if i >= 2:
+                rt.wait(cs, ev_read[b])     # step i-2's result has left o_d[b]
+            step(i, xp=xd_p[b], op=od_p[b])
+            rt.record(ev_used[b], cs)
+            rt.wait(ds, ev_used[b])
+            rt.copy(oh_p[b], od_p[b], ob, Cudart.D2H, ds)
+            rt.record(ev_read[b], ds)
+    else:
+        for i in range(K):
+            b = i % 2
+            with torch.cuda.stream(h2d_s):
+                if i >= 2:
+                    h2d_s.wait_event(used[b])   # step i-2 has read x_d[b]
+                x_d[b].copy_(x_h, non_blocking=True)
+                ready[b].record(h2d_s)
+            stream.wait_event(ready[b])
+            if i >= 2:
+                stream.wait_event(read[b])      # step i-2's result has left o_d[b]
+            step(i, xp=xd_p[b], op=od_p[b])
+            used[b].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(used[b])
+                out_h[b].copy_(o_d[b], non_blocking=True)
+                read[b].record(d2h_s)
     stream.wait_stream(h2d_s)
     stream.wait_stream(d2h_s)
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
     e2e_value = job_tokens_per_s(world, K, T, e2e_ms)
+    if rt is not None:
+        for ev in ev_ready + ev_used + ev_read:
+            rt.lib.cudaEventDestroy(ev)
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
