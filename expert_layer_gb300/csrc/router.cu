@@ -1004,9 +1004,11 @@ __global__ void __launch_bounds__(kTileThreads, 2) router_tile_kernel(
   }
 }
 
-// Selection for the tiled path (E <= 128): one warp per token, whose logits,
-// expert norms and ||x_t|| are loaded in one batch (lane l: experts l + 32i)
-// and ranked from registers.
+// Selection for the tiled path (E <= 128): one warp per token.  The token's
+// logits are the sum of its block's stream-K pieces in slot order (then the
+// bias), ||x_t|| the root of its pieces' partial squares; logits and expert
+// norms are loaded in one batch (lane l: experts l + 32i) and ranked from
+// registers.
 __global__ void __launch_bounds__(256, 3) router_select_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw, const float* __restrict__ bias,
     int T, int H, int E, int k, float gamma, const float* __restrict__ lpart,
