@@ -57,6 +57,24 @@ def test_workspace_size(lib):
     assert moe.workspace_size(-1, 2048, 128, 768, 8) == 0
 
 
+def test_workspace_holds_the_tiled_router_pieces(lib):
+    """From T = 2048 (E <= 128) the router's logits come in up to four
+    stream-K pieces per token block, each with partial squares of x: the
+    workspace grows by at least 4*T*E + 4*T floats at that step, beyond what
+    one more token costs anywhere else."""
+    for E in (32, 128):
+        below = moe.workspace_size(2047, 2048, E, 768, 8)
+        at = moe.workspace_size(2048, 2048, E, 768, 8)
+        per_token = moe.workspace_size(2047, 2048, E, 768, 8) - moe.workspace_size(2046, 2048, E, 768, 8)
+        # two 256-byte-aligned regions: up to 2 x 255 bytes of padding may be absorbed
+        assert at - below - per_token >= 4 * (4 * 2048 * E + 4 * 2048) - 2 * 256
+    # more than 128 experts keeps the small-batch router: no pieces
+    below = moe.workspace_size(2047, 2048, 256, 768, 8)
+    at = moe.workspace_size(2048, 2048, 256, 768, 8)
+    per_token = below - moe.workspace_size(2046, 2048, 256, 768, 8)
+    assert at - below <= per_token + 4 * 256
+
+
 P = ctypes.c_void_p
 
 
